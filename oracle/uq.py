@@ -1,0 +1,101 @@
+"""UltraQuant head_dim=256 4-bit decode: slot decode, Q rotation, attention,
+un-rotation.
+
+TEST INFRASTRUCTURE (see the package header).
+
+Slot ([UQ] builder docstring and STEP F addressing): the cache is
+``[num_blocks][bs][Hk][padded_slot]`` uint8; per (token, KV head) the slot
+holds K e2m1 codes in bytes 0..127, K scales in 128..135 (one per 32 dims),
+V codes in 136..263 and V scales in 264..271. Dim 2i is the low nibble of
+code byte i.
+
+Dequantisation (readings of the pages, listed in the design notes):
+  K[d] = e2m1(code) * e4m3(kscale[d // 32])
+  V[d] = centroid[code] * e4m3(vscale[d // 32])     (16-entry fp32 table)
+The page prints UE8M0 scales and an e2m1 V convert; the e2m1 table as the
+centroid table reproduces that V path, and ``scale_format='ue8m0'`` selects
+the page's scale decode.
+
+Rotation ([UQ] STEP B'): the cached K and V live in the domain rotated by
+the orthonormal Sylvester-Hadamard matrix R = H_256 / 16, H[i][j] =
+(-1)^popcount(i & j); R is symmetric and its own inverse. Q is rotated with
+the same R, attention runs in the rotated domain with scale 1/sqrt(256)
+(the builder's default softmax scale), and the output is rotated back:
+o = softmax(scale q_r K_r^T) V_r R.
+
+Pins (tests/test_oracle_uq.py): R R^T = I, R = R^T, R R = I, the +-1 entries
+against the recursive Sylvester construction, a fast butterfly transform
+against R to within the fp32 difference the page reports (1.8e-6); a
+hand-built slot against its expected dequantised vector (tests/golden); the
+page's 81.6 MB slot byte count at B=4, seq 75k, one KV head; the whole
+rotated pipeline against plain attention on the logical K = K_r R,
+V = V_r R.
+"""
+import math
+
+import numpy as np
+
+from .attention import attend, gather_tokens
+from .formats import decode_bf16, decode_e2m1, decode_e4m3fn, decode_ue8m0, unpack_nibbles
+
+HEAD = 256
+K_CODES, K_SCALES, V_CODES, V_SCALES, CONTENT = 0, 128, 136, 264, 272
+GROUP = 32
+
+
+def wht_matrix(n: int = HEAD) -> np.ndarray:
+    """Orthonormal Sylvester-Hadamard matrix, entry (i, j) = (-1)^popcount(i&j)
+    / sqrt(n)."""
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    x = i & j
+    parity = np.zeros_like(x)
+    while np.any(x):
+        parity ^= x & 1
+        x = x >> 1
+    return np.where(parity == 1, -1.0, 1.0) / math.sqrt(n)
+
+
+def decode_uq_slots(slots: np.ndarray, centroids, scale_format: str = "e4m3"):
+    """slots [..., >=272] uint8 -> (K [..., 256], V [..., 256]) float64."""
+    s = np.asarray(slots, dtype=np.uint8)
+    dec = decode_e4m3fn if scale_format == "e4m3" else decode_ue8m0
+    kcode = unpack_nibbles(s[..., K_CODES:K_SCALES])
+    vcode = unpack_nibbles(s[..., V_CODES:V_SCALES])
+    ks = np.repeat(dec(s[..., K_SCALES:V_CODES]), GROUP, axis=-1)
+    vs = np.repeat(dec(s[..., V_SCALES:CONTENT]), GROUP, axis=-1)
+    cent = np.asarray(centroids, dtype=np.float32).astype(np.float64)
+    return decode_e2m1(kcode) * ks, cent[vcode] * vs
+
+
+def dense_kv_uq(kv_cache, centroids, block_table, seq, kv_head, L, scale_format="e4m3"):
+    slots = gather_tokens(kv_cache[:, :, kv_head], block_table[seq], L)
+    return decode_uq_slots(slots, centroids, scale_format)
+
+
+def uq_decode_hd256(q_bits, kv_cache, centroids, block_table, seq_lens, query_group: int,
+                    softmax_scale: float | None = None, units=None,
+                    scale_format: str = "e4m3") -> np.ndarray:
+    """Reference output [B, Hq, 256] in the un-rotated (logical) domain.
+
+    q_bits [B, Hq, 256] uint16 bf16 bits (un-rotated); kv_cache [NB, bs, Hk,
+    padded_slot] uint8; centroids [16] float32."""
+    q = decode_bf16(q_bits)
+    B, Hq, D = q.shape
+    assert D == HEAD
+    Hk = kv_cache.shape[2]
+    assert Hq == Hk * query_group
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(HEAD)
+    R = wht_matrix(HEAD)
+    out = np.zeros((B, Hq, D))
+    if units is None:
+        units = [(s, h) for s in range(B) for h in range(Hk)]
+    for s, h in units:
+        L = int(seq_lens[s])
+        k_r, v_r = dense_kv_uq(kv_cache, centroids, block_table, s, h, L, scale_format)
+        rows = slice(h * query_group, (h + 1) * query_group)
+        q_r = q[s, rows] @ R
+        o_r = attend(q_r, k_r, v_r, softmax_scale)
+        out[s, rows] = o_r @ R
+    return out
