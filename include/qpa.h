@@ -1,0 +1,139 @@
+/*
+ * qpa.h -- quantised paged-attention decode for NVIDIA GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels. Every entry point takes plain
+ * pointers and sizes, enqueues its kernels on the caller's stream and returns
+ * without synchronising. The caller owns every buffer (inputs, outputs and
+ * the workspace that holds per-partition partial results); the library
+ * allocates nothing and keeps no state between calls, so a call may be
+ * captured in a CUDA graph and made from any host thread.
+ *
+ * Sources the operations follow (web pages, cited by title and section):
+ *   [PA]  ROCm/FlyDSL PR #825, "perf(pa tile): readable tile-programming PA
+ *         decode kernel" -- fp8 per-tensor paged decode, its partition split,
+ *         the flash-combine reduce kernel and the caller-preallocated
+ *         partials used under CUDA-graph capture.
+ *   [UQ]  vLLM API docs, vllm/v1/attention/ops/flydsl_kernels/
+ *         ultraquant_decode_hd256 (PR 59857) -- the 4-bit head_dim=256 slot
+ *         cache with in-kernel Walsh-Hadamard rotation of Q (steps A..G).
+ *   [IDX] vLLM API docs, vllm/models/minimax_m3/amd/ops/nvfp4_index_decode/
+ *         kernel (PR 59747) -- the paged NVFP4 index scorer.
+ *
+ * Errors: every call returns QPA_OK (0) or a negative status. Argument
+ * problems are found on the host before anything is enqueued (no device data
+ * is read on the host). QPA_ERR_CUDA reports a launch error from the CUDA
+ * runtime. A kernel that meets an invalid block id (outside
+ * [0, num_blocks)) reads block 0 instead and raises a device error word;
+ * qpa_kernel_error() reads it.
+ */
+#ifndef QPA_H
+#define QPA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QPA_OK 0
+#define QPA_ERR_NULL (-1)        /* a required pointer is NULL */
+#define QPA_ERR_SHAPE (-2)       /* unsupported head_dim / group / block size / sizes */
+#define QPA_ERR_ALIGN (-3)       /* a pointer or stride breaks the 16-byte rule */
+#define QPA_ERR_WORKSPACE (-4)   /* workspace smaller than *_workspace_size() */
+#define QPA_ERR_PARTITIONS (-5)  /* num_partitions < 1 */
+#define QPA_ERR_CUDA (-6)        /* the CUDA runtime rejected a launch */
+
+#define QPA_OUT_F32 0
+#define QPA_OUT_BF16 1
+
+/* Returns a static string naming a status code. */
+const char* qpa_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int qpa_version(void);
+
+/* Synchronises `stream` (a cudaStream_t, NULL = legacy default stream), then
+ * returns and clears the device error word of the current device: 0 when no
+ * kernel reported a problem, otherwise a positive code (1, 2: a wait gave up
+ * after its time limit; 3: an invalid block id was met). Returns QPA_ERR_CUDA
+ * if the synchronisation fails. Diagnostic only; the decode entry points
+ * never call it. */
+int qpa_kernel_error(void* stream);
+
+/* ========================================================================
+ * fp8 paged-attention decode ([PA]; partition map from [UQ] step F)
+ *
+ * For every sequence s (length L = seq_lens[s]), KV head h and query row g
+ * (query head h*query_group + g):
+ *     out = sum_t softmax_t(softmax_scale * q . k_t) v_t,   t = 0 .. L-1,
+ *     k_t = e4m3fn(K byte) * (*k_scale),  v_t = e4m3fn(V byte) * (*v_scale).
+ * The work is split over num_partitions partitions per (s, h): partition p
+ * owns the 256-token tile groups p, p+P, p+2P, ... and writes (m_p, l_p,
+ * O_p) to the workspace; the combine kernel merges them. Any P >= 1 gives the
+ * same result (up to rounding); a partition with no tokens contributes
+ * nothing. L = 0 gives 0. There is no cap on tile groups per partition.
+ *
+ * Layouts (row-major, element counts in brackets):
+ *   q           bf16  [num_seqs][num_kv_heads*query_group][128] with the
+ *               strides of the descriptor (elements; a multiple of 8), so a
+ *               slice of a fused QKV projection can be passed directly.
+ *   kv_cache    uint8 [num_blocks][2 (K, V)][num_kv_heads][block_size][128]
+ *               e4m3fn bytes; each (block, K/V, head) chunk is contiguous.
+ *   block_table int32 [num_seqs][max_blocks_per_seq]; token t of sequence s
+ *               is slot t % block_size of block block_table[s][t/block_size].
+ *               Only entries below ceil(L/block_size) are read.
+ *   seq_lens    int32 [num_seqs]; values are clamped to
+ *               [0, max_blocks_per_seq*block_size] on the device.
+ *   k_scale,    float [1] each, on the device (read by the kernels).
+ *   v_scale
+ *   out         [num_seqs][num_kv_heads*query_group][128], float32 or bf16
+ *               per out_dtype, contiguous.
+ *   workspace   device memory of pa_decode_fp8_workspace_size() bytes,
+ *               256-byte aligned; its contents need no initialisation. It
+ *               holds, at 256-byte-aligned offsets, float32
+ *               O [num_seqs][num_kv_heads][P][query_group][128],
+ *               m [num_seqs][num_kv_heads][P][query_group] (max scaled logit,
+ *               natural-log units, -inf for an empty partition) and
+ *               l [num_seqs][num_kv_heads][P][query_group]
+ *               (sum of exp(logit - m)); O is normalised by l and already
+ *               multiplied by v_scale.
+ * Supported: head_dim 128, query_group 1..16, block_size 16/32/64/128/256.
+ * Alignment: q, kv_cache and out 16-byte aligned.
+ * ====================================================================== */
+typedef struct qpa_fp8_desc {
+  int32_t num_seqs;
+  int32_t num_kv_heads;
+  int32_t query_group;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t out_dtype;        /* QPA_OUT_F32 or QPA_OUT_BF16 */
+  int64_t q_stride_seq;     /* elements; 0 = num_kv_heads*query_group*head_dim */
+  int64_t q_stride_head;    /* elements; 0 = head_dim */
+  float softmax_scale;      /* 0 = 1/sqrt(head_dim) */
+} qpa_fp8_desc;
+
+size_t pa_decode_fp8_workspace_size(const qpa_fp8_desc* d, int num_partitions);
+
+/* Whole decode step: partition kernel then combine kernel, on `stream`. */
+int pa_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t* block_table,
+                  const int32_t* seq_lens, const float* k_scale, const float* v_scale,
+                  int num_partitions, void* out, const qpa_fp8_desc* d, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* The two halves of pa_decode_fp8, for callers that time or schedule them
+ * separately. The partition kernel fills the workspace; the combine kernel
+ * reads it and writes `out`. */
+int pa_decode_fp8_partition(const void* q, const uint8_t* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, const float* k_scale, const float* v_scale,
+                            int num_partitions, const qpa_fp8_desc* d, void* workspace,
+                            size_t workspace_bytes, void* stream);
+int pa_decode_fp8_combine(int num_partitions, void* out, const qpa_fp8_desc* d,
+                          const void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QPA_H */

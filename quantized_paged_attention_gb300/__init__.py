@@ -1,0 +1,175 @@
+"""Quantised paged-attention decode for GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI of ``libqpa.so`` (declared in
+``include/qpa.h``). It only marshals arguments: every step of the decode runs
+in the library's CUDA kernels. PyTorch supplies device memory and streams.
+There is no CPU fallback: if the library is missing or a tensor is not on a
+CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqpa.so")
+
+QPA_OK = 0
+QPA_OUT_F32 = 0
+QPA_OUT_BF16 = 1
+_lib = None
+
+
+class QpaError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        msg = _lib.qpa_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{fn} failed: {msg} ({status})")
+
+
+class Fp8Desc(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("query_group", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("q_stride_seq", ctypes.c_int64), ("q_stride_head", ctypes.c_int64),
+                ("softmax_scale", ctypes.c_float)]
+
+
+_P = ctypes.c_void_p
+_SIGS = {
+    "qpa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "qpa_version": (ctypes.c_int, []),
+    "qpa_kernel_error": (ctypes.c_int, [_P]),
+    "pa_decode_fp8_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Fp8Desc), ctypes.c_int]),
+    "pa_decode_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, _P,
+                                     ctypes.POINTER(Fp8Desc), _P, ctypes.c_size_t, _P]),
+    "pa_decode_fp8_partition": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int,
+                                               ctypes.POINTER(Fp8Desc), _P, ctypes.c_size_t, _P]),
+    "pa_decode_fp8_combine": (ctypes.c_int, [ctypes.c_int, _P, ctypes.POINTER(Fp8Desc), _P,
+                                             ctypes.c_size_t, _P]),
+}
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libqpa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libqpa.so not found at {path}; build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def declared_symbols():
+    return list(_SIGS)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("qpa runs on CUDA tensors only (no CPU path)")
+
+
+def _check(fn, st):
+    if st != QPA_OK:
+        raise QpaError(fn, st)
+
+
+def kernel_error(stream=None) -> int:
+    """Synchronise the stream and return/clear the device error word."""
+    return load_library().qpa_kernel_error(_stream(stream))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns blocks aligned to at least 512 bytes
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+# --------------------------------------------------------------------- fp8
+def fp8_desc(q, kv_cache, block_table, query_group, softmax_scale=None, out_dtype=torch.float32):
+    B, Hq, D = q.shape
+    NB, two, Hk, bs, D2 = kv_cache.shape
+    assert two == 2 and D2 == D and Hq == Hk * query_group
+    d = Fp8Desc()
+    d.num_seqs, d.num_kv_heads, d.query_group, d.head_dim = B, Hk, query_group, D
+    d.block_size, d.num_blocks, d.max_blocks_per_seq = bs, NB, block_table.shape[1]
+    d.out_dtype = QPA_OUT_BF16 if out_dtype == torch.bfloat16 else QPA_OUT_F32
+    if q.stride(2) != 1:
+        raise ValueError("q must be contiguous along head_dim")
+    d.q_stride_seq, d.q_stride_head = q.stride(0), q.stride(1)
+    d.softmax_scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    return d
+
+
+def pa_decode_fp8_workspace_size(desc: Fp8Desc, num_partitions: int) -> int:
+    return int(load_library().pa_decode_fp8_workspace_size(ctypes.byref(desc), num_partitions))
+
+
+def pa_decode_fp8(q, kv_cache, block_table, seq_lens, k_scale, v_scale, num_partitions: int,
+                  query_group: int, out=None, workspace=None, softmax_scale=None,
+                  out_dtype=torch.float32, stream=None, desc=None):
+    """fp8 paged-attention decode. q bf16 [B, Hq, 128]; kv_cache uint8
+    [NB, 2, Hk, bs, 128]; block_table int32 [B, maxb]; seq_lens int32 [B];
+    k_scale / v_scale float32 [1] on the device. Returns out [B, Hq, 128]."""
+    lib = load_library()
+    _need_cuda(q, kv_cache, block_table, seq_lens, k_scale, v_scale)
+    if desc is None:
+        desc = fp8_desc(q, kv_cache, block_table, query_group, softmax_scale, out_dtype)
+    if out is None:
+        odt = torch.bfloat16 if desc.out_dtype == QPA_OUT_BF16 else torch.float32
+        out = torch.empty((q.shape[0], q.shape[1], q.shape[2]), dtype=odt, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(pa_decode_fp8_workspace_size(desc, num_partitions), q.device)
+    st = lib.pa_decode_fp8(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), _ptr(k_scale),
+                           _ptr(v_scale), num_partitions, _ptr(out), ctypes.byref(desc),
+                           _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("pa_decode_fp8", st)
+    return out
+
+
+def pa_decode_fp8_partition(q, kv_cache, block_table, seq_lens, k_scale, v_scale, num_partitions,
+                            desc, workspace, stream=None):
+    st = load_library().pa_decode_fp8_partition(
+        _ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), _ptr(k_scale), _ptr(v_scale),
+        num_partitions, ctypes.byref(desc), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("pa_decode_fp8_partition", st)
+
+
+def pa_decode_fp8_combine(num_partitions, out, desc, workspace, stream=None):
+    st = load_library().pa_decode_fp8_combine(num_partitions, _ptr(out), ctypes.byref(desc),
+                                              _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("pa_decode_fp8_combine", st)
+
+
+def fp8_workspace_views(workspace, desc: Fp8Desc, num_partitions: int):
+    """(O, m, l) float32 views of the partition partials in a workspace."""
+    rows = desc.num_seqs * desc.num_kv_heads * num_partitions * desc.query_group
+    up = lambda x: (x + 255) // 256 * 256
+    m_off = up(rows * desc.head_dim * 4)
+    l_off = up(m_off + rows * 4)
+    f = workspace.view(torch.uint8)
+    shp = (desc.num_seqs, desc.num_kv_heads, num_partitions, desc.query_group)
+    O = f[:rows * desc.head_dim * 4].view(torch.float32).view(*shp, desc.head_dim)
+    m = f[m_off:m_off + rows * 4].view(torch.float32).view(*shp)
+    l = f[l_off:l_off + rows * 4].view(torch.float32).view(*shp)
+    return O, m, l

@@ -1,0 +1,183 @@
+// C-ABI layer: argument validation, workspace carving and kernel launches on
+// the caller's stream. Nothing here reads device data or synchronises (except
+// qpa_kernel_error, a diagnostic).
+#include <cmath>
+#include <cstring>
+
+#include "qpa.h"
+#include "common.cuh"
+#include "qpa_internal.h"
+
+namespace qpa {
+__device__ int g_kernel_error = 0;
+
+namespace {
+
+int num_sms_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ fp8
+struct Fp8Layout {
+  size_t o_off, m_off, l_off, total;
+};
+
+bool fp8_shape_ok(const qpa_fp8_desc* d) {
+  if (d->num_seqs < 0 || d->num_kv_heads < 1 || d->query_group < 1 || d->query_group > 16) return false;
+  if (d->head_dim != 128) return false;
+  const int bs = d->block_size;
+  if (!(bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256)) return false;
+  if (d->num_blocks < 1 || d->max_blocks_per_seq < 1) return false;
+  if (d->out_dtype != QPA_OUT_F32 && d->out_dtype != QPA_OUT_BF16) return false;
+  if ((long long)d->max_blocks_per_seq * bs > 0x7fffffffLL) return false;
+  return true;
+}
+
+Fp8Layout fp8_layout(const qpa_fp8_desc* d, int P) {
+  const size_t rows = size_t(d->num_seqs) * d->num_kv_heads * P * d->query_group;
+  Fp8Layout L;
+  L.o_off = 0;
+  L.m_off = round_up(L.o_off + rows * d->head_dim * sizeof(float), 256);
+  L.l_off = round_up(L.m_off + rows * sizeof(float), 256);
+  L.total = round_up(L.l_off + rows * sizeof(float), 256);
+  return L;
+}
+
+int fp8_check(const void* q, const uint8_t* kv, const int32_t* bt, const int32_t* sl, const float* ks,
+              const float* vs, int P, const qpa_fp8_desc* d, const void* ws, size_t wsb) {
+  if (!d) return QPA_ERR_NULL;
+  if (!fp8_shape_ok(d)) return QPA_ERR_SHAPE;
+  if (P < 1) return QPA_ERR_PARTITIONS;
+  if ((long long)d->num_seqs * d->num_kv_heads * P * d->query_group > 0x7fffffffLL) return QPA_ERR_SHAPE;
+  if (d->num_seqs == 0) return QPA_OK;
+  if (!q || !kv || !bt || !sl || !ks || !vs || !ws) return QPA_ERR_NULL;
+  const long long sh = d->q_stride_head ? d->q_stride_head : d->head_dim;
+  const long long ss = d->q_stride_seq ? d->q_stride_seq : (long long)d->num_kv_heads * d->query_group * d->head_dim;
+  if (sh < 0 || ss < 0 || (sh % 8) || (ss % 8)) return QPA_ERR_ALIGN;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(ws, 256)) return QPA_ERR_ALIGN;
+  if (wsb < fp8_layout(d, P).total) return QPA_ERR_WORKSPACE;
+  return QPA_OK;
+}
+
+}  // namespace
+}  // namespace qpa
+
+using namespace qpa;
+
+extern "C" {
+
+const char* qpa_status_string(int s) {
+  switch (s) {
+    case QPA_OK: return "ok";
+    case QPA_ERR_NULL: return "null pointer";
+    case QPA_ERR_SHAPE: return "unsupported shape";
+    case QPA_ERR_ALIGN: return "misaligned pointer or stride";
+    case QPA_ERR_WORKSPACE: return "workspace too small";
+    case QPA_ERR_PARTITIONS: return "num_partitions must be >= 1";
+    case QPA_ERR_CUDA: return "CUDA launch error";
+    default: return "unknown status";
+  }
+}
+
+int qpa_version(void) { return 100; }
+
+int qpa_kernel_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QPA_ERR_CUDA;
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, qpa::g_kernel_error, sizeof(int)) != cudaSuccess) return QPA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(qpa::g_kernel_error, &z, sizeof(int)) != cudaSuccess) return QPA_ERR_CUDA;
+  return v;
+}
+
+size_t pa_decode_fp8_workspace_size(const qpa_fp8_desc* d, int num_partitions) {
+  if (!d || num_partitions < 1 || !fp8_shape_ok(d)) return 0;
+  return fp8_layout(d, num_partitions).total;
+}
+
+int pa_decode_fp8_partition(const void* q, const uint8_t* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, const float* k_scale, const float* v_scale,
+                            int num_partitions, const qpa_fp8_desc* d, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  int st = fp8_check(q, kv_cache, block_table, seq_lens, k_scale, v_scale, num_partitions, d, workspace,
+                     workspace_bytes);
+  if (st != QPA_OK || d->num_seqs == 0) return st;
+  const Fp8Layout L = fp8_layout(d, num_partitions);
+  Fp8Launch a;
+  a.q = q;
+  a.kv = kv_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.part_o = reinterpret_cast<float*>(ws + L.o_off);
+  a.part_m = reinterpret_cast<float*>(ws + L.m_off);
+  a.part_l = reinterpret_cast<float*>(ws + L.l_off);
+  a.q_stride_head = d->q_stride_head ? d->q_stride_head : d->head_dim;
+  a.q_stride_seq = d->q_stride_seq ? d->q_stride_seq : (long long)d->num_kv_heads * d->query_group * d->head_dim;
+  a.num_seqs = d->num_seqs;
+  a.num_kv_heads = d->num_kv_heads;
+  a.qg = d->query_group;
+  a.block_size = d->block_size;
+  a.num_blocks = d->num_blocks;
+  a.max_blocks = d->max_blocks_per_seq;
+  a.num_partitions = num_partitions;
+  a.softmax_scale = d->softmax_scale != 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
+  a.num_sms = num_sms_current();
+  if (a.num_sms <= 0) return QPA_ERR_CUDA;
+  return launch_fp8_partition(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;
+}
+
+int pa_decode_fp8_combine(int num_partitions, void* out, const qpa_fp8_desc* d, const void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (!d) return QPA_ERR_NULL;
+  if (!fp8_shape_ok(d)) return QPA_ERR_SHAPE;
+  if (num_partitions < 1) return QPA_ERR_PARTITIONS;
+  if (d->num_seqs == 0) return QPA_OK;
+  if (!out || !workspace) return QPA_ERR_NULL;
+  if (!aligned(out, 16) || !aligned(workspace, 256)) return QPA_ERR_ALIGN;
+  const Fp8Layout L = fp8_layout(d, num_partitions);
+  if (workspace_bytes < L.total) return QPA_ERR_WORKSPACE;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  CombineLaunch c;
+  c.part_o = reinterpret_cast<const float*>(ws + L.o_off);
+  c.part_m = reinterpret_cast<const float*>(ws + L.m_off);
+  c.part_l = reinterpret_cast<const float*>(ws + L.l_off);
+  c.out = out;
+  c.out_bf16 = d->out_dtype == QPA_OUT_BF16;
+  c.num_seqs = d->num_seqs;
+  c.num_kv_heads = d->num_kv_heads;
+  c.qg = d->query_group;
+  c.num_partitions = num_partitions;
+  c.d = d->head_dim;
+  c.out_stride_head = d->head_dim;
+  c.out_stride_seq = (long long)d->num_kv_heads * d->query_group * d->head_dim;
+  return launch_combine(c, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;
+}
+
+int pa_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t* block_table, const int32_t* seq_lens,
+                  const float* k_scale, const float* v_scale, int num_partitions, void* out,
+                  const qpa_fp8_desc* d, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = fp8_check(q, kv_cache, block_table, seq_lens, k_scale, v_scale, num_partitions, d, workspace,
+                     workspace_bytes);
+  if (st != QPA_OK) return st;
+  if (d->num_seqs == 0) return QPA_OK;
+  if (!out) return QPA_ERR_NULL;
+  if (!aligned(out, 16)) return QPA_ERR_ALIGN;
+  st = pa_decode_fp8_partition(q, kv_cache, block_table, seq_lens, k_scale, v_scale, num_partitions, d,
+                               workspace, workspace_bytes, stream);
+  if (st != QPA_OK) return st;
+  return pa_decode_fp8_combine(num_partitions, out, d, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// Internal launch descriptors shared by the C-ABI layer and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda.h>
+#include <stdint.h>
+#include <algorithm>
+
+namespace qpa {
+
+struct Fp8Launch {
+  const void* q;
+  const uint8_t* kv;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const float* k_scale;
+  const float* v_scale;
+  float* part_o;
+  float* part_m;
+  float* part_l;
+  long long q_stride_seq, q_stride_head;
+  int num_seqs, num_kv_heads, qg, block_size, num_blocks, max_blocks, num_partitions;
+  float softmax_scale;
+  int num_sms;
+};
+
+struct CombineLaunch {
+  const float* part_o;
+  const float* part_m;
+  const float* part_l;
+  void* out;
+  int out_bf16;
+  int num_seqs, num_kv_heads, qg, num_partitions, d;
+  long long out_stride_seq, out_stride_head;
+};
+
+__device__ __forceinline__ void store4(float* dst, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* dst, float a, float b, float c, float d) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  uint2 v;
+  v.x = *reinterpret_cast<uint32_t*>(&lo);
+  v.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(dst) = v;
+}
+
+cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream);
+cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t stream);
+
+}  // namespace qpa

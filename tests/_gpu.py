@@ -1,0 +1,77 @@
+"""Helpers shared by the GPU parity tests: move a synthetic case to the
+device, run the library through its C ABI, and compute the tolerances the
+parity bar states (attention: max|err| <= 2e-3 * max|V| of the sequence and
+KV head; scores: |err| <= 1e-4 * max(|ref|, mean|ref| of the row))."""
+import numpy as np
+import torch
+
+import oracle
+import quantized_paged_attention_gb300 as qpa
+
+ATT_TOL = 2e-3
+SCORE_TOL = 1e-4
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def bf16_tensor(bits, device):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+class Fp8Dev:
+    def __init__(self, c, device=None):
+        device = device or dev()
+        self.c = c
+        self.q = bf16_tensor(c.q_bits, device)
+        self.kv = torch.from_numpy(c.kv_cache).to(device)
+        self.bt = torch.from_numpy(c.block_table).to(device)
+        self.sl = torch.from_numpy(c.seq_lens).to(device)
+        self.ks = torch.tensor([c.k_scale], dtype=torch.float32, device=device)
+        self.vs = torch.tensor([c.v_scale], dtype=torch.float32, device=device)
+
+    def desc(self, out_dtype=torch.float32, q=None):
+        q = self.q if q is None else q
+        return qpa.fp8_desc(q, self.kv, self.bt, self.c.query_group, self.c.softmax_scale, out_dtype)
+
+    def run(self, P, out_dtype=torch.float32, q=None, workspace=None, out=None):
+        q = self.q if q is None else q
+        desc = self.desc(out_dtype, q)
+        if workspace is None:
+            workspace = qpa.alloc_workspace(qpa.pa_decode_fp8_workspace_size(desc, P), q.device)
+        out = qpa.pa_decode_fp8(q, self.kv, self.bt, self.sl, self.ks, self.vs, P, self.c.query_group,
+                                out=out, workspace=workspace, desc=desc)
+        torch.cuda.synchronize()
+        assert qpa.kernel_error() == 0
+        return out, workspace, desc
+
+
+def fp8_v_absmax(c, s, h):
+    L = int(c.seq_lens[s])
+    if L == 0:
+        return 0.0
+    _, v = oracle.attention.dense_kv_fp8(c.kv_cache, c.block_table, s, h, L, c.k_scale, c.v_scale)
+    return float(np.abs(v).max())
+
+
+def check_attention(got, ref, vmax_fn, c, units=None, what=""):
+    """got/ref [B, Hq, D]; vmax_fn(s, h) -> max|V| for the tolerance."""
+    B = got.shape[0]
+    Hk, QG = c.num_kv_heads, c.query_group
+    if units is None:
+        units = [(s, h) for s in range(B) for h in range(Hk)]
+    worst = 0.0
+    for s, h in units:
+        rows = slice(h * QG, (h + 1) * QG)
+        g, r = got[s, rows], ref[s, rows]
+        assert np.all(np.isfinite(g)), f"{what} non-finite output at seq {s} head {h}"
+        L = int(c.seq_lens[s])
+        if L == 0:
+            assert np.all(g == 0.0), f"{what} L=0 must give 0 (seq {s})"
+            continue
+        err = float(np.max(np.abs(g - r)))
+        tol = ATT_TOL * vmax_fn(s, h)
+        worst = max(worst, err / tol if tol > 0 else 0.0)
+        assert err <= tol, f"{what} seq {s} head {h}: max|err| {err:.3e} > tol {tol:.3e}"
+    return worst

@@ -1,0 +1,79 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_paged_attention_gb300 as qpa
+    return qpa.load_library()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "qpa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = "\n".join(l for l in src.splitlines() if not l.lstrip().startswith("#"))
+    names = re.findall(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\([^;{]*\)\s*;", src)
+    return sorted(set(n for n in names if n not in ("sizeof",)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert "pa_decode_fp8" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_covers_header():
+    import quantized_paged_attention_gb300 as qpa
+    assert set(_declared_functions()) <= set(qpa.declared_symbols())
+
+
+def test_status_strings(lib):
+    assert lib.qpa_status_string(0) == b"ok"
+    assert b"partitions" in lib.qpa_status_string(-5)
+
+
+def _desc(**kw):
+    import quantized_paged_attention_gb300 as qpa
+    d = qpa.Fp8Desc()
+    d.num_seqs, d.num_kv_heads, d.query_group, d.head_dim = 2, 1, 8, 128
+    d.block_size, d.num_blocks, d.max_blocks_per_seq, d.out_dtype = 16, 32, 13, 0
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+FAKE = ctypes.c_void_p(0x100000)      # never dereferenced: every call below fails validation
+
+
+def _call(lib, d, P=2, ws_bytes=1 << 20, q=FAKE, ws=FAKE):
+    return lib.pa_decode_fp8(q, FAKE, FAKE, FAKE, FAKE, FAKE, P, FAKE, ctypes.byref(d), ws, ws_bytes, None)
+
+
+def test_host_validation(lib):
+    assert _call(lib, _desc(), P=0) == -5
+    assert _call(lib, _desc(head_dim=64)) == -2
+    assert _call(lib, _desc(block_size=24)) == -2
+    assert _call(lib, _desc(query_group=17)) == -2
+    assert _call(lib, _desc(), q=ctypes.c_void_p(0)) == -1
+    assert _call(lib, _desc(), q=ctypes.c_void_p(0x100008)) == -3
+    assert _call(lib, _desc(q_stride_head=100)) == -3
+    assert _call(lib, _desc(), ws_bytes=16) == -4
+    assert lib.pa_decode_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, FAKE, None, FAKE, 1, None) == -1
+
+
+def test_workspace_size(lib):
+    d = _desc()
+    n = lib.pa_decode_fp8_workspace_size(ctypes.byref(d), 2)
+    rows = 2 * 1 * 2 * 8
+    assert n >= rows * 130 * 4 and n % 256 == 0
+    assert lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc(head_dim=64)), 2) == 0

@@ -1,0 +1,158 @@
+"""GPU parity of pa_decode_fp8 against the float64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_paged_attention_gb300 as qpa
+import synth
+from _gpu import Fp8Dev, check_attention, fp8_v_absmax
+from oracle.attention import dense_kv_fp8, partition_partials
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _oracle(c, units=None):
+    return oracle.pa_decode_fp8(c.q_bits, c.kv_cache, c.block_table, c.seq_lens, c.k_scale, c.v_scale,
+                                c.query_group, c.softmax_scale, units=units)
+
+
+def _check(c, got, units=None, what=""):
+    ref = _oracle(c, units)
+    return check_attention(got, ref, lambda s, h: fp8_v_absmax(c, s, h), c, units, what)
+
+
+def test_tiny_config():
+    """2 seqs (37, 200), 1 KV head, group 8, block 16, 32 permuted blocks, P=2."""
+    c = synth.fp8_tiny()
+    out, _, _ = Fp8Dev(c).run(2)
+    _check(c, out.cpu().double().numpy(), what="tiny")
+
+
+def test_tiny_partials_match_oracle_partitions():
+    c = synth.fp8_tiny()
+    P = 2
+    out, ws, desc = Fp8Dev(c).run(P)
+    O, m, l = [t.cpu().double().numpy() for t in qpa.fp8_workspace_views(ws, desc, P)]
+    q = oracle.decode_bf16(c.q_bits)
+    for s in range(c.num_seqs):
+        L = int(c.seq_lens[s])
+        k, v = dense_kv_fp8(c.kv_cache, c.block_table, s, 0, L, c.k_scale, c.v_scale)
+        rm, rl, rO = partition_partials(q[s, :8], k, v, c.softmax_scale, P)
+        vmax = float(np.abs(v).max())
+        for p in range(P):
+            if np.isinf(rm[p]).all():
+                assert np.all(np.isneginf(m[s, 0, p])) and np.all(l[s, 0, p] == 0)
+                assert np.all(O[s, 0, p] == 0)
+                continue
+            assert np.max(np.abs(m[s, 0, p] - rm[p])) < 1e-3
+            assert np.max(np.abs(l[s, 0, p] / rl[p] - 1)) < 2e-3
+            assert np.max(np.abs(O[s, 0, p] - rO[p])) <= 2e-3 * vmax
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 7, 32, 100])
+def test_partition_counts_ragged(P):
+    lens = [0, 1, 15, 16, 17, 63, 64, 65, 255, 256, 257, 1000, 2049]
+    c = synth.make_fp8_case(40 + P, lens, 2, 8, 128, 16)
+    out, _, _ = Fp8Dev(c).run(P)
+    _check(c, out.cpu().double().numpy(), what=f"P={P}")
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128, 256])
+def test_block_sizes(bs):
+    lens = [1, bs - 1, bs, bs + 1, 300, 777]
+    c = synth.make_fp8_case(60 + bs, lens, 2, 8, 128, bs)
+    out, _, _ = Fp8Dev(c).run(3)
+    _check(c, out.cpu().double().numpy(), what=f"bs={bs}")
+
+
+@pytest.mark.parametrize("qg", [1, 4, 6, 8, 12, 16])
+def test_query_groups(qg):
+    c = synth.make_fp8_case(80 + qg, [5, 129, 600], 2, qg, 128, 16)
+    out, _, _ = Fp8Dev(c).run(2)
+    _check(c, out.cpu().double().numpy(), what=f"qg={qg}")
+
+
+def test_strided_query_from_fused_qkv():
+    c = synth.make_fp8_case(91, [100, 300], 2, 8, 128, 16)
+    d = Fp8Dev(c)
+    B, Hq, D = c.q_bits.shape
+    Hk = c.num_kv_heads
+    qkv = torch.randn(B, Hq + 2 * Hk, D, device=d.q.device).to(torch.bfloat16)
+    qkv[:, :Hq] = d.q
+    out, _, _ = d.run(4, q=qkv[:, :Hq])
+    _check(c, out.cpu().double().numpy(), what="strided q")
+
+
+def test_bf16_output():
+    c = synth.make_fp8_case(92, [50, 513], 1, 8, 128, 16)
+    out, _, _ = Fp8Dev(c).run(2, out_dtype=torch.bfloat16)
+    assert out.dtype == torch.bfloat16
+    got = out.float().cpu().double().numpy()
+    ref = _oracle(c)
+    # bf16 output rounding adds up to 2^-8 |o| on top of the kernel error
+    for s in range(2):
+        vmax = fp8_v_absmax(c, s, 0)
+        assert np.max(np.abs(got[s] - ref[s])) <= 2e-3 * vmax + np.max(np.abs(ref[s])) * 2 ** -8
+
+
+def test_scales_and_softmax_scale():
+    c = synth.make_fp8_case(93, [333], 1, 8, 128, 16, k_scale=0.3, v_scale=2.5, softmax_scale=0.02)
+    out, _, _ = Fp8Dev(c).run(2)
+    _check(c, out.cpu().double().numpy(), what="scales")
+
+
+def test_repeat_is_deterministic():
+    c = synth.make_fp8_case(94, [1000, 37], 2, 8, 128, 16)
+    d = Fp8Dev(c)
+    a, ws, _ = d.run(5)
+    b, _, _ = d.run(5, workspace=ws)
+    assert torch.equal(a, b)
+
+
+def test_invalid_block_id_raises_error_word():
+    c = synth.make_fp8_case(95, [40], 1, 8, 128, 16)
+    c.block_table[0, 1] = c.kv_cache.shape[0] + 5       # past the cache
+    d = Fp8Dev(c)
+    desc = d.desc()
+    ws = qpa.alloc_workspace(qpa.pa_decode_fp8_workspace_size(desc, 1), d.q.device)
+    qpa.pa_decode_fp8(d.q, d.kv, d.bt, d.sl, d.ks, d.vs, 1, 8, workspace=ws, desc=desc)
+    assert qpa.kernel_error() == 3
+    assert qpa.kernel_error() == 0                      # reading clears it
+
+
+def _sampled_units(c, n, seed):
+    rng = np.random.default_rng(seed)
+    all_units = [(s, h) for s in range(c.num_seqs) for h in range(c.num_kv_heads)]
+    idx = rng.choice(len(all_units), size=min(n, len(all_units)), replace=False)
+    return [all_units[i] for i in sorted(idx)]
+
+
+def test_full_gqa_config_sampled():
+    """16 seqs x 16384, 8 KV heads, group 8, P=32 (512-token partitions), as
+    the benchmark runs it; 8 sampled (seq, head) units against the oracle and
+    every output finite."""
+    c = synth.fp8_gqa()
+    out, _, _ = Fp8Dev(c).run(32)
+    got = out.cpu().double().numpy()
+    assert np.all(np.isfinite(got))
+    _check(c, got, units=_sampled_units(c, 8, 1), what="gqa-full")
+
+
+def test_full_ragged_config_sampled():
+    """128 seqs, lengths U[1024, 16384], P=32; sampled units plus the
+    shortest and the longest sequence."""
+    c = synth.fp8_ragged()
+    out, _, _ = Fp8Dev(c).run(32)
+    got = out.cpu().double().numpy()
+    assert np.all(np.isfinite(got))
+    units = _sampled_units(c, 6, 2)
+    for s in (int(np.argmin(c.seq_lens)), int(np.argmax(c.seq_lens))):
+        units.append((s, 7))
+    _check(c, got, units=units, what="ragged-full")
