@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantised paged-attention decode hot path on GB300.
+
+Metric: paged-decode microseconds per step and KV-cache GB/s (as a fraction
+of the measured HBM peak) at 1 GPU. A step is one decode over the whole
+batch: the partition kernel and the combine kernel of pa_decode_fp8 on the
+16 seqs x 16384 tokens, 8 KV heads, group 8, head_dim 128, block 16 workload
+with 512-token partitions (P = 32). Inputs are seeded synthetic data, resident
+in HBM when the timed region starts; the 537 MB KV stream is larger than L2.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+Prints one JSON line. Under torchrun (N > 1) every rank runs an independent
+replica (no collective on the data path) and rank 0 reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode µs/step and KV-cache GB/s (% of GB300 HBM peak) at 1 GPU"
+WORKLOAD = ("fp8 paged decode: 16 seqs x 16384 tokens, 8 KV heads, query group 8 (64 q heads), "
+            "head_dim 128, block_size 16, random-permutation block table, P=32 (512-token partitions)")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_fp8_partition_gqa16x16k.md")
+KERNEL_SRC = os.path.join(ROOT, "quantized_paged_attention_gb300", "csrc", "pa_fp8.cu")
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the ragged-batch extra measurement")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
+        if not sm:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, n in enumerate(names):
+                if len(r) > 5 + i and "Active" in r[5 + i] and "Not" not in r[5 + i]:
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ traffic from the committed ncu summary
+def _profiled_traffic():
+    """Per-launch DRAM bytes of the partition kernel from the committed ncu
+    summary, if it was taken on the current kernel source (hash match)."""
+    try:
+        txt = open(PROFILE_SUMMARY).read()
+        h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", txt).group(1)
+        t = float(re.search(r"dram_bytes_per_launch_full_workload:\s*([0-9.eE+]+)", txt).group(1))
+        cur = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+        return t if cur == h else None
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def _oracle_unit(args):
+    """Oracle on one (seq, kv_head) unit, re-packed as a single-sequence case."""
+    import numpy as np
+    import oracle
+    q_bits, kv_blocks, L, k_scale, v_scale, qg, scale = args
+    nb = kv_blocks.shape[0]
+    bt = np.arange(nb, dtype=np.int32)[None, :]
+    oracle.pa_decode_fp8(q_bits, kv_blocks, bt, np.array([L], dtype=np.int32), k_scale, v_scale, qg, scale)
+    return L * 2 * kv_blocks.shape[2] * kv_blocks.shape[4]
+
+
+def _unit_args(c, s, h):
+    import numpy as np
+    L = int(c.seq_lens[s])
+    nb = (L + c.block_size - 1) // c.block_size
+    blocks = c.kv_cache[c.block_table[s, :nb]][:, :, h:h + 1]          # [nb, 2, 1, bs, D]
+    qg = c.query_group
+    q = c.q_bits[s:s + 1, h * qg:(h + 1) * qg]
+    return (np.ascontiguousarray(q), np.ascontiguousarray(blocks), L, c.k_scale, c.v_scale, qg, c.softmax_scale)
+
+
+class OraclePool:
+    """The float64 oracle on (seq, kv_head) units of a workload, spread over a
+    spawn-started process pool on the host cores (one worker per core)."""
+
+    def __init__(self, c):
+        import multiprocessing as mp
+        self.c = c
+        self.cores = os.cpu_count() or 1
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"          # one BLAS thread per worker process
+        self.pool = mp.get_context("spawn").Pool(self.cores)
+        self.units = [(s, h) for s in range(c.num_seqs) for h in range(c.num_kv_heads)]
+        self.next = 0
+        self.pool.map(_oracle_unit, [_unit_args(c, 0, 0)] * self.cores)     # warm the workers
+
+    def run(self, n):
+        """Runs the next n units; returns (KV bytes, seconds)."""
+        sel = [self.units[(self.next + i) % len(self.units)] for i in range(n)]
+        self.next = (self.next + n) % len(self.units)
+        args = [_unit_args(self.c, s, h) for s, h in sel]
+        t0 = time.perf_counter()
+        b = sum(self.pool.map(_oracle_unit, args, chunksize=1))
+        return b, time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+# ------------------------------------------------------------------ GPU timing
+def _device_inputs(c, dev):
+    import numpy as np
+    import torch
+    return dict(
+        q=torch.from_numpy(c.q_bits.view(np.int16)).view(torch.bfloat16).to(dev),
+        kv=torch.from_numpy(c.kv_cache).to(dev),
+        bt=torch.from_numpy(c.block_table).to(dev),
+        sl=torch.from_numpy(c.seq_lens).to(dev),
+        ks=torch.tensor([c.k_scale], dtype=torch.float32, device=dev),
+        vs=torch.tensor([c.v_scale], dtype=torch.float32, device=dev))
+
+
+def time_fp8(c, P, steps, warmup, dev, sampler=None):
+    """Times `steps` decode steps back to back on the current stream. Returns
+    (ms per step, mean partition-kernel ms, mean combine ms, launches)."""
+    import torch
+    import quantized_paged_attention_gb300 as qpa
+    x = _device_inputs(c, dev)
+    desc = qpa.fp8_desc(x["q"], x["kv"], x["bt"], c.query_group, c.softmax_scale)
+    ws = qpa.alloc_workspace(qpa.pa_decode_fp8_workspace_size(desc, P), dev)
+    out = torch.empty(x["q"].shape, dtype=torch.float32, device=dev)
+    args = (x["q"], x["kv"], x["bt"], x["sl"], x["ks"], x["vs"], P, desc, ws)
+    for _ in range(warmup):
+        qpa.pa_decode_fp8_partition(*args)
+        qpa.pa_decode_fp8_combine(P, out, desc, ws)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.05)
+    start.record()
+    for i in range(steps):
+        ev[i][0].record()
+        qpa.pa_decode_fp8_partition(*args)
+        ev[i][1].record()
+        qpa.pa_decode_fp8_combine(P, out, desc, ws)
+    end.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    _barrier()
+    total = start.elapsed_time(end)
+    part = [a.elapsed_time(b) for a, b in ev]
+    if qpa.kernel_error() != 0:
+        raise RuntimeError("device error word raised during the benchmark")
+    return total / steps, statistics.mean(part), total / steps - statistics.mean(part), 2 * steps, clocks, total
+
+
+def time_e2e(c, P, steps, dev):
+    """The same decode through the C ABI from pinned host buffers: every step
+    copies all inputs host->device, runs the step and copies the output back."""
+    import numpy as np
+    import torch
+    import quantized_paged_attention_gb300 as qpa
+    h = dict(q=torch.from_numpy(c.q_bits.view(np.int16)).view(torch.bfloat16).pin_memory(),
+             kv=torch.from_numpy(c.kv_cache).pin_memory(),
+             bt=torch.from_numpy(c.block_table).pin_memory(),
+             sl=torch.from_numpy(c.seq_lens).pin_memory(),
+             ks=torch.tensor([c.k_scale], dtype=torch.float32).pin_memory(),
+             vs=torch.tensor([c.v_scale], dtype=torch.float32).pin_memory())
+    d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+    desc = qpa.fp8_desc(d["q"], d["kv"], d["bt"], c.query_group, c.softmax_scale)
+    ws = qpa.alloc_workspace(qpa.pa_decode_fp8_workspace_size(desc, P), dev)
+    out = torch.empty(d["q"].shape, dtype=torch.float32, device=dev)
+    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = out.numel() * out.element_size()
+
+    def step():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        qpa.pa_decode_fp8(d["q"], d["kv"], d["bt"], d["sl"], d["ks"], d["vs"], P, c.query_group, out=out,
+                          workspace=ws, desc=desc)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    _barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+# ------------------------------------------------------------------ distributed plumbing
+_DIST = {"on": False}
+
+
+def _barrier():
+    if _DIST["on"]:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x):
+    if not _DIST["on"]:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    a = _args()
+    if a.warmup < 3:
+        a.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    import synth
+
+    if a.impl == "reference":
+        # The reference arm is the float64 CPU oracle, on the host cores, rank 0
+        # only; each step is one batch of (seq, kv_head) units of the workload.
+        if rank != 0:
+            return
+        c = synth.fp8_gqa()
+        pool = OraclePool(c)
+        n = pool.cores
+        tot_b, tot_t = 0, 0.0
+        for i in range(a.warmup + a.steps):
+            b, t = pool.run(n)
+            if i >= a.warmup:
+                tot_b += b
+                tot_t += t
+        pool.close()
+        val = tot_b / tot_t / 1e9
+        sample = (f"{n} (seq, kv_head) units ({n * c.kv_bytes // (c.num_seqs * c.num_kv_heads) / 1e6:.0f} MB "
+                  f"of KV) per step, float64 numpy oracle, spawn pool of {pool.cores} workers")
+        line = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+                "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+                "ms_per_step": round(tot_t / a.steps * 1e3, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "reference": "float64 CPU oracle (oracle/), host cores"},
+                "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": pool.cores,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        _DIST["on"] = True
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peak, peak_kind = _peaks()
+
+    c = synth.fp8_gqa(seed=1001 + rank)
+    P = 32
+    sampler = ClockSampler(local) if rank == 0 else None
+    ms, part_ms, comb_ms, launches, clocks, total_ms = time_fp8(c, P, a.steps, a.warmup, dev, sampler)
+    ms_max = _max_over_ranks(ms)
+    kv = c.kv_bytes
+    value = kv * world / (ms_max * 1e-3) / 1e9
+    part_gbs = kv / (part_ms * 1e-3) / 1e9
+
+    e2e = None
+    if not a.no_e2e:
+        e_ms, h2d, d2h = time_e2e(c, P, max(3, min(a.steps, 10)), dev)
+        e_ms = _max_over_ranks(e_ms)
+        e2e = {"value": round(kv * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4)}
+
+    extra = {}
+    if not a.no_extra:
+        cr = synth.fp8_ragged(seed=1002 + rank)
+        r_ms, r_part, _, _, _, _ = time_fp8(cr, 32, max(20, a.steps // 4), a.warmup, dev)
+        r_ms = _max_over_ranks(r_ms)
+        extra["fp8_ragged_b128"] = {
+            "workload": "fp8 paged decode, 128 seqs, lengths U[1024,16384], 8 KV heads, group 8, block 16, P=32",
+            "us_per_step": round(r_ms * 1e3, 2), "partition_us": round(r_part * 1e3, 2),
+            "kv_bytes": cr.kv_bytes, "gbs": round(cr.kv_bytes / (r_ms * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(cr.kv_bytes / (r_ms * 1e-3) / 1e9 / peak, 4)}
+        del cr
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu:
+        pool = OraclePool(c)
+        nbytes, dt, units = 0, 0.0, 0
+        while dt < 10.0 and units < len(pool.units):
+            b, t = pool.run(pool.cores)
+            nbytes += b
+            dt += t
+            units += pool.cores
+        pool.close()
+        cpu = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": pool.cores, "kind": "oracle",
+               "sample": f"{units} of {len(pool.units)} (seq, kv_head) units of the workload "
+                         f"({nbytes / 1e6:.0f} MB of KV) in {dt:.1f} s, float64 numpy oracle, "
+                         f"spawn pool of {pool.cores} workers"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": round(ms_max, 5), "us_per_step": round(ms_max * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded N(0,1) K/V quantised to e4m3, bf16 Q)",
+        "config": {"workload": WORKLOAD, "kv_bytes_per_step": kv,
+                   "l2": "no flush: the 537 MB KV stream per step is larger than the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(part_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(part_gbs / peak, 4), "traffic": _profiled_traffic(),
+                     "kernel": "pa_fp8_partition_kernel", "peak_kind": peak_kind,
+                     "step_frac": round(value / world / peak, 4)},
+        "partition_us": round(part_ms * 1e3, 2), "combine_us": round(comb_ms * 1e3, 2),
+        "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "extra": extra,
+    }
+    print(json.dumps(line))
+    if _DIST["on"]:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
