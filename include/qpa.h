@@ -133,6 +133,40 @@ int pa_decode_fp8_partition(const void* q, const uint8_t* kv_cache, const int32_
 int pa_decode_fp8_combine(int num_partitions, void* out, const qpa_fp8_desc* d,
                           const void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * pa_decode_fp8_static -- pa_decode_fp8 without a workspace argument.
+ *
+ * The paper has no counterpart; this is a convenience of this library. It is
+ * meant for callers that cannot call cudaMalloc or otherwise obtain device
+ * memory: for example a plugin whose host framework hands it only its input
+ * and output tensors, with every device allocation owned by the host
+ * application's allocator, or a runtime that reserves all device memory up
+ * front and forbids allocations on the decode path. This entry point
+ * allocates nothing. The partition partials go to one static device array of
+ * QPA_FP8_STATIC_SCRATCH_BYTES (8 MiB), which every GPU that loads the library
+ * holds until the process exits.
+ *
+ * Arguments, layouts and results are those of pa_decode_fp8. The partials
+ * need num_seqs*num_kv_heads*num_partitions*query_group*130*4 bytes, plus
+ * 256-byte padding; a call that needs more than the array returns
+ * QPA_ERR_WORKSPACE without launching anything.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current) and caches it. Make that first call
+ * before capturing any stream on that device.
+ *
+ * All calls share the one array and it keeps the last call's contents.
+ * Nothing in it needs to start at zero: the partition kernel writes every
+ * partial before the combine kernel reads it. Calls that overlap on the GPU
+ * (different streams, or different host threads on one device) race on the
+ * array and must be serialised by the caller.
+ * ---------------------------------------------------------------------- */
+#define QPA_FP8_STATIC_SCRATCH_BYTES (8u << 20)
+
+int pa_decode_fp8_static(const void* q, const uint8_t* kv_cache, const int32_t* block_table,
+                         const int32_t* seq_lens, const float* k_scale, const float* v_scale,
+                         int num_partitions, void* out, const qpa_fp8_desc* d, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -50,6 +50,8 @@ _SIGS = {
                                                ctypes.POINTER(Fp8Desc), _P, ctypes.c_size_t, _P]),
     "pa_decode_fp8_combine": (ctypes.c_int, [ctypes.c_int, _P, ctypes.POINTER(Fp8Desc), _P,
                                              ctypes.c_size_t, _P]),
+    "pa_decode_fp8_static": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, _P,
+                                            ctypes.POINTER(Fp8Desc), _P]),
 }
 
 
@@ -173,3 +175,22 @@ def fp8_workspace_views(workspace, desc: Fp8Desc, num_partitions: int):
     m = f[m_off:m_off + rows * 4].view(torch.float32).view(*shp)
     l = f[l_off:l_off + rows * 4].view(torch.float32).view(*shp)
     return O, m, l
+
+
+def pa_decode_fp8_static(q, kv_cache, block_table, seq_lens, k_scale, v_scale, num_partitions: int,
+                         query_group: int, out=None, softmax_scale=None, out_dtype=torch.float32,
+                         stream=None, desc=None):
+    """pa_decode_fp8 without a workspace: for callers that cannot allocate
+    device memory. The partials go to the library's static device array
+    (8 MiB per GPU); calls that overlap on the GPU race on it."""
+    lib = load_library()
+    _need_cuda(q, kv_cache, block_table, seq_lens, k_scale, v_scale, out)
+    if desc is None:
+        desc = fp8_desc(q, kv_cache, block_table, query_group, softmax_scale, out_dtype)
+    if out is None:
+        raise ValueError("pa_decode_fp8_static writes into a caller-provided `out` tensor")
+    st = lib.pa_decode_fp8_static(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+                                  _ptr(k_scale), _ptr(v_scale), num_partitions, _ptr(out),
+                                  ctypes.byref(desc), _stream(stream))
+    _check("pa_decode_fp8_static", st)
+    return out
