@@ -133,6 +133,63 @@ int pa_decode_fp8_partition(const void* q, const uint8_t* kv_cache, const int32_
 int pa_decode_fp8_combine(int num_partitions, void* out, const qpa_fp8_desc* d,
                           const void* workspace, size_t workspace_bytes, void* stream);
 
+/* ========================================================================
+ * UltraQuant head_dim=256 4-bit decode ([UQ] steps A..G)
+ *
+ * For every sequence s, KV head h and query row g (query head h*qg + g):
+ *     q_r = q R,  R = H_256 / 16 (orthonormal Sylvester-Hadamard, R = R^T = R^-1)
+ *     o_r = sum_t softmax_t(softmax_scale * q_r . k_t) v_t,    out = o_r R
+ * where k_t, v_t are the stored (rotated-domain) vectors of token t:
+ *     k[d] = e2m1(K code d) * e4m3(K scale byte d/32)
+ *     v[d] = centroids[V code d] * e4m3(V scale byte d/32)
+ * Slot of (token, KV head), padded_slot bytes (>= 272, a multiple of 16):
+ *   bytes   0..127  K codes, dim 2i in the low nibble of byte i
+ *   bytes 128..135  K scales (e4m3fn), one per 32 dims
+ *   bytes 136..263  V codes (same nibble order)
+ *   bytes 264..271  V scales (e4m3fn), one per 32 dims
+ * Q is rotated inside the partition kernel and the output is rotated back in
+ * the combine kernel. Partitions, empty partitions and L = 0 behave as for
+ * pa_decode_fp8; the workspace holds the same (O, m, l) partials with
+ * head_dim 256, in the rotated domain (no v_scale: the scales are per group).
+ *
+ * Layouts:
+ *   q          bf16 [num_seqs][num_kv_heads*query_group][256] (not rotated),
+ *              descriptor strides in elements (multiples of 8)
+ *   kv_cache   uint8 [num_blocks][block_size][num_kv_heads][padded_slot]
+ *   centroids  float32 [16] on the device (code -> value)
+ *   block_table, seq_lens, out, workspace: as for pa_decode_fp8 (head_dim 256)
+ * Supported: head_dim 256, query_group 1..8, block_size 16/32/64/128/256.
+ * Alignment: q, kv_cache and out 16-byte aligned; workspace 256-byte aligned.
+ * ====================================================================== */
+typedef struct qpa_uq_desc {
+  int32_t num_seqs;
+  int32_t num_kv_heads;
+  int32_t query_group;
+  int32_t head_dim;         /* 256 */
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t padded_slot;      /* bytes per (token, KV head) slot */
+  int32_t out_dtype;        /* QPA_OUT_F32 or QPA_OUT_BF16 */
+  int32_t reserved;
+  int64_t q_stride_seq;     /* elements; 0 = num_kv_heads*query_group*256 */
+  int64_t q_stride_head;    /* elements; 0 = 256 */
+  float softmax_scale;      /* 0 = 1/sqrt(256) */
+} qpa_uq_desc;
+
+size_t uq_decode_hd256_workspace_size(const qpa_uq_desc* d, int num_partitions);
+
+int uq_decode_hd256(const void* q, const uint8_t* kv_cache, const float* centroids,
+                    const int32_t* block_table, const int32_t* seq_lens, int num_partitions,
+                    void* out, const qpa_uq_desc* d, void* workspace, size_t workspace_bytes,
+                    void* stream);
+int uq_decode_hd256_partition(const void* q, const uint8_t* kv_cache, const float* centroids,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              int num_partitions, const qpa_uq_desc* d, void* workspace,
+                              size_t workspace_bytes, void* stream);
+int uq_decode_hd256_combine(int num_partitions, void* out, const qpa_uq_desc* d,
+                            const void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------------------
  * pa_decode_fp8_static -- pa_decode_fp8 without a workspace argument.
  *

@@ -38,6 +38,16 @@ class Fp8Desc(ctypes.Structure):
                 ("softmax_scale", ctypes.c_float)]
 
 
+class UqDesc(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("query_group", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("padded_slot", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("q_stride_seq", ctypes.c_int64), ("q_stride_head", ctypes.c_int64),
+                ("softmax_scale", ctypes.c_float)]
+
+
 _P = ctypes.c_void_p
 _SIGS = {
     "qpa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -52,6 +62,13 @@ _SIGS = {
                                              ctypes.c_size_t, _P]),
     "pa_decode_fp8_static": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, _P,
                                             ctypes.POINTER(Fp8Desc), _P]),
+    "uq_decode_hd256_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(UqDesc), ctypes.c_int]),
+    "uq_decode_hd256": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.POINTER(UqDesc), _P,
+                                       ctypes.c_size_t, _P]),
+    "uq_decode_hd256_partition": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int, ctypes.POINTER(UqDesc),
+                                                 _P, ctypes.c_size_t, _P]),
+    "uq_decode_hd256_combine": (ctypes.c_int, [ctypes.c_int, _P, ctypes.POINTER(UqDesc), _P,
+                                               ctypes.c_size_t, _P]),
 }
 
 
@@ -194,3 +211,59 @@ def pa_decode_fp8_static(q, kv_cache, block_table, seq_lens, k_scale, v_scale, n
                                   ctypes.byref(desc), _stream(stream))
     _check("pa_decode_fp8_static", st)
     return out
+
+
+# --------------------------------------------------------------------- uq hd256
+def uq_desc(q, kv_cache, block_table, query_group, softmax_scale=None, out_dtype=torch.float32):
+    B, Hq, D = q.shape
+    NB, bs, Hk, slot = kv_cache.shape
+    assert D == 256 and Hq == Hk * query_group
+    if q.stride(2) != 1:
+        raise ValueError("q must be contiguous along head_dim")
+    d = UqDesc()
+    d.num_seqs, d.num_kv_heads, d.query_group, d.head_dim = B, Hk, query_group, D
+    d.block_size, d.num_blocks, d.max_blocks_per_seq, d.padded_slot = bs, NB, block_table.shape[1], slot
+    d.out_dtype = QPA_OUT_BF16 if out_dtype == torch.bfloat16 else QPA_OUT_F32
+    d.q_stride_seq, d.q_stride_head = q.stride(0), q.stride(1)
+    d.softmax_scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    return d
+
+
+def uq_decode_hd256_workspace_size(desc: UqDesc, num_partitions: int) -> int:
+    return int(load_library().uq_decode_hd256_workspace_size(ctypes.byref(desc), num_partitions))
+
+
+def uq_decode_hd256(q, kv_cache, centroids, block_table, seq_lens, num_partitions: int, query_group: int,
+                    out=None, workspace=None, softmax_scale=None, out_dtype=torch.float32, stream=None,
+                    desc=None):
+    """4-bit head_dim=256 decode. q bf16 [B, Hq, 256] (not rotated); kv_cache
+    uint8 [NB, bs, Hk, padded_slot]; centroids float32 [16]; returns the
+    un-rotated out [B, Hq, 256]."""
+    lib = load_library()
+    _need_cuda(q, kv_cache, centroids, block_table, seq_lens)
+    if desc is None:
+        desc = uq_desc(q, kv_cache, block_table, query_group, softmax_scale, out_dtype)
+    if out is None:
+        odt = torch.bfloat16 if desc.out_dtype == QPA_OUT_BF16 else torch.float32
+        out = torch.empty((q.shape[0], q.shape[1], 256), dtype=odt, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(uq_decode_hd256_workspace_size(desc, num_partitions), q.device)
+    st = lib.uq_decode_hd256(_ptr(q), _ptr(kv_cache), _ptr(centroids), _ptr(block_table), _ptr(seq_lens),
+                             num_partitions, _ptr(out), ctypes.byref(desc), _ptr(workspace), workspace.numel(),
+                             _stream(stream))
+    _check("uq_decode_hd256", st)
+    return out
+
+
+def uq_decode_hd256_partition(q, kv_cache, centroids, block_table, seq_lens, num_partitions, desc, workspace,
+                              stream=None):
+    st = load_library().uq_decode_hd256_partition(
+        _ptr(q), _ptr(kv_cache), _ptr(centroids), _ptr(block_table), _ptr(seq_lens), num_partitions,
+        ctypes.byref(desc), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("uq_decode_hd256_partition", st)
+
+
+def uq_decode_hd256_combine(num_partitions, out, desc, workspace, stream=None):
+    st = load_library().uq_decode_hd256_combine(num_partitions, _ptr(out), ctypes.byref(desc), _ptr(workspace),
+                                                workspace.numel(), _stream(stream))
+    _check("uq_decode_hd256_combine", st)

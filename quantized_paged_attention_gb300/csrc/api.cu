@@ -69,6 +69,45 @@ int fp8_check(const void* q, const uint8_t* kv, const int32_t* bt, const int32_t
   return QPA_OK;
 }
 
+// ------------------------------------------------------------------ uq hd256
+bool uq_shape_ok(const qpa_uq_desc* d) {
+  if (d->num_seqs < 0 || d->num_kv_heads < 1 || d->query_group < 1 || d->query_group > 8) return false;
+  if (d->head_dim != 256) return false;
+  const int bs = d->block_size;
+  if (!(bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256)) return false;
+  if (d->num_blocks < 1 || d->max_blocks_per_seq < 1) return false;
+  if (d->padded_slot < 272 || d->padded_slot % 16) return false;
+  if (d->out_dtype != QPA_OUT_F32 && d->out_dtype != QPA_OUT_BF16) return false;
+  if ((long long)d->max_blocks_per_seq * bs > 0x7fffffffLL) return false;
+  return true;
+}
+
+Fp8Layout uq_layout(const qpa_uq_desc* d, int P) {
+  const size_t rows = size_t(d->num_seqs) * d->num_kv_heads * P * d->query_group;
+  Fp8Layout L;
+  L.o_off = 0;
+  L.m_off = round_up(rows * 256 * sizeof(float), 256);
+  L.l_off = round_up(L.m_off + rows * sizeof(float), 256);
+  L.total = round_up(L.l_off + rows * sizeof(float), 256);
+  return L;
+}
+
+int uq_check(const void* q, const uint8_t* kv, const float* cent, const int32_t* bt, const int32_t* sl, int P,
+             const qpa_uq_desc* d, const void* ws, size_t wsb) {
+  if (!d) return QPA_ERR_NULL;
+  if (!uq_shape_ok(d)) return QPA_ERR_SHAPE;
+  if (P < 1) return QPA_ERR_PARTITIONS;
+  if ((long long)d->num_seqs * d->num_kv_heads * P * d->query_group > 0x7fffffffLL) return QPA_ERR_SHAPE;
+  if (d->num_seqs == 0) return QPA_OK;
+  if (!q || !kv || !cent || !bt || !sl || !ws) return QPA_ERR_NULL;
+  const long long sh = d->q_stride_head ? d->q_stride_head : 256;
+  const long long ss = d->q_stride_seq ? d->q_stride_seq : (long long)d->num_kv_heads * d->query_group * 256;
+  if (sh < 0 || ss < 0 || (sh % 8) || (ss % 8)) return QPA_ERR_ALIGN;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(ws, 256) || !aligned(cent, 4)) return QPA_ERR_ALIGN;
+  if (wsb < uq_layout(d, P).total) return QPA_ERR_WORKSPACE;
+  return QPA_OK;
+}
+
 }  // namespace
 }  // namespace qpa
 
@@ -178,6 +217,84 @@ int pa_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t* block_t
                                workspace, workspace_bytes, stream);
   if (st != QPA_OK) return st;
   return pa_decode_fp8_combine(num_partitions, out, d, workspace, workspace_bytes, stream);
+}
+
+size_t uq_decode_hd256_workspace_size(const qpa_uq_desc* d, int num_partitions) {
+  if (!d || num_partitions < 1 || !uq_shape_ok(d)) return 0;
+  return uq_layout(d, num_partitions).total;
+}
+
+int uq_decode_hd256_partition(const void* q, const uint8_t* kv_cache, const float* centroids,
+                              const int32_t* block_table, const int32_t* seq_lens, int num_partitions,
+                              const qpa_uq_desc* d, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = uq_check(q, kv_cache, centroids, block_table, seq_lens, num_partitions, d, workspace, workspace_bytes);
+  if (st != QPA_OK || d->num_seqs == 0) return st;
+  const Fp8Layout L = uq_layout(d, num_partitions);
+  UqLaunch a;
+  a.q = q;
+  a.kv = kv_cache;
+  a.centroids = centroids;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.part_o = reinterpret_cast<float*>(ws + L.o_off);
+  a.part_m = reinterpret_cast<float*>(ws + L.m_off);
+  a.part_l = reinterpret_cast<float*>(ws + L.l_off);
+  a.q_stride_head = d->q_stride_head ? d->q_stride_head : 256;
+  a.q_stride_seq = d->q_stride_seq ? d->q_stride_seq : (long long)d->num_kv_heads * d->query_group * 256;
+  a.num_seqs = d->num_seqs;
+  a.num_kv_heads = d->num_kv_heads;
+  a.qg = d->query_group;
+  a.block_size = d->block_size;
+  a.num_blocks = d->num_blocks;
+  a.max_blocks = d->max_blocks_per_seq;
+  a.num_partitions = num_partitions;
+  a.padded_slot = d->padded_slot;
+  a.softmax_scale = d->softmax_scale != 0.f ? d->softmax_scale : 1.0f / 16.0f;
+  a.num_sms = num_sms_current();
+  if (a.num_sms <= 0) return QPA_ERR_CUDA;
+  return launch_uq_partition(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;
+}
+
+int uq_decode_hd256_combine(int num_partitions, void* out, const qpa_uq_desc* d, const void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!d) return QPA_ERR_NULL;
+  if (!uq_shape_ok(d)) return QPA_ERR_SHAPE;
+  if (num_partitions < 1) return QPA_ERR_PARTITIONS;
+  if (d->num_seqs == 0) return QPA_OK;
+  if (!out || !workspace) return QPA_ERR_NULL;
+  if (!aligned(out, 16) || !aligned(workspace, 256)) return QPA_ERR_ALIGN;
+  const Fp8Layout L = uq_layout(d, num_partitions);
+  if (workspace_bytes < L.total) return QPA_ERR_WORKSPACE;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  CombineLaunch c;
+  c.part_o = reinterpret_cast<const float*>(ws + L.o_off);
+  c.part_m = reinterpret_cast<const float*>(ws + L.m_off);
+  c.part_l = reinterpret_cast<const float*>(ws + L.l_off);
+  c.out = out;
+  c.out_bf16 = d->out_dtype == QPA_OUT_BF16;
+  c.num_seqs = d->num_seqs;
+  c.num_kv_heads = d->num_kv_heads;
+  c.qg = d->query_group;
+  c.num_partitions = num_partitions;
+  c.d = 256;
+  c.out_stride_head = 256;
+  c.out_stride_seq = (long long)d->num_kv_heads * d->query_group * 256;
+  return launch_uq_combine(c, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;
+}
+
+int uq_decode_hd256(const void* q, const uint8_t* kv_cache, const float* centroids, const int32_t* block_table,
+                    const int32_t* seq_lens, int num_partitions, void* out, const qpa_uq_desc* d, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  int st = uq_check(q, kv_cache, centroids, block_table, seq_lens, num_partitions, d, workspace, workspace_bytes);
+  if (st != QPA_OK) return st;
+  if (d->num_seqs == 0) return QPA_OK;
+  if (!out) return QPA_ERR_NULL;
+  if (!aligned(out, 16)) return QPA_ERR_ALIGN;
+  st = uq_decode_hd256_partition(q, kv_cache, centroids, block_table, seq_lens, num_partitions, d, workspace,
+                                 workspace_bytes, stream);
+  if (st != QPA_OK) return st;
+  return uq_decode_hd256_combine(num_partitions, out, d, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

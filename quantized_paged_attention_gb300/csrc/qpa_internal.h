@@ -34,6 +34,21 @@ struct CombineLaunch {
   long long out_stride_seq, out_stride_head;
 };
 
+struct UqLaunch {
+  const void* q;
+  const uint8_t* kv;
+  const float* centroids;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* part_o;
+  float* part_m;
+  float* part_l;
+  long long q_stride_seq, q_stride_head;
+  int num_seqs, num_kv_heads, qg, block_size, num_blocks, max_blocks, num_partitions, padded_slot;
+  float softmax_scale;
+  int num_sms;
+};
+
 __device__ __forceinline__ void store4(float* dst, float a, float b, float c, float d) {
   *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
 }
@@ -47,5 +62,7 @@ __device__ __forceinline__ void store4(__nv_bfloat16* dst, float a, float b, flo
 
 cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t stream);
+cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream);
+cudaError_t launch_uq_combine(const CombineLaunch& a, cudaStream_t stream);
 
 }  // namespace qpa

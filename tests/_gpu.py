@@ -75,3 +75,35 @@ def check_attention(got, ref, vmax_fn, c, units=None, what=""):
         worst = max(worst, err / tol if tol > 0 else 0.0)
         assert err <= tol, f"{what} seq {s} head {h}: max|err| {err:.3e} > tol {tol:.3e}"
     return worst
+
+
+class UqDev:
+    def __init__(self, c, device=None):
+        device = device or dev()
+        self.c = c
+        self.q = bf16_tensor(c.q_bits, device)
+        self.kv = torch.from_numpy(c.kv_cache).to(device)
+        self.cent = torch.from_numpy(np.ascontiguousarray(c.centroids, dtype=np.float32)).to(device)
+        self.bt = torch.from_numpy(c.block_table).to(device)
+        self.sl = torch.from_numpy(c.seq_lens).to(device)
+
+    def desc(self, out_dtype=torch.float32):
+        return qpa.uq_desc(self.q, self.kv, self.bt, self.c.query_group, self.c.softmax_scale, out_dtype)
+
+    def run(self, P, out_dtype=torch.float32, workspace=None):
+        desc = self.desc(out_dtype)
+        if workspace is None:
+            workspace = qpa.alloc_workspace(qpa.uq_decode_hd256_workspace_size(desc, P), self.q.device)
+        out = qpa.uq_decode_hd256(self.q, self.kv, self.cent, self.bt, self.sl, P, self.c.query_group,
+                                  workspace=workspace, desc=desc)
+        torch.cuda.synchronize()
+        assert qpa.kernel_error() == 0
+        return out, workspace, desc
+
+
+def uq_v_absmax(c, s, h):
+    L = int(c.seq_lens[s])
+    if L == 0:
+        return 0.0
+    _, v = oracle.uq.dense_kv_uq(c.kv_cache, c.centroids, c.block_table, s, h, L)
+    return float(np.abs(v).max())

@@ -1,0 +1,91 @@
+"""GPU parity of uq_decode_hd256 (4-bit head_dim=256 slot cache, in-kernel
+WHT rotation of Q, un-rotated output) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu import UqDev, check_attention, uq_v_absmax
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _check(c, got, units=None, what=""):
+    ref = oracle.uq_decode_hd256(c.q_bits, c.kv_cache, c.centroids, c.block_table, c.seq_lens,
+                                 c.query_group, c.softmax_scale, units=units)
+    return check_attention(got, ref, lambda s, h: uq_v_absmax(c, s, h), c, units, what)
+
+
+LENS = [0, 1, 15, 63, 64, 65, 255, 256, 257, 777, 1500]
+
+
+@pytest.mark.parametrize("P", [1, 3, 7])
+def test_e2m1_centroids_partitions(P):
+    c = synth.make_uq_case(200 + P, LENS, 2, 8, 64, 288)
+    out, _, _ = UqDev(c).run(P)
+    _check(c, out.cpu().double().numpy(), what=f"e2m1 P={P}")
+
+
+@pytest.mark.parametrize("P", [1, 4])
+def test_random_sorted_centroids(P):
+    c = synth.make_uq_case(210 + P, LENS, 2, 8, 64, 288, centroids=synth.sorted_random_centroids(5))
+    out, _, _ = UqDev(c).run(P)
+    _check(c, out.cpu().double().numpy(), what=f"lut P={P}")
+
+
+@pytest.mark.parametrize("qg", [6, 8, 3])
+def test_query_groups(qg):
+    c = synth.make_uq_case(220 + qg, [70, 500], 2, qg, 64, 288)
+    out, _, _ = UqDev(c).run(2)
+    _check(c, out.cpu().double().numpy(), what=f"qg={qg}")
+
+
+@pytest.mark.parametrize("bs", [16, 32, 128, 256])
+def test_block_sizes(bs):
+    c = synth.make_uq_case(230 + bs, [1, bs - 1, bs + 1, 700], 2, 8, bs, 288)
+    out, _, _ = UqDev(c).run(3)
+    _check(c, out.cpu().double().numpy(), what=f"bs={bs}")
+
+
+@pytest.mark.parametrize("slot", [272, 320])
+def test_slot_padding(slot):
+    c = synth.make_uq_case(240 + slot, [100, 333], 1, 8, 64, slot,
+                           centroids=synth.sorted_random_centroids(6))
+    out, _, _ = UqDev(c).run(2)
+    _check(c, out.cpu().double().numpy(), what=f"slot={slot}")
+
+
+def test_bf16_output_and_determinism():
+    c = synth.make_uq_case(250, [300, 64], 2, 8, 64, 288)
+    d = UqDev(c)
+    a, ws, _ = d.run(3)
+    b, _, _ = d.run(3, workspace=ws)
+    assert torch.equal(a, b)
+    o16, _, _ = d.run(3, out_dtype=torch.bfloat16)
+    assert o16.dtype == torch.bfloat16
+    assert torch.max(torch.abs(o16.float() - a)).item() <= torch.max(torch.abs(a)).item() * 2 ** -8 + 1e-6
+
+
+def _sampled_units(c, n, seed):
+    rng = np.random.default_rng(seed)
+    all_units = [(s, h) for s in range(c.num_seqs) for h in range(c.num_kv_heads)]
+    idx = rng.choice(len(all_units), size=min(n, len(all_units)), replace=False)
+    return [all_units[i] for i in sorted(idx)]
+
+
+@pytest.mark.parametrize("qg", [8, 6])
+def test_full_config_sampled(qg):
+    """4 seqs x 75000 tokens, 2 KV heads, block 64, 288-byte slots, P=147
+    (as the benchmark runs it); 3 sampled (seq, head) units against the oracle."""
+    c = synth.uq_full(query_group=qg)
+    out, _, _ = UqDev(c).run(147)
+    got = out.cpu().double().numpy()
+    assert np.all(np.isfinite(got))
+    _check(c, got, units=_sampled_units(c, 3, qg), what=f"uq-full qg={qg}")
