@@ -190,6 +190,52 @@ int uq_decode_hd256_partition(const void* q, const uint8_t* kv_cache, const floa
 int uq_decode_hd256_combine(int num_partitions, void* out, const qpa_uq_desc* d,
                             const void* workspace, size_t workspace_bytes, void* stream);
 
+/* ========================================================================
+ * NVFP4 paged index scorer ([IDX] compile_score_decode)
+ *
+ * For request r (length L = seq_lens[r]), query row qoff < query_len, index
+ * head h and block b:
+ *     k[t][d]   = e2m1(code[t][d]) * e4m3(scale[t][d/16])
+ *     dot[t]    = sum_d e4m3(q[r*query_len + qoff][h][d]) * k[t][d]
+ *     scores[h][r*query_len + qoff][b] = max{ dot[t] : t in block b, t <= L - query_len + qoff }
+ * and -inf when no token of the block is visible. Every column b of
+ * [0, num_cols) of every row is written: columns at or past ceil(L/128) get
+ * -inf. No scale, weight or activation is applied to the dot.
+ *
+ * Layouts:
+ *   q          uint8 (e4m3fn) [num_reqs*query_len][num_heads][128] with byte
+ *              strides q_stride_tok / q_stride_head (multiples of 16)
+ *   kv_pages   uint8 [num_blocks] pages at page_stride bytes (>= 9216, a
+ *              multiple of 16); a page holds 128 tokens: bytes 0..8191 are
+ *              the codes (64 per token, dim 2i in the low nibble of byte i),
+ *              bytes 8192..9215 the e4m3 scales (8 per token, one per 16 dims)
+ *   block_table int32 [num_reqs][max_blocks_per_seq]; only entries below
+ *              min(ceil(L/128), num_cols) are read
+ *   seq_lens   int32 [num_reqs]
+ *   scores     float32 [num_heads][num_reqs*query_len][num_cols] with element
+ *              strides s_stride_head / s_stride_row (the last dim contiguous)
+ * Supported: head_dim 128, query_len * num_heads <= 16.
+ * Alignment: q and kv_pages 16-byte aligned, scores 4-byte aligned.
+ * ====================================================================== */
+typedef struct qpa_idx_desc {
+  int32_t num_reqs;
+  int32_t query_len;
+  int32_t num_heads;
+  int32_t head_dim;         /* 128 */
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t num_cols;         /* S: score columns per row */
+  int32_t reserved;
+  int64_t page_stride;      /* bytes; 0 = 9216 */
+  int64_t q_stride_tok;     /* bytes; 0 = num_heads*128 */
+  int64_t q_stride_head;    /* bytes; 0 = 128 */
+  int64_t s_stride_head;    /* elements; 0 = num_reqs*query_len*num_cols */
+  int64_t s_stride_row;     /* elements; 0 = num_cols */
+} qpa_idx_desc;
+
+int nvfp4_index_score(const uint8_t* q, const uint8_t* kv_pages, const int32_t* block_table,
+                      const int32_t* seq_lens, float* scores, const qpa_idx_desc* d, void* stream);
+
 /* ------------------------------------------------------------------------
  * pa_decode_fp8_static -- pa_decode_fp8 without a workspace argument.
  *

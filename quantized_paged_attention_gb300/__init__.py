@@ -48,6 +48,16 @@ class UqDesc(ctypes.Structure):
                 ("softmax_scale", ctypes.c_float)]
 
 
+class IdxDesc(ctypes.Structure):
+    _fields_ = [("num_reqs", ctypes.c_int32), ("query_len", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("num_cols", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("page_stride", ctypes.c_int64), ("q_stride_tok", ctypes.c_int64),
+                ("q_stride_head", ctypes.c_int64), ("s_stride_head", ctypes.c_int64),
+                ("s_stride_row", ctypes.c_int64)]
+
+
 _P = ctypes.c_void_p
 _SIGS = {
     "qpa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -69,6 +79,7 @@ _SIGS = {
                                                  _P, ctypes.c_size_t, _P]),
     "uq_decode_hd256_combine": (ctypes.c_int, [ctypes.c_int, _P, ctypes.POINTER(UqDesc), _P,
                                                ctypes.c_size_t, _P]),
+    "nvfp4_index_score": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.POINTER(IdxDesc), _P]),
 }
 
 
@@ -267,3 +278,34 @@ def uq_decode_hd256_combine(num_partitions, out, desc, workspace, stream=None):
     st = load_library().uq_decode_hd256_combine(num_partitions, _ptr(out), ctypes.byref(desc), _ptr(workspace),
                                                 workspace.numel(), _stream(stream))
     _check("uq_decode_hd256_combine", st)
+
+
+# --------------------------------------------------------------------- nvfp4 index scorer
+def idx_desc(q_codes, pages, block_table, query_len, num_cols, scores=None):
+    RQ, H, D = q_codes.shape
+    assert D == 128 and RQ % query_len == 0
+    d = IdxDesc()
+    d.num_reqs, d.query_len, d.num_heads, d.head_dim = RQ // query_len, query_len, H, D
+    d.num_blocks, d.max_blocks_per_seq, d.num_cols = pages.shape[0], block_table.shape[1], num_cols
+    d.page_stride = pages.stride(0) * pages.element_size()
+    d.q_stride_tok, d.q_stride_head = q_codes.stride(0), q_codes.stride(1)
+    if scores is not None:
+        d.s_stride_head, d.s_stride_row = scores.stride(0), scores.stride(1)
+    return d
+
+
+def nvfp4_index_score(q_codes, pages, block_table, seq_lens, query_len: int, num_cols: int, scores=None,
+                      stream=None, desc=None):
+    """Paged NVFP4 index scores. q_codes uint8 (e4m3) [R*QL, H, 128]; pages
+    uint8 [NB, 9216]; returns float32 scores [H, R*QL, num_cols]."""
+    lib = load_library()
+    _need_cuda(q_codes, pages, block_table, seq_lens, scores)
+    if scores is None:
+        scores = torch.empty((q_codes.shape[1], q_codes.shape[0], num_cols), dtype=torch.float32,
+                             device=q_codes.device)
+    if desc is None:
+        desc = idx_desc(q_codes, pages, block_table, query_len, num_cols, scores)
+    st = lib.nvfp4_index_score(_ptr(q_codes), _ptr(pages), _ptr(block_table), _ptr(seq_lens), _ptr(scores),
+                               ctypes.byref(desc), _stream(stream))
+    _check("nvfp4_index_score", st)
+    return scores

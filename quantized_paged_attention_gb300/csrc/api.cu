@@ -108,6 +108,25 @@ int uq_check(const void* q, const uint8_t* kv, const float* cent, const int32_t*
   return QPA_OK;
 }
 
+// ------------------------------------------------------------------ nvfp4 scorer
+int idx_check(const uint8_t* q, const uint8_t* pages, const int32_t* bt, const int32_t* sl, const float* sc,
+              const qpa_idx_desc* d) {
+  if (!d) return QPA_ERR_NULL;
+  if (d->num_reqs < 0 || d->query_len < 1 || d->num_heads < 1 || d->head_dim != 128) return QPA_ERR_SHAPE;
+  if (d->query_len * d->num_heads > 16 || d->num_blocks < 1 || d->max_blocks_per_seq < 1 || d->num_cols < 1)
+    return QPA_ERR_SHAPE;
+  if ((long long)d->num_reqs * d->query_len > 0x7fffffffLL) return QPA_ERR_SHAPE;
+  if (d->num_reqs == 0) return QPA_OK;
+  if (!q || !pages || !bt || !sl || !sc) return QPA_ERR_NULL;
+  const long long ps = d->page_stride ? d->page_stride : 9216;
+  const long long qt = d->q_stride_tok ? d->q_stride_tok : (long long)d->num_heads * 128;
+  const long long qh = d->q_stride_head ? d->q_stride_head : 128;
+  if (ps < 9216) return QPA_ERR_SHAPE;
+  if ((ps % 16) || (qt % 16) || (qh % 16) || qt < 0 || qh < 0) return QPA_ERR_ALIGN;
+  if (!aligned(q, 16) || !aligned(pages, 16) || !aligned(sc, 4)) return QPA_ERR_ALIGN;
+  return QPA_OK;
+}
+
 }  // namespace
 }  // namespace qpa
 
@@ -295,6 +314,32 @@ int uq_decode_hd256(const void* q, const uint8_t* kv_cache, const float* centroi
                                  workspace_bytes, stream);
   if (st != QPA_OK) return st;
   return uq_decode_hd256_combine(num_partitions, out, d, workspace, workspace_bytes, stream);
+}
+
+int nvfp4_index_score(const uint8_t* q, const uint8_t* kv_pages, const int32_t* block_table,
+                      const int32_t* seq_lens, float* scores, const qpa_idx_desc* d, void* stream) {
+  const int st = idx_check(q, kv_pages, block_table, seq_lens, scores, d);
+  if (st != QPA_OK || d->num_reqs == 0) return st;
+  IdxLaunch a;
+  a.q = q;
+  a.pages = kv_pages;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.scores = scores;
+  a.page_stride = d->page_stride ? d->page_stride : 9216;
+  a.q_stride_tok = d->q_stride_tok ? d->q_stride_tok : (long long)d->num_heads * 128;
+  a.q_stride_head = d->q_stride_head ? d->q_stride_head : 128;
+  a.s_stride_row = d->s_stride_row ? d->s_stride_row : d->num_cols;
+  a.s_stride_head = d->s_stride_head ? d->s_stride_head : (long long)d->num_reqs * d->query_len * a.s_stride_row;
+  a.num_reqs = d->num_reqs;
+  a.query_len = d->query_len;
+  a.num_heads = d->num_heads;
+  a.max_blocks = d->max_blocks_per_seq;
+  a.num_cols = d->num_cols;
+  a.num_blocks = d->num_blocks;
+  a.num_sms = num_sms_current();
+  if (a.num_sms <= 0) return QPA_ERR_CUDA;
+  return launch_idx_score(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -49,6 +49,18 @@ struct UqLaunch {
   int num_sms;
 };
 
+struct IdxLaunch {
+  const uint8_t* q;
+  const uint8_t* pages;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* scores;
+  long long page_stride, q_stride_tok, q_stride_head;   // bytes
+  long long s_stride_head, s_stride_row;                // elements
+  int num_reqs, query_len, num_heads, max_blocks, num_cols, num_blocks;
+  int num_sms;
+};
+
 __device__ __forceinline__ void store4(float* dst, float a, float b, float c, float d) {
   *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
 }
@@ -64,5 +76,6 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t stream);
 cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream);
 cudaError_t launch_uq_combine(const CombineLaunch& a, cudaStream_t stream);
+cudaError_t launch_idx_score(const IdxLaunch& a, cudaStream_t stream);
 
 }  // namespace qpa

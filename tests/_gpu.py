@@ -107,3 +107,39 @@ def uq_v_absmax(c, s, h):
         return 0.0
     _, v = oracle.uq.dense_kv_uq(c.kv_cache, c.centroids, c.block_table, s, h, L)
     return float(np.abs(v).max())
+
+
+class IdxDev:
+    def __init__(self, c, device=None):
+        device = device or dev()
+        self.c = c
+        self.q = torch.from_numpy(c.q_codes).to(device)
+        self.pages = torch.from_numpy(c.pages).to(device)
+        self.bt = torch.from_numpy(c.block_table).to(device)
+        self.sl = torch.from_numpy(c.seq_lens).to(device)
+
+    def run(self, scores=None):
+        out = qpa.nvfp4_index_score(self.q, self.pages, self.bt, self.sl, self.c.query_len, self.c.num_cols,
+                                    scores=scores)
+        torch.cuda.synchronize()
+        assert qpa.kernel_error() == 0
+        return out
+
+
+def check_scores(got, ref, rows=None, what=""):
+    """got/ref [H, rows, S]: -inf must match exactly; finite values within
+    1e-4 * max(|ref|, mean |ref| of the row's finite scores)."""
+    if rows is not None:
+        got, ref = got[:, rows], ref[:, rows]
+    ninf = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), ninf), f"{what}: -inf pattern differs"
+    assert not np.any(np.isnan(got)), f"{what}: NaN in scores"
+    fin = ~ninf
+    with np.errstate(invalid="ignore"):
+        cnt = fin.sum(axis=2, keepdims=True)
+        rowsum = np.where(fin, np.abs(ref), 0.0).sum(axis=2, keepdims=True)
+        rowmean = np.where(cnt > 0, rowsum / np.maximum(cnt, 1), 0.0)
+        bound = SCORE_TOL * np.maximum(np.abs(ref), rowmean)
+        err = np.where(fin, np.abs(got - ref), 0.0)
+    bad = fin & (err > bound)
+    assert not np.any(bad), f"{what}: {int(bad.sum())} scores out of tolerance, worst {float(np.nanmax(np.where(fin, err / np.maximum(bound, 1e-30), np.nan))):.3g}x"

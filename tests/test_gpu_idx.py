@@ -1,0 +1,70 @@
+"""GPU parity of nvfp4_index_score against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu import IdxDev, check_scores
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _ref(c, reqs=None):
+    return oracle.nvfp4_index_score(c.q_codes, c.pages, c.block_table, c.seq_lens, c.query_len, c.num_cols,
+                                    reqs=reqs)
+
+
+@pytest.mark.parametrize("ql,h", [(4, 2), (1, 1), (2, 4), (3, 2), (4, 4)])
+def test_small_ragged(ql, h):
+    lens = [0, 1, 3, 4, 5, 127, 128, 129, 255, 256, 257, 1000]
+    c = synth.make_idx_case(300 + ql * 10 + h, lens, query_len=ql, num_heads=h, num_cols=12)
+    got = IdxDev(c).run().cpu().double().numpy()
+    check_scores(got, _ref(c), what=f"ql={ql} h={h}")
+
+
+def test_columns_beyond_blocks_and_table_width():
+    c = synth.make_idx_case(320, [300, 900], query_len=4, num_heads=2, num_cols=20)
+    got = IdxDev(c).run().cpu().double().numpy()
+    check_scores(got, _ref(c), what="wide")
+    assert np.all(np.isneginf(got[:, :, 8:]))
+
+
+def test_strided_scores_output():
+    c = synth.make_idx_case(321, [500, 40, 1300], query_len=4, num_heads=2, num_cols=11)
+    d = IdxDev(c)
+    big = torch.full((2, 12, 16), 7.0, device=d.q.device)
+    view = big[:, :, :11]
+    d.run(scores=view)
+    got = big.cpu().double().numpy()
+    check_scores(got[:, :, :11], _ref(c), what="strided")
+    assert np.all(got[:, :, 11:] == 7.0)      # nothing written outside the view
+
+
+def test_repeat_is_deterministic():
+    c = synth.make_idx_case(322, [4000, 2500], query_len=4, num_heads=2, num_cols=32)
+    d = IdxDev(c)
+    a = d.run().clone()
+    b = d.run()
+    assert torch.equal(a, b)
+
+
+def test_full_config_sampled():
+    """64 requests, lengths U[4096, 32768], query_len 4, 2 heads, S=256 (as
+    the benchmark runs it); 6 requests (incl. the shortest and longest)
+    against the oracle."""
+    c = synth.idx_full()
+    got = IdxDev(c).run().cpu().double().numpy()
+    assert not np.any(np.isnan(got))
+    rng = np.random.default_rng(5)
+    reqs = sorted(set(rng.choice(c.num_reqs, 4, replace=False).tolist()
+                      + [int(np.argmin(c.seq_lens)), int(np.argmax(c.seq_lens))]))
+    ref = _ref(c, reqs=reqs)
+    rows = [r * 4 + q for r in reqs for q in range(4)]
+    check_scores(got, ref, rows=rows, what="idx-full")
