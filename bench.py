@@ -42,9 +42,13 @@ def _args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-extra", action="store_true", help="skip the ragged-batch extra measurement")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads' measurements")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile-case", choices=["fp8", "uq", "uq_rand", "idx"], default=None,
+                    help="run only this case's kernels (warmup + steps launches) for a profiler; "
+                         "fp8: 8 seqs x 16384 (268 MB), uq: 4 seqs x 75000 (173 MB), "
+                         "idx: 128 requests (170 MB); prints one status line, not the bench line")
     return ap.parse_args()
 
 
@@ -220,6 +224,67 @@ def time_fp8(c, P, steps, warmup, dev, sampler=None):
     return total / steps, statistics.mean(part), total / steps - statistics.mean(part), 2 * steps, clocks, total
 
 
+def _time_loop(step_a, step_b, steps, warmup):
+    """Times `steps` back-to-back steps (step_a = partition or whole kernel,
+    step_b = combine or None). Returns (ms/step, mean ms of step_a)."""
+    import torch
+    for _ in range(warmup):
+        step_a()
+        if step_b:
+            step_b()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(steps):
+        ev[i][0].record()
+        step_a()
+        ev[i][1].record()
+        if step_b:
+            step_b()
+    end.record()
+    torch.cuda.synchronize()
+    _barrier()
+    return start.elapsed_time(end) / steps, statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def time_uq(c, P, steps, warmup, dev):
+    import numpy as np
+    import torch
+    import quantized_paged_attention_gb300 as qpa
+    q = torch.from_numpy(c.q_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    kv = torch.from_numpy(c.kv_cache).to(dev)
+    cent = torch.from_numpy(np.ascontiguousarray(c.centroids, dtype=np.float32)).to(dev)
+    bt = torch.from_numpy(c.block_table).to(dev)
+    sl = torch.from_numpy(c.seq_lens).to(dev)
+    desc = qpa.uq_desc(q, kv, bt, c.query_group, c.softmax_scale)
+    ws = qpa.alloc_workspace(qpa.uq_decode_hd256_workspace_size(desc, P), dev)
+    out = torch.empty((q.shape[0], q.shape[1], 256), dtype=torch.float32, device=dev)
+    r = _time_loop(lambda: qpa.uq_decode_hd256_partition(q, kv, cent, bt, sl, P, desc, ws),
+                   lambda: qpa.uq_decode_hd256_combine(P, out, desc, ws), steps, warmup)
+    if qpa.kernel_error() != 0:
+        raise RuntimeError("device error word raised during the benchmark")
+    return r
+
+
+def time_idx(c, steps, warmup, dev):
+    import torch
+    import quantized_paged_attention_gb300 as qpa
+    q = torch.from_numpy(c.q_codes).to(dev)
+    pages = torch.from_numpy(c.pages).to(dev)
+    bt = torch.from_numpy(c.block_table).to(dev)
+    sl = torch.from_numpy(c.seq_lens).to(dev)
+    scores = torch.empty((c.num_heads, q.shape[0], c.num_cols), dtype=torch.float32, device=dev)
+    desc = qpa.idx_desc(q, pages, bt, c.query_len, c.num_cols, scores)
+    r = _time_loop(lambda: qpa.nvfp4_index_score(q, pages, bt, sl, c.query_len, c.num_cols, scores=scores,
+                                                 desc=desc), None, steps, warmup)
+    if qpa.kernel_error() != 0:
+        raise RuntimeError("device error word raised during the benchmark")
+    return r
+
+
 def time_e2e(c, P, steps, dev):
     """The same decode through the C ABI from pinned host buffers: every step
     copies all inputs host->device, runs the step and copies the output back."""
@@ -280,6 +345,31 @@ def _max_over_ranks(x):
     return float(t.item())
 
 
+def _profile_case(a):
+    """Small cases (larger than L2) of each kernel for profiling runs."""
+    import numpy as np
+    import torch
+    import synth
+    dev = torch.device("cuda", 0)
+    if a.profile_case == "fp8":
+        c = synth.make_fp8_case(1001, [16384] * 8, 8, 8, 128, 16, poison=False)
+        ms, part, *_ = time_fp8(c, 32, a.steps, a.warmup, dev)
+        nbytes = c.kv_bytes
+    elif a.profile_case in ("uq", "uq_rand"):
+        cent = synth.sorted_random_centroids(5) if a.profile_case == "uq_rand" else None
+        c = synth.uq_full(centroids=cent)
+        ms, part = time_uq(c, 147, a.steps, a.warmup, dev)
+        nbytes = c.kv_bytes
+    else:
+        r = synth.rng(1104)
+        c = synth.make_idx_case(1004, r.integers(4096, 32769, size=128).astype(np.int32), 4, 2,
+                                num_cols=256, poison=False)
+        ms, part = time_idx(c, a.steps, a.warmup, dev)
+        nbytes = c.kv_bytes
+    print(f"profile case {a.profile_case}: {ms * 1e3:.1f} us/step, first kernel {part * 1e3:.1f} us, "
+          f"{nbytes / 1e6:.1f} MB, {nbytes / (part * 1e-3) / 1e9:.0f} GB/s")
+
+
 def main():
     a = _args()
     if a.warmup < 3:
@@ -322,6 +412,9 @@ def main():
     import torch
     import __graft_entry__
     __graft_entry__.build()
+    if a.profile_case:
+        _profile_case(a)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -357,6 +450,29 @@ def main():
             "kv_bytes": cr.kv_bytes, "gbs": round(cr.kv_bytes / (r_ms * 1e-3) / 1e9, 1),
             "frac_of_peak": round(cr.kv_bytes / (r_ms * 1e-3) / 1e9 / peak, 4)}
         del cr
+        esteps = max(20, a.steps // 4)
+        for name, cent in (("uq_hd256_b4_75k_e2m1", None), ("uq_hd256_b4_75k_randtable", "rand")):
+            cu = synth.uq_full(seed=1003 + rank, centroids=None if cent is None else synth.sorted_random_centroids(5))
+            u_ms, u_part = time_uq(cu, 147, esteps, a.warmup, dev)
+            u_ms = _max_over_ranks(u_ms)
+            extra[name] = {
+                "workload": "4-bit head_dim 256 decode, 4 seqs x 75000 tokens, 2 KV heads, group 8, block 64, "
+                            "288-byte slots, P=147, centroid table " + ("e2m1 values" if cent is None else
+                                                                         "seeded sorted random"),
+                "us_per_step": round(u_ms * 1e3, 2), "partition_us": round(u_part * 1e3, 2),
+                "kv_bytes": cu.kv_bytes, "gbs": round(cu.kv_bytes / (u_ms * 1e-3) / 1e9, 1),
+                "frac_of_peak": round(cu.kv_bytes / (u_ms * 1e-3) / 1e9 / peak, 4)}
+            del cu
+        ci = synth.idx_full(seed=1004 + rank)
+        i_ms, _ = time_idx(ci, esteps, a.warmup, dev)
+        i_ms = _max_over_ranks(i_ms)
+        extra["nvfp4_index_score_64req"] = {
+            "workload": "NVFP4 paged index scorer, 64 requests, lengths U[4096,32768], query_len 4, 2 heads, "
+                        "128-token pages of 72 B/token, S=256",
+            "us_per_step": round(i_ms * 1e3, 2), "kv_bytes": ci.kv_bytes,
+            "gbs": round(ci.kv_bytes / (i_ms * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(ci.kv_bytes / (i_ms * 1e-3) / 1e9 / peak, 4)}
+        del ci
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu:
