@@ -107,6 +107,25 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// The 8 copies of one 16-row x 128-byte K chunk and its V chunk (4 KB) into a
+// shared slot with the 128-byte XOR swizzle (chunk j of row r at j ^ (r & 7)).
+// Copy i (0..3) of K covers rows 4i..4i+3; lane l copies bytes 16 l of it.
+// d0 / d1 are the slot address plus this lane's swizzled offset for even /
+// odd i; src_k / src_v point at the chunk plus 16 l.
+__device__ __forceinline__ void cp_async_chunk_pair(uint32_t d0, uint32_t d1, const void* src_k,
+                                                    const void* src_v, uint64_t pol) {
+  asm volatile(
+      "cp.async.cg.shared.global.L2::cache_hint [%0], [%2], 16, %4;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%1+512], [%2+512], 16, %4;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%0+1024], [%2+1024], 16, %4;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%1+1536], [%2+1536], 16, %4;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%0+2048], [%3], 16, %4;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%1+2560], [%3+512], 16, %4;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%0+3072], [%3+1024], 16, %4;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%1+3584], [%3+1536], 16, %4;\n\t"
+      ::"r"(d0), "r"(d1), "l"(src_k), "l"(src_v), "l"(pol) : "memory");
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -15,13 +15,17 @@
 //  * every warp runs its own copy pipeline: 16-byte cp.async copies (L1
 //    bypass, L2 evict-first) of each slice's K and V chunks, 4 events deep,
 //    into a private shared-memory ring, XOR-swizzled so the fragment reads
-//    below are conflict-free. Query rows travel in the same event stream.
+//    below are conflict-free; the 8 copies of a slice use per-lane offsets
+//    computed once and immediate displacements. Query rows travel in the
+//    same event stream.
 //    There is no producer warp and no cross-warp handshake on the stream;
 //    the block table is read one tile group ahead.
-//  * QK runs on fp8 mma.sync (m16n8k32) straight from the e4m3 K bytes: each
-//    bf16 query row is scaled by a power of two and split exactly into two
-//    e4m3 pieces q = q_hi + q_lo (8 significant bits = 4 + 4), so no K byte is
-//    ever converted;
+//  * QK runs on f16 mma.sync (m16n8k16): K bytes are converted e4m3 -> f16
+//    (exact) in registers; each bf16 query row is scaled by a power of two so
+//    its largest element lands in [2^14, 2^15) and rounded to f16, which is
+//    exact for every element within 2^23 of the row maximum. (fp8 mma.sync
+//    on sm_103a is lowered to conversions plus f16 MMAs, about 11 issued
+//    instructions each, so converting K once here is cheaper.)
 //  * PV runs on f16 mma.sync (m16n8k16): V bytes are paired across tokens with
 //    prmt and converted to f16 (exact), P is rounded to f16 and transposed
 //    into the B operand with movmatrix;
@@ -106,7 +110,14 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   int i_L = 0, i_Lnext = 0;
   int i_seq = 0, i_kvh = 0, i_part = 0;
   int32_t i_ent = 0, i_nent = 0;  // table entries of the current / next tile group (lane j: entry j)
-  int rec_kind = 0, rec_a = 0, rec_b = 0;
+  size_t kvh_off = 0;              // byte offset of the KV head's chunk inside a block
+  int rec_a = 0, rec_b = 0;        // event record: (payload << 2) | kind, length
+  // per-lane constants of the slice copies (see cp_async_chunk_pair)
+  const int l3 = lane >> 3, j8 = lane & 7;
+  const uint32_t doff0 = l3 * D + ((j8 ^ l3) << 4);
+  const uint32_t doff1 = l3 * D + ((j8 ^ (l3 | 4)) << 4);
+  const uint32_t l16 = lane * 16;
+  const size_t blk_bytes = size_t(2) * p.num_kv_heads * head_bytes;   // one block: K and V of all heads
 
   auto load_len = [&](int item) -> int {
     if (item >= num_items) return 0;
@@ -132,6 +143,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         const int t = ik_item / P;
         i_kvh = t % p.num_kv_heads;
         i_seq = t / p.num_kv_heads;
+        kvh_off = size_t(i_kvh) * head_bytes;
         if (i_part * TG < i_L) {
           // query rows of (seq, kv_head): qg rows x 256 B, 16 B per copy
           const uint16_t* qrow0 = p.q + i_seq * p.q_stride_seq + (long long)(i_kvh * p.qg) * p.q_stride_head;
@@ -171,20 +183,13 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         if (lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
         phys = 0;
       }
-      const uint8_t* kb = p.kv + (size_t(phys) * 2 * p.num_kv_heads + i_kvh) * head_bytes +
-                          size_t((s * SLICE) & (bs - 1)) * D;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = 4 * i + (lane >> 3), j = lane & 7;
-        const uint32_t dst = slot + r * D + ((j ^ (r & 7)) << 4);
-        cp_async16(dst, kb + r * D + j * 16, pol);
-        cp_async16(dst + 2048, kb + v_off + r * D + j * 16, pol);
-      }
+      const uint8_t* kb = p.kv + size_t(phys) * blk_bytes + kvh_off + size_t((s * SLICE) & (bs - 1)) * D + l16;
+      cp_async_chunk_pair(slot + doff0, slot + doff1, kb, kb + v_off, pol);
       kind = EV_SLICE; a = s; b = i_L;
       break;
     }
     cp_async_commit();
-    if (lane == e % DEPTH) { rec_kind = kind; rec_a = a; rec_b = b; }
+    if (lane == e % DEPTH) { rec_a = (a << 2) | kind; rec_b = b; }
   };
 
   // ---------------------------------------------------------------- consume side
@@ -194,7 +199,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   const float vscale = __ldg(p.v_scale);
   const float base_scale = kscale * p.softmax_scale * kLog2e;
 
-  uint32_t qhi[NT][8], qlo[NT][8];
+  uint32_t qf[NT][16];   // query row 8nt+g, dims [32c, 32c+32), scaled, f16x2
   float rowc[NT][2];
   float o[NT][8][4];
   float m_run[NT][2], l_run[NT][2];
@@ -210,9 +215,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 
 #pragma unroll 1
   for (int e = 0;; ++e) {
-    const int kind = __shfl_sync(0xffffffffu, rec_kind, e % DEPTH);
-    const int ea = __shfl_sync(0xffffffffu, rec_a, e % DEPTH);
+    const int ra = __shfl_sync(0xffffffffu, rec_a, e % DEPTH);
     const int eb = __shfl_sync(0xffffffffu, rec_b, e % DEPTH);
+    const int kind = ra & 3, ea = ra >> 2;
 
     if (kind != EV_SLICE && cur_item >= 0) {
       // ---- end of the current item: merge the four warps' (m, l, O) in a
@@ -297,8 +302,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     if (kind == EV_ITEM) {
       cur_item = ea;
       const bool work = (ea % P) * TG < eb;
-      // ---- query fragments: q row r = 8*nt + g, dims [32c, 32c+32), split
-      // exactly into e4m3 hi + lo after scaling by a power of two.
+      // ---- query fragments: q row r = 8*nt + g, dims [32c, 32c+32), scaled
+      // by a power of two (largest element in [2^14, 2^15)) and rounded to f16
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int r = nt * 8 + g;
@@ -323,24 +328,16 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(x[k]));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        int a = 0;     // 2^a with amax * 2^a in [128, 256)
+        int a = 0;     // 2^a with amax * 2^a in [2^14, 2^15)
         if (amax > 0.f) {
           int ex;
           frexpf(amax, &ex);
-          a = max(-126, min(127, 8 - ex));
+          a = max(-126, min(127, 15 - ex));
         }
         const float up = __uint_as_float(uint32_t(127 + a) << 23);
         const float down = 1.0f / up;   // exact power of two
 #pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          const float x0 = x[k] * up, x1 = x[k + 1] * up, x2 = x[k + 2] * up, x3 = x[k + 3] * up;
-          const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
-          const uint32_t hf01 = e4m3x2_lo_to_f16x2(h01), hf23 = e4m3x2_lo_to_f16x2(h23);
-          const uint32_t l01 = f32x2_to_e4m3x2(x0 - f16_lo_to_f32(hf01), x1 - f16_hi_to_f32(hf01));
-          const uint32_t l23 = f32x2_to_e4m3x2(x2 - f16_lo_to_f32(hf23), x3 - f16_hi_to_f32(hf23));
-          qhi[nt][k / 4] = h01 | (h23 << 16);
-          qlo[nt][k / 4] = l01 | (l23 << 16);
-        }
+        for (int k = 0; k < 16; ++k) qf[nt][k] = f32x2_to_f16x2(x[2 * k] * up, x[2 * k + 1] * up);
         const float mine = down * base_scale;   // logit multiplier of row r
         rowc[nt][0] = __shfl_sync(0xffffffffu, mine, (2 * c) * 4);
         rowc[nt][1] = __shfl_sync(0xffffffffu, mine, (2 * c + 1) * 4);
@@ -402,14 +399,16 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      // S^T (16 tokens x 8 rows) = K (q_hi + q_lo)^T in two chains
+      // S^T (16 tokens x 8 rows) = K q^T; k-step ks covers dims 32c+4ks+{0,1} | {2,3},
+      // i.e. K word ks of rows g and g+8 (two chains)
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_e4m3_16832(sa, kr0[2 * ks], kr8[2 * ks], kr0[2 * ks + 1], kr8[2 * ks + 1],
-                       qhi[nt][2 * ks], qhi[nt][2 * ks + 1]);
-        mma_e4m3_16832(sb, kr0[2 * ks], kr8[2 * ks], kr0[2 * ks + 1], kr8[2 * ks + 1],
-                       qlo[nt][2 * ks], qlo[nt][2 * ks + 1]);
+      for (int ks = 0; ks < 8; ks += 2) {
+        mma_f16_16816(sa, e4m3x2_lo_to_f16x2(kr0[ks]), e4m3x2_lo_to_f16x2(kr8[ks]), e4m3x2_hi_to_f16x2(kr0[ks]),
+                      e4m3x2_hi_to_f16x2(kr8[ks]), qf[nt][2 * ks], qf[nt][2 * ks + 1]);
+        mma_f16_16816(sb, e4m3x2_lo_to_f16x2(kr0[ks + 1]), e4m3x2_lo_to_f16x2(kr8[ks + 1]),
+                      e4m3x2_hi_to_f16x2(kr0[ks + 1]), e4m3x2_hi_to_f16x2(kr8[ks + 1]), qf[nt][2 * ks + 2],
+                      qf[nt][2 * ks + 3]);
       }
       // logits (log2 units): token t0+g -> x0, x1; t0+g+8 -> x2, x3
       float x0 = (sa[0] + sb[0]) * rowc[nt][0];
