@@ -166,14 +166,8 @@ idx_score_kernel(const IdxParams p) {
         }
         const uint8_t* pg = p.pages + (long long)phys * p.page_stride;
         // 4096 B of codes + 512 B of scales of tokens [64 half, 64 half + 64)
-#pragma unroll
-        for (int i = 0; i < 9; ++i) {
-          const int c = lane + 32 * i;      // 288 chunks: 256 code chunks, 32 scale chunks
-          if (c < 256)
-            cp_async16(slot + c * 16, pg + ihalf * HALF_CODES + c * 16, pol);
-          else
-            cp_async16(slot + HALF_CODES + (c - 256) * 16, pg + PAGE_CODES + ihalf * HALF_SCALES + (c - 256) * 16, pol);
-        }
+        cp_async_halfpage(slot + 16 * lane, slot + HALF_CODES + 16 * lane, pg + ihalf * HALF_CODES + 16 * lane,
+                          pg + PAGE_CODES + ihalf * HALF_SCALES + 16 * lane, pol);
         kind = IEV_HALF; a = ir; bh = (ib << 1) | ihalf; lv = iL;
         if (ihalf == 1) {
           advance_page();

@@ -34,6 +34,7 @@
 //    order (deterministic) through each warp's just-consumed ring slot.
 #include "common.cuh"
 #include "qpa_internal.h"
+#include "combine.cuh"
 
 namespace qpa {
 
@@ -458,71 +459,25 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   cp_async_wait<0>();
 }
 
-// Flash-combine of the partitions ([PA] reduce kernel). One CTA of 128
-// threads per query row (seq, kv_head, row): M = max_p m_p, w_p = l_p e^(m_p-M),
-// out = sum_p w_p O_p / sum_p w_p. Threads split the partitions into
-// 128/(D/4) interleaved subsets and combine the subsets through shared memory.
-// Partitions with weight 0 (empty) are skipped.
+// Flash-combine of the partitions ([PA] reduce kernel): one CTA per query
+// row (seq, kv_head, r), see combine_row.
 template <typename OutT>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
                const float* __restrict__ part_l, OutT* __restrict__ out, int num_kv_heads, int qg,
-               int num_partitions, int d, long long out_stride_seq, long long out_stride_head) {
-  extern __shared__ float sw[];   // [P] weights, then [128] float4 partial sums
-  __shared__ float red[4];
+               int num_partitions, long long out_stride_seq, long long out_stride_head) {
+  extern __shared__ __align__(16) float sw[];
+  __shared__ __align__(16) float vec[fp8::D];
   pdl_wait_primary();
   const int row = blockIdx.x;                 // ((seq * Hk) + kvh) * qg + r
   const int r = row % qg;
   const int sk = row / qg;                    // seq * Hk + kvh
   const int seq = sk / num_kv_heads, kvh = sk % num_kv_heads;
-  const long long pbase = (long long)sk * num_partitions * qg + r;   // + pp * qg
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float M = -INFINITY;
-  for (int pp = tid; pp < num_partitions; pp += 128) M = fmaxf(M, part_m[pbase + (long long)pp * qg]);
-  for (int sh = 16; sh; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
-  // weights and their sum (the exponent argument is clamped; an empty
-  // partition, m = -inf, gives exactly 0)
-  float den = 0.f;
-  for (int pp = tid; pp < num_partitions; pp += 128) {
-    const float m = part_m[pbase + (long long)pp * qg];
-    const float w = (M == -INFINITY || m == -INFINITY)
-                        ? 0.f
-                        : part_l[pbase + (long long)pp * qg] * __expf(fmaxf(m - M, -80.f));
-    sw[pp] = w;
-    den += w;
-  }
-  for (int sh = 16; sh; sh >>= 1) den += __shfl_xor_sync(0xffffffffu, den, sh);
-  if (lane == 0) red[warp] = den;
-  __syncthreads();
-  den = red[0] + red[1] + red[2] + red[3];
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  const int nvec = d / 4;                     // float4 per row
-  const int nsub = 128 / nvec;                // partition subsets
-  const int v4 = tid % nvec, sub = tid / nvec;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* ob = part_o + ((long long)sk * num_partitions * qg + r) * d + 4 * v4;
-#pragma unroll 4
-  for (int pp = sub; pp < num_partitions; pp += nsub) {
-    const float w = sw[pp];
-    if (w != 0.f) {
-      const float4 o = __ldg(reinterpret_cast<const float4*>(ob + (long long)pp * qg * d));
-      acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-    }
-  }
-  float4* part = reinterpret_cast<float4*>(sw + ((num_partitions + 3) & ~3));
-  part[tid] = acc;
-  __syncthreads();
-  if (sub == 0) {
-    for (int s = 1; s < nsub; ++s) {
-      const float4 b = part[s * nvec + v4];
-      acc.x += b.x; acc.y += b.y; acc.z += b.z; acc.w += b.w;
-    }
-    OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + 4 * v4;
-    store4(dst, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  combine_row<fp8::D>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg, num_partitions, sw, vec);
+  if (threadIdx.x < fp8::D / 4) {
+    const int t = threadIdx.x;
+    OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + 4 * t;
+    store4(dst, vec[4 * t], vec[4 * t + 1], vec[4 * t + 2], vec[4 * t + 3]);
   }
 }
 
@@ -569,12 +524,12 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
 template <typename OutT>
 static cudaError_t launch_combine_t(const CombineLaunch& a, OutT* out, cudaStream_t stream) {
   const int grid = a.num_seqs * a.num_kv_heads * a.qg;
-  const size_t smem = (size_t((a.num_partitions + 3) & ~3) + 128 * 4) * sizeof(float);
-  if (smem > 48 * 1024)
+  const size_t smem = combine_smem_bytes(a.num_partitions);
+  if (smem > 40 * 1024)
     cudaFuncSetAttribute(combine_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -583,7 +538,7 @@ static cudaError_t launch_combine_t(const CombineLaunch& a, OutT* out, cudaStrea
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, combine_kernel<OutT>, a.part_o, a.part_m, a.part_l, out, a.num_kv_heads,
-                            a.qg, a.num_partitions, a.d, a.out_stride_seq, a.out_stride_head);
+                            a.qg, a.num_partitions, a.out_stride_seq, a.out_stride_head);
 }
 
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t stream) {

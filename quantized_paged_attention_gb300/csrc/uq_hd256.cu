@@ -28,6 +28,7 @@
 //    all of its V fragments of a token pair.
 #include "common.cuh"
 #include "qpa_internal.h"
+#include "combine.cuh"
 
 namespace qpa {
 
@@ -183,17 +184,11 @@ uq_partition_kernel(const UqParams p) {
         if (lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
         phys = 0;
       }
-      // 16 token slots of this KV head: 17 chunks of 16 B each
-      const uint8_t* s0 = p.kv + (size_t(phys) * bs + ((s * SLICE) & (bs - 1))) * tok_stride +
-                          size_t(i_kvh) * p.padded_slot;
-#pragma unroll
-      for (int i = 0; i < 9; ++i) {
-        const int idx = lane + 32 * i;
-        if (idx < SLICE * 17) {
-          const int r = idx / 17, ch = idx - r * 17;
-          cp_async16(slot + r * CONTENT + ch * 16, s0 + r * tok_stride + ch * 16, pol);
-        }
-      }
+      // 16 token slots of this KV head, 272 bytes each: lanes 2r and 2r+1 copy
+      // the alternate 16-byte chunks of token r
+      const uint8_t* tok = p.kv + (size_t(phys) * bs + ((s * SLICE) & (bs - 1)) + (lane >> 1)) * tok_stride +
+                           size_t(i_kvh) * p.padded_slot + 16 * (lane & 1);
+      cp_async_slot272(slot + (lane >> 1) * CONTENT + 16 * (lane & 1), tok, (lane & 1) == 0, pol);
       kind = UEV_SLICE; a = s; b = i_L;
       break;
     }
@@ -492,67 +487,23 @@ uq_partition_kernel(const UqParams p) {
   cp_async_wait<0>();
 }
 
-// Combine the partitions of one query row and rotate it back: out = o_r H/16.
+// Combine the partitions of one query row (combine_row) and rotate it back:
+// out = o_r H/16, 8 butterfly stages over the 256 dims, one pair per thread.
 template <typename OutT>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kCombineThreads)
 uq_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
                   const float* __restrict__ part_l, OutT* __restrict__ out, int num_kv_heads, int qg,
                   int num_partitions, long long out_stride_seq, long long out_stride_head) {
   constexpr int D = 256;
-  extern __shared__ float sw[];          // [P] weights, then [128] float4 partial sums
-  __shared__ float red[4];
-  __shared__ float vec[D];
+  extern __shared__ __align__(16) float sw[];
+  __shared__ __align__(16) float vec[D];
   pdl_wait_primary();
   const int row = blockIdx.x;
   const int r = row % qg;
   const int sk = row / qg;
   const int seq = sk / num_kv_heads, kvh = sk % num_kv_heads;
-  const long long pbase = (long long)sk * num_partitions * qg + r;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float M = -INFINITY;
-  for (int pp = tid; pp < num_partitions; pp += 128) M = fmaxf(M, part_m[pbase + (long long)pp * qg]);
-  for (int sh = 16; sh; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
-  float den = 0.f;
-  for (int pp = tid; pp < num_partitions; pp += 128) {
-    const float m = part_m[pbase + (long long)pp * qg];
-    const float w = (M == -INFINITY || m == -INFINITY)
-                        ? 0.f
-                        : part_l[pbase + (long long)pp * qg] * __expf(fmaxf(m - M, -80.f));
-    sw[pp] = w;
-    den += w;
-  }
-  for (int sh = 16; sh; sh >>= 1) den += __shfl_xor_sync(0xffffffffu, den, sh);
-  if (lane == 0) red[warp] = den;
-  __syncthreads();
-  den = red[0] + red[1] + red[2] + red[3];
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  const int v4 = tid & 63, sub = tid >> 6;   // 64 float4 per row, 2 partition subsets
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* ob = part_o + ((long long)sk * num_partitions * qg + r) * D + 4 * v4;
-#pragma unroll 4
-  for (int pp = sub; pp < num_partitions; pp += 2) {
-    const float w = sw[pp];
-    if (w != 0.f) {
-      const float4 o = __ldg(reinterpret_cast<const float4*>(ob + (long long)pp * qg * D));
-      acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-    }
-  }
-  float4* part = reinterpret_cast<float4*>(sw + ((num_partitions + 3) & ~3));
-  part[tid] = acc;
-  __syncthreads();
-  if (sub == 0) {
-    const float4 b = part[64 + v4];
-    vec[4 * v4 + 0] = (acc.x + b.x) * inv;
-    vec[4 * v4 + 1] = (acc.y + b.y) * inv;
-    vec[4 * v4 + 2] = (acc.z + b.z) * inv;
-    vec[4 * v4 + 3] = (acc.w + b.w) * inv;
-  }
-  __syncthreads();
-  // un-rotation: 8 butterfly stages over the 256 dims, one pair per thread
+  const int tid = threadIdx.x;
+  combine_row<D>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg, num_partitions, sw, vec);
   for (int st = 1; st < D; st <<= 1) {
     const int i = ((tid & ~(st - 1)) << 1) | (tid & (st - 1));   // index with bit `st` clear
     const float x = vec[i], y = vec[i + st];
@@ -561,7 +512,7 @@ uq_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ pa
     vec[i + st] = x - y;
     __syncthreads();
   }
-  if (tid < 64) {
+  if (tid < D / 4) {
     OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + 4 * tid;
     store4(dst, vec[4 * tid] * 0.0625f, vec[4 * tid + 1] * 0.0625f, vec[4 * tid + 2] * 0.0625f,
            vec[4 * tid + 3] * 0.0625f);
@@ -603,12 +554,12 @@ cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream) {
 template <typename OutT>
 static cudaError_t launch_uq_combine_t(const CombineLaunch& a, OutT* out, cudaStream_t stream) {
   const int grid = a.num_seqs * a.num_kv_heads * a.qg;
-  const size_t smem = (size_t((a.num_partitions + 3) & ~3) + 128 * 4) * sizeof(float);
+  const size_t smem = combine_smem_bytes(a.num_partitions);
   if (smem > 40 * 1024)
     cudaFuncSetAttribute(uq_combine_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
