@@ -7,57 +7,64 @@
 // reduce) and the partition map of the ultraquant_decode_hd256 page (STEP F:
 // partition p owns the 256-token tile groups p, p+P, p+2P, ...).
 //
-// GB300 design (not the pages' AMD design):
-//  * persistent CTAs of four warps, three per SM. Each CTA walks its work
-//    items (seq, kv_head, partition); inside an item warp w owns the 16-token
-//    slices 4k+w of every tile group, so each slice is one page chunk
-//    (block_size 16) or a 16-row piece of one (larger blocks).
-//  * every warp runs its own copy pipeline: 16-byte cp.async copies (L1
-//    bypass, L2 evict-first) of each slice's K and V chunks, 4 events deep,
-//    into a private shared-memory ring, XOR-swizzled so the fragment reads
-//    below are conflict-free; the 8 copies of a slice use per-lane offsets
-//    computed once and immediate displacements. Query rows travel in the
-//    same event stream.
-//    There is no producer warp and no cross-warp handshake on the stream;
-//    the block table is read one tile group ahead.
-//  * QK runs on f16 mma.sync (m16n8k16): K bytes are converted e4m3 -> f16
-//    (exact) in registers; each bf16 query row is scaled by a power of two so
-//    its largest element lands in [2^14, 2^15) and rounded to f16, which is
-//    exact for every element within 2^23 of the row maximum. (fp8 mma.sync
-//    on sm_103a is lowered to conversions plus f16 MMAs, about 11 issued
-//    instructions each, so converting K once here is cheaper.)
-//  * PV runs on f16 mma.sync (m16n8k16): V bytes are paired across tokens with
-//    prmt and converted to f16 (exact), P is rounded to f16 and transposed
-//    into the B operand with movmatrix;
-//  * each warp keeps its own online-softmax state; at the end of an item the
-//    four states are rescaled to the common maximum and summed in a fixed
-//    order (deterministic) through each warp's just-consumed ring slot.
+// GB300 design (not the pages' AMD design): one persistent CTA per SM with
+// three warp roles around the 5th-generation tensor core.
+//  * 4 copy warps stream the item's 128-token tiles (K 16 KB + V 16 KB) into a
+//    ring of shared-memory slots with per-lane 16-byte cp.async (a page chunk
+//    of block_size 16 is only 2 KB, far too small per copy for one TMA issuing
+//    thread), XOR-swizzled so that each slot is the 128-byte-swizzle canonical
+//    layout the tensor core reads; tokens past the sequence length are
+//    zero-filled. The copy warps also build the item's query operand.
+//  * 1 MMA warp issues tcgen05.mma kind::f8f6f4 straight on the e4m3 bytes:
+//    S^T = K Q'^T (M = 128 tokens, N = 32) and O^T = V^T P'^T (M = 128 dims,
+//    N = 32), accumulators in tensor memory (two S and two O buffers).
+//  * 4 softmax warps: thread t owns tensor-memory lane t, i.e. token t of an
+//    S tile and dim t of an O tile. They turn S into probabilities (online
+//    softmax across the item's tiles), write P' for the next MMA, and fold
+//    each O tile into per-dim register accumulators with the softmax rescale.
+// Exactness: the query (bf16) and the probabilities (f16) enter the fp8 MMA
+// as sums of e4m3 terms with power-of-two weights -- 4 terms for q (exact for
+// bf16 inputs), 3 terms for p (exact for its f16 value) -- so the tensor core
+// sees K and V unconverted and the products carry no fp8 rounding of q or p.
+// Every wait has a time limit; a timeout raises the error word and all roles
+// leave through the common teardown.
 #include "common.cuh"
 #include "qpa_internal.h"
 #include "combine.cuh"
+#include "tc.cuh"
 
 namespace qpa {
 
 namespace fp8 {
 constexpr int D = 128;          // head_dim
-constexpr int TG = 256;         // tile-group tokens
-constexpr int SLICE = 16;       // tokens per warp step (one mma M tile)
-constexpr int NW = 4;           // warps per CTA
-constexpr int THREADS = NW * 32;
-constexpr int DEPTH = 4;        // ring slots per warp (DEPTH-1 copy events in flight)
-constexpr int SLOT_BYTES = 4096;   // one slice (K 2 KB + V 2 KB) or one item's query rows
+constexpr int TG = 256;         // tile-group tokens (partition granule)
+constexpr int TILE = 128;       // tokens per MMA tile
+constexpr int TILE_BYTES = 2 * TILE * D;   // K tile then V tile
+constexpr int V_OFF = TILE * D;
+constexpr int WARP_PROD0 = 4, WARP_MMA = 8;
+constexpr int THREADS = 9 * 32;
 
 template <int NT>
 struct Smem {
+  static constexpr int NS = NT == 1 ? 6 : 5;       // ring slots (tiles)
+  static constexpr int R = 8 * NT;                 // query rows (padded)
+  static constexpr int NQ = 32 * NT;               // MMA N: 4 term slots x R rows
+  static constexpr int qBytes = NQ * D;            // Q' [NQ rows][128 dims] e4m3
+  static constexpr int pBytes = TILE * NQ;         // P'^T [128 tokens][NQ] e4m3
   static constexpr int ringOff = 0;
-  static constexpr int ringBytes = NW * DEPTH * SLOT_BYTES;
-  static constexpr int mOff = ringOff + ringBytes;                // [NW][8NT] f32 running max
-  static constexpr int lOff = mOff + NW * 8 * NT * 4;             // [NW][8NT] f32 running sum
-  static constexpr int fOff = lOff + NW * 8 * NT * 4;             // [NW] scratch-slot address
-  static constexpr int total = fOff + NW * 4;
+  static constexpr int qOff = NS * TILE_BYTES;
+  static constexpr int pOff = qOff + 2 * qBytes;
+  static constexpr int cOff = pOff + 2 * pBytes;           // [2][R] logit multiplier per row
+  static constexpr int redOff = cOff + 2 * R * 4;          // [2][4][R] tile maxima per warp
+  static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][4][R] row sums per warp
+  static constexpr int msmOff = lredOff + 2 * 4 * R * 4;   // [2][R] final row maxima
+  static constexpr int infoOff = msmOff + 2 * R * 4;       // [2] {item, L, tiles, partition}
+  static constexpr int barOff = (infoOff + 2 * 16 + 7) & ~7;
+  static constexpr int NBAR = 2 * NS + 2 * 10 + 1;
+  static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag
+  static constexpr int total = miscOff + 16 + 1024;        // + alignment slack
+  static constexpr int TMEM_COLS = 4 * NQ;                 // S[2], O[2]
 };
-template <int NT>
-constexpr int ctas_per_sm() { return NT == 1 ? 3 : 2; }
 }  // namespace fp8
 
 struct Fp8Params {
@@ -75,388 +82,603 @@ struct Fp8Params {
   float softmax_scale;
 };
 
-enum : int { EV_NONE = 0, EV_ITEM = 1, EV_SLICE = 2 };
+// Bounded mbarrier wait that also gives up as soon as another role aborted.
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int k = 0; k < 16; ++k)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicExch(&g_kernel_error, err);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int err) {
+  return __all_sync(0xffffffffu, role_wait(bar, parity, abort_flag, err));
+}
+
+// Max (or sum) of R values per lane over the warp's 32 lanes, by halving
+// exchanges: lane l ends with row (l >> (5 - log2 R)).
+template <int R, bool MAX>
+__device__ __forceinline__ float transpose_reduce(float (&a)[R], int lane) {
+  constexpr int LOG2R = R == 8 ? 3 : 4;
+#pragma unroll
+  for (int step = 0; step < LOG2R; ++step) {
+    const int off = 16 >> step;
+    const int half = R >> (step + 1);
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = up ? a[k] : a[k + half];
+      const float keep = up ? a[k + half] : a[k];
+      const float got = __shfl_xor_sync(0xffffffffu, send, off);
+      a[k] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+#pragma unroll
+  for (int off = 16 >> LOG2R; off >= 1; off >>= 1) {
+    const float got = __shfl_xor_sync(0xffffffffu, a[0], off);
+    a[0] = MAX ? fmaxf(a[0], got) : a[0] + got;
+  }
+  return a[0];
+}
+
+// Tiles of an item: partition `part` owns tile groups part, part+P, ...; each
+// tile group is two 128-token tiles, the second absent when it starts at or
+// past the length.
+__device__ __forceinline__ int item_tiles(int part, int P, int L) {
+  if (part * fp8::TG >= L) return 0;
+  const int ntg_seq = (L + fp8::TG - 1) / fp8::TG;
+  const int ntg = (ntg_seq - 1 - part) / P + 1;
+  const int last = part + (ntg - 1) * P;
+  return 2 * ntg - ((last * fp8::TG + fp8::TILE < L) ? 0 : 1);
+}
 
 template <int NT>
-__global__ void __launch_bounds__(fp8::THREADS, fp8::ctas_per_sm<NT>())
+__global__ void __launch_bounds__(fp8::THREADS, 1)
 pa_fp8_partition_kernel(const Fp8Params p) {
   using namespace fp8;
   using S = Smem<NT>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int R = S::R, NQ = S::NQ;
+  constexpr uint32_t IDESC_QK = idesc_e4m3(128, NQ, false, false);
+  constexpr uint32_t IDESC_PV = idesc_e4m3(128, NQ, true, true);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;     // swizzle atoms need 1024-byte alignment
+  uint8_t* sm = smem_raw + (sbase - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::barOff);
+  constexpr int NS = S::NS;
+  uint64_t* full = bars;              // [NS] tile copied (128 copy lanes)
+  uint64_t* empty = full + NS;        // [NS] tile consumed (MMA commit)
+  uint64_t* qfull = empty + NS;       // [2] Q' built (4 copy warps)
+  uint64_t* qempty = qfull + 2;       // [2] Q' consumed (MMA commit + 4 softmax warps)
+  uint64_t* sfull = qempty + 2;       // [2] S tile ready (MMA commit)
+  uint64_t* sfree = sfull + 2;        // [2] S tile read (4 softmax warps)
+  uint64_t* pfull = sfree + 2;        // [2] P' tile written (4 softmax warps)
+  uint64_t* ofull = pfull + 2;        // [2] O tile ready (MMA commit)
+  uint64_t* ofree = ofull + 2;        // [2] O tile read (4 softmax warps)
+  uint64_t* xbar = ofree + 2;         // [2] tile maxima exchanged (4 softmax warps)
+  uint64_t* lbar = xbar + 2;          // [2] row sums exchanged (4 softmax warps)
+  uint64_t* done = lbar + 2;          // [1] all MMAs finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::miscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::miscOff + 4);
+  const uint32_t cbuf_s = sbase + S::cOff;
+  const uint32_t red_s = sbase + S::redOff;
+  const uint32_t lred_s = sbase + S::lredOff;
+  const uint32_t msm_s = sbase + S::msmOff;
+  const uint32_t info_s = sbase + S::infoOff;
+  const uint32_t ring = sbase + S::ringOff;
+  const uint32_t qsm = sbase + S::qOff;
+  const uint32_t psm = sbase + S::pOff;
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_items = p.num_seqs * p.num_kv_heads * p.num_partitions;
-  const int P = p.num_partitions;
-  const int bs = p.block_size;
-  const int lbs = p.log2_bs;
-  const int bpt = TG / bs > 0 ? TG / bs : 1;      // table entries per tile group
-  float* ms = reinterpret_cast<float*>(smem + S::mOff);
-  float* ls = reinterpret_cast<float*>(smem + S::lOff);
-  uint32_t* fslot = reinterpret_cast<uint32_t*>(smem + S::fOff);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 128);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 4);
+      mbar_init(&qempty[i], 5);
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sfree[i], 4);
+      mbar_init(&pfull[i], 4);
+      mbar_init(&ofull[i], 1);
+      mbar_init(&ofree[i], 4);
+      mbar_init(&xbar[i], 4);
+      mbar_init(&lbar[i], 4);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_MMA) tmem_alloc(tmem_slot, S::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();   // the combine kernel waits for this grid before reading
 
-  const uint64_t pol = policy_evict_first();
-  const uint32_t ring = smem_u32(smem + S::ringOff) + warp * DEPTH * SLOT_BYTES;
-  const size_t head_bytes = size_t(bs) * D;                     // one (block, K/V, head) chunk
-  const size_t v_off = size_t(p.num_kv_heads) * head_bytes;     // K chunk -> V chunk
-
-  // ---------------------------------------------------------------- issue side
-  // The warp walks its own event stream: for every item of this CTA, an item
-  // event (copies the item's query rows) followed by the item's slices owned
-  // by this warp (slice 4k + warp of every tile group). Events are issued
-  // DEPTH-1 ahead of their use; lane (e % DEPTH) keeps event e's record.
-  int ik_item = blockIdx.x;       // global index of the issue cursor's item
-  int i_state = 0;                // 0: item event next, 1: slices next
-  int i_tg = 0, i_kk = 0;
-  int i_L = 0, i_Lnext = 0;
-  int i_seq = 0, i_kvh = 0, i_part = 0;
-  int32_t i_ent = 0, i_nent = 0;  // table entries of the current / next tile group (lane j: entry j)
-  size_t kvh_off = 0;              // byte offset of the KV head's chunk inside a block
-  int rec_a = 0, rec_b = 0;        // event record: (payload << 2) | kind, length
-  // per-lane constants of the slice copies (see cp_async_chunk_pair)
-  const int l3 = lane >> 3, j8 = lane & 7;
-  const uint32_t doff0 = l3 * D + ((j8 ^ l3) << 4);
-  const uint32_t doff1 = l3 * D + ((j8 ^ (l3 | 4)) << 4);
-  const uint32_t l16 = lane * 16;
-  const size_t blk_bytes = size_t(2) * p.num_kv_heads * head_bytes;   // one block: K and V of all heads
-
+  const int P = p.num_partitions;
+  const int Hk = p.num_kv_heads;
+  const int num_items = p.num_seqs * Hk * P;
+  const int G = gridDim.x;
+  const int bs = p.block_size;
+  const int lbs = p.log2_bs;
+  const int bpt = TG / bs;                  // table entries per tile group
   auto load_len = [&](int item) -> int {
     if (item >= num_items) return 0;
-    const int seq = item / (P * p.num_kv_heads);
+    const int seq = item / (P * Hk);
     return max(0, min(__ldg(p.seq_lens + seq), p.max_blocks * bs));
   };
-  auto load_entries = [&](int seq, int tg, int L) -> int32_t {
-    const int e = tg * bpt + lane;
-    int32_t v = 0;
-    if (lane < bpt && (e << lbs) < L) v = __ldg(p.block_table + (long long)seq * p.max_blocks + e);
-    return v;
-  };
-  if (ik_item < num_items) i_L = load_len(ik_item);
-  i_Lnext = load_len(ik_item + gridDim.x);
 
-  auto issue = [&](int e) {
-    const uint32_t slot = ring + (e % DEPTH) * SLOT_BYTES;
-    int kind = EV_NONE, a = 0, b = 0;
-    while (true) {
-      if (ik_item >= num_items) break;
-      if (i_state == 0) {
-        i_part = ik_item % P;
-        const int t = ik_item / P;
-        i_kvh = t % p.num_kv_heads;
-        i_seq = t / p.num_kv_heads;
-        kvh_off = size_t(i_kvh) * head_bytes;
-        if (i_part * TG < i_L) {
-          // query rows of (seq, kv_head): qg rows x 256 B, 16 B per copy
-          const uint16_t* qrow0 = p.q + i_seq * p.q_stride_seq + (long long)(i_kvh * p.qg) * p.q_stride_head;
-          for (int idx = lane; idx < p.qg * 16; idx += 32) {
-            const int row = idx >> 4, ch = idx & 15;
-            cp_async16(slot + row * 256 + ch * 16, qrow0 + row * p.q_stride_head + ch * 8, pol);
-          }
-          i_ent = load_entries(i_seq, i_part, i_L);
-          if ((i_part + P) * TG < i_L) i_nent = load_entries(i_seq, i_part + P, i_L);
-        }
-        i_state = 1;
-        i_tg = i_part;
-        i_kk = 0;
-        kind = EV_ITEM; a = ik_item; b = i_L;
-        break;
-      }
-      if (i_tg * TG >= i_L) {          // item exhausted: move to the CTA's next item
-        ik_item += gridDim.x;
-        i_state = 0;
-        i_L = i_Lnext;
-        i_Lnext = load_len(ik_item + gridDim.x);
-        continue;
-      }
-      const int s = (i_tg * TG) / SLICE + 4 * i_kk + warp;   // 16-token slice index in the sequence
-      const bool valid = s * SLICE < i_L;
-      int phys = __shfl_sync(0xffffffffu, i_ent, ((s * SLICE) & (TG - 1)) >> lbs);
-      if (++i_kk == 4) {               // next tile group of this item
-        i_kk = 0;
-        i_tg += P;
-        if (i_tg * TG < i_L) {
-          i_ent = i_nent;
-          if ((i_tg + P) * TG < i_L) i_nent = load_entries(i_seq, i_tg + P, i_L);
-        }
-      }
-      if (!valid) continue;
-      if (phys < 0 || phys >= p.num_blocks) {
-        if (lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
-        phys = 0;
-      }
-      const uint8_t* kb = p.kv + size_t(phys) * blk_bytes + kvh_off + size_t((s * SLICE) & (bs - 1)) * D + l16;
-      cp_async_chunk_pair(slot + doff0, slot + doff1, kb, kb + v_off, pol);
-      kind = EV_SLICE; a = s; b = i_L;
-      break;
-    }
-    cp_async_commit();
-    if (lane == e % DEPTH) { rec_a = (a << 2) | kind; rec_b = b; }
-  };
-
-  // ---------------------------------------------------------------- consume side
-  const int g = lane >> 2;      // fragment group id (row within 8)
-  const int c = lane & 3;       // thread within group
-  const float kscale = __ldg(p.k_scale);
-  const float vscale = __ldg(p.v_scale);
-  const float base_scale = kscale * p.softmax_scale * kLog2e;
-
-  uint32_t qf[NT][16];   // query row 8nt+g, dims [32c, 32c+32), scaled, f16x2
-  float rowc[NT][2];
-  float o[NT][8][4];
-  float m_run[NT][2], l_run[NT][2];
-  int cur_item = -1;
-
-  // Event e lives in slot e % DEPTH. Iteration e first refills the slot that
-  // iteration e-1 read (all lanes are past those reads: every iteration ends
-  // with __syncwarp), so DEPTH-1 events stay in flight while event e is
-  // computed. At an item boundary that slot, not yet refilled, is this warp's
-  // scratch for the merge.
-#pragma unroll 1
-  for (int e = 0; e < DEPTH - 1; ++e) issue(e);
-
-#pragma unroll 1
-  for (int e = 0;; ++e) {
-    const int ra = __shfl_sync(0xffffffffu, rec_a, e % DEPTH);
-    const int eb = __shfl_sync(0xffffffffu, rec_b, e % DEPTH);
-    const int kind = ra & 3, ea = ra >> 2;
-
-    if (kind != EV_SLICE && cur_item >= 0) {
-      // ---- end of the current item: merge the four warps' (m, l, O) in a
-      // fixed order and write this partition's partials.
-      const long long row0 = (long long)cur_item * p.qg;     // item index = (seq*Hk + kvh)*P + part
-      const uint32_t myfree = ring + ((e + DEPTH - 1) % DEPTH) * SLOT_BYTES;
+  if (warp < WARP_PROD0) {
+    // ======================================================== softmax warps
+    const int t = threadIdx.x;                         // tensor-memory lane
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    const float vscale = __ldg(p.v_scale);
+    const uint32_t ptok = psm + (t >> 3) * (8 * NQ) + (t & 7) * 16;   // this token's P' row
+    float m[R], l[R], o[R], c[R], alpha[R], pend_alpha[R];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+    for (int r = 0; r < R; ++r) { o[r] = 0.f; m[r] = -INFINITY; l[r] = 0.f; c[r] = 0.f; pend_alpha[r] = 0.f; }
+    int j = 0, qcnt = 0;
+    int pend_j = -1, pend_item = 0, pend_kpar = 0, pend_lph = 0;
+    bool pend_last = false, ok = true;
+
+    // O tile pend_j into the accumulators; at an item's last tile, write the
+    // item's partials.
+    auto correction = [&]() -> bool {
+      const int b = pend_j & 1;
+      if (!warp_wait(&ofull[b], (pend_j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) return false;
+      tc_fence_after();
+      float w[NQ];
 #pragma unroll
-        for (int sh = 4; sh < 32; sh <<= 1) {
-          l_run[nt][0] += __shfl_xor_sync(0xffffffffu, l_run[nt][0], sh);
-          l_run[nt][1] += __shfl_xor_sync(0xffffffffu, l_run[nt][1], sh);
+      for (int h = 0; h < NT; ++h) tmem_ld32(tl + 2 * NQ + b * NQ + 32 * h, *reinterpret_cast<float(*)[32]>(w + 32 * h));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ofree[b]);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float s = fmaf(fmaf(w[2 * R + r], 0.0625f, w[R + r]), 0.0625f, w[r]);
+        o[r] = fmaf(s, 0.00390625f, o[r] * pend_alpha[r]);
+      }
+      if (pend_last) {
+        if (!warp_wait(&lbar[pend_kpar], pend_lph, abort_flag, KERR_TIMEOUT_FULL)) return false;
+        const uint32_t lr = lred_s + pend_kpar * 4 * R * 4;
+        const long long row0 = (long long)pend_item * p.qg;
+        float lt[R];
+#pragma unroll
+        for (int q4 = 0; q4 < R / 4; ++q4) {
+          const float4 a0 = lds_f4(lr + 16 * q4), a1 = lds_f4(lr + 16 * (R / 4 + q4));
+          const float4 a2 = lds_f4(lr + 16 * (2 * R / 4 + q4)), a3 = lds_f4(lr + 16 * (3 * R / 4 + q4));
+          lt[4 * q4] = (a0.x + a1.x) + (a2.x + a3.x);
+          lt[4 * q4 + 1] = (a0.y + a1.y) + (a2.y + a3.y);
+          lt[4 * q4 + 2] = (a0.z + a1.z) + (a2.z + a3.z);
+          lt[4 * q4 + 3] = (a0.w + a1.w) + (a2.w + a3.w);
         }
-        if (g == 0) {
-          ms[warp * 8 * NT + nt * 8 + 2 * c] = m_run[nt][0];
-          ms[warp * 8 * NT + nt * 8 + 2 * c + 1] = m_run[nt][1];
-          ls[warp * 8 * NT + nt * 8 + 2 * c] = l_run[nt][0];
-          ls[warp * 8 * NT + nt * 8 + 2 * c + 1] = l_run[nt][1];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          // (lt >= 1: the row maximum's own term is exactly 1)
+          if (r < p.qg) p.part_o[(row0 + r) * D + t] = o[r] * (vscale * rcp_approx(lt[r]));
+          o[r] = 0.f;
+        }
+        if (t < p.qg) {
+          const float lrow = (ldsf(lr + 4 * t) + ldsf(lr + 4 * (R + t))) + (ldsf(lr + 4 * (2 * R + t)) + ldsf(lr + 4 * (3 * R + t)));
+          p.part_m[row0 + t] = ldsf(msm_s + pend_kpar * R * 4 + 4 * t) * kLn2;
+          p.part_l[row0 + t] = lrow;
         }
       }
-      if (lane == 0) fslot[warp] = myfree;
-      named_barrier(1, THREADS);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        // rescale this warp's O to the common row maximum and park it in the
-        // scratch slot as fp32 [8 rows][128 dims]; the dim is XOR-swizzled
-        // within its 16-group by (row >> 1, dim >> 5) so that both the
-        // fragment-order stores and the dim-order loads are conflict-free.
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int row = 2 * c + h;
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < NW; ++w) M = fmaxf(M, ms[w * 8 * NT + nt * 8 + row]);
-          const float sc = (m_run[nt][h] == -INFINITY) ? 0.f : ex2(m_run[nt][h] - M);
-          const int sw = (((g >> 1) & 3) | (c << 2));
-#pragma unroll
-          for (int mi = 0; mi < 8; ++mi) {
-            const int d0 = 16 * g + mi, d1 = 16 * g + 8 + mi;
-            stsf(myfree + (row * D + (d0 ^ sw)) * 4, o[nt][mi][h] * sc);
-            stsf(myfree + (row * D + (d1 ^ sw)) * 4, o[nt][mi][2 + h] * sc);
-          }
-        }
-        named_barrier(1, THREADS);
-        {
-          const int tid = threadIdx.x;   // = dim
-          uint32_t fs[NW];
-#pragma unroll
-          for (int w = 0; w < NW; ++w) fs[w] = fslot[w];
-          for (int r = 0; r < 8 && nt * 8 + r < p.qg; ++r) {
-            const int row = nt * 8 + r;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) M = fmaxf(M, ms[w * 8 * NT + row]);
-            float lsum = 0.f, acc = 0.f;
-            const int pd = tid ^ (((tid >> 5) & 3) | ((r >> 1) << 2));
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-              const float mw = ms[w * 8 * NT + row];
-              const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-              lsum += wt * ls[w * 8 * NT + row];
-              acc += ldsf(fs[w] + (r * D + pd) * 4);
-            }
-            p.part_o[(row0 + row) * D + tid] = lsum > 0.f ? acc / lsum * vscale : 0.f;
-            if (tid == 0) {
-              p.part_m[row0 + row] = M == -INFINITY ? -INFINITY : M * kLn2;
-              p.part_l[row0 + row] = lsum;
-            }
-          }
-        }
-        named_barrier(1, THREADS);
-      }
-      cur_item = -1;
-    }
+      return true;
+    };
 
-    if (kind == EV_NONE) break;
-    issue(e + DEPTH - 1);
-    cp_async_wait<DEPTH - 1>();
-    __syncwarp();
-    const uint32_t slot = ring + (e % DEPTH) * SLOT_BYTES;
-
-    if (kind == EV_ITEM) {
-      cur_item = ea;
-      const bool work = (ea % P) * TG < eb;
-      // ---- query fragments: q row r = 8*nt + g, dims [32c, 32c+32), scaled
-      // by a power of two (largest element in [2^14, 2^15)) and rounded to f16
+    // the copy warps publish each non-empty item (and a final entry with no
+    // tiles) with its query operand
+    while (ok) {
+      const int qb = qcnt & 1;
+      if (!warp_wait(&qfull[qb], (qcnt >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
+      const int4 inf = lds_i4(info_s + 16 * qb);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int r = nt * 8 + g;
-        float x[32];
-        if (work && r < p.qg) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 w4 = lds128(slot + r * 256 + 64 * c + 16 * j);
-            const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              x[8 * j + 2 * k] = __uint_as_float(ws[k] << 16);
-              x[8 * j + 2 * k + 1] = __uint_as_float(ws[k] & 0xffff0000u);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) x[k] = 0.f;
-        }
-        float amax = 0.f;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(x[k]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        int a = 0;     // 2^a with amax * 2^a in [2^14, 2^15)
-        if (amax > 0.f) {
-          int ex;
-          frexpf(amax, &ex);
-          a = max(-126, min(127, 15 - ex));
-        }
-        const float up = __uint_as_float(uint32_t(127 + a) << 23);
-        const float down = 1.0f / up;   // exact power of two
-#pragma unroll
-        for (int k = 0; k < 16; ++k) qf[nt][k] = f32x2_to_f16x2(x[2 * k] * up, x[2 * k + 1] * up);
-        const float mine = down * base_scale;   // logit multiplier of row r
-        rowc[nt][0] = __shfl_sync(0xffffffffu, mine, (2 * c) * 4);
-        rowc[nt][1] = __shfl_sync(0xffffffffu, mine, (2 * c + 1) * 4);
-        m_run[nt][0] = m_run[nt][1] = -INFINITY;
-        l_run[nt][0] = l_run[nt][1] = 0.f;
-#pragma unroll
-        for (int mi = 0; mi < 8; ++mi)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) o[nt][mi][k] = 0.f;
+      for (int q4 = 0; q4 < R / 4; ++q4) {
+        const float4 cv = lds_f4(cbuf_s + 4 * (qb * R + 4 * q4));
+        c[4 * q4] = cv.x;
+        c[4 * q4 + 1] = cv.y;
+        c[4 * q4 + 2] = cv.z;
+        c[4 * q4 + 3] = cv.w;
       }
       __syncwarp();
-      continue;   // (the __syncwarp above ends this iteration's reads of the slot)
-    }
-
-    // ---- EV_SLICE: 16 tokens [16*ea, 16*ea + 16) of the current item
-    const int t0 = ea * SLICE;
-    const int L = eb;
-    const bool partial = t0 + SLICE > L;
-    // K rows g and g+8, chunks 2c and 2c+1 (chunk j of row r is stored at j ^ (r & 7))
-    const uint4 ka0 = lds128(slot + g * D + (((2 * c) ^ g) << 4));
-    const uint4 ka1 = lds128(slot + g * D + (((2 * c + 1) ^ g) << 4));
-    const uint4 kb0 = lds128(slot + (g + 8) * D + (((2 * c) ^ g) << 4));
-    const uint4 kb1 = lds128(slot + (g + 8) * D + (((2 * c + 1) ^ g) << 4));
-    // V rows 2c, 2c+1, 2c+8, 2c+9, chunk g
-    uint4 v0 = lds128(slot + 2048 + (2 * c) * D + ((g ^ (2 * c)) << 4));
-    uint4 v1 = lds128(slot + 2048 + (2 * c + 1) * D + ((g ^ (2 * c + 1)) << 4));
-    uint4 v8 = lds128(slot + 2048 + (2 * c + 8) * D + ((g ^ (2 * c)) << 4));
-    uint4 v9 = lds128(slot + 2048 + (2 * c + 9) * D + ((g ^ (2 * c + 1)) << 4));
-    const uint32_t kr0[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
-    const uint32_t kr8[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
-    if (partial) {
-      // V bytes past the end may be NaN codes: zero them (0 * NaN = NaN)
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      if (t0 + 2 * c >= L) v0 = z;
-      if (t0 + 2 * c + 1 >= L) v1 = z;
-      if (t0 + 2 * c + 8 >= L) v8 = z;
-      if (t0 + 2 * c + 9 >= L) v9 = z;
-    }
-    // V^T A fragments (f16): dim 16g+dd, token pairs (2c,2c+1) -> [dd][0], (2c+8,2c+9) -> [dd][1]
-    uint32_t aT[16][2];
-    {
-      const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
-      const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
-      const uint32_t w8[4] = {v8.x, v8.y, v8.z, v8.w};
-      const uint32_t w9[4] = {v9.x, v9.y, v9.z, v9.w};
+      if (lane == 0) mbar_arrive(&qempty[qb]);
+      const int item = inf.x, L = inf.y, nt = inf.z, part = inf.w;
+      if (nt == 0) break;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t lo01 = prmt(w0[j], w1[j], 0x5140), hi01 = prmt(w0[j], w1[j], 0x7362);
-        const uint32_t lo89 = prmt(w8[j], w9[j], 0x5140), hi89 = prmt(w8[j], w9[j], 0x7362);
-        aT[4 * j + 0][0] = e4m3x2_lo_to_f16x2(lo01);
-        aT[4 * j + 1][0] = e4m3x2_hi_to_f16x2(lo01);
-        aT[4 * j + 2][0] = e4m3x2_lo_to_f16x2(hi01);
-        aT[4 * j + 3][0] = e4m3x2_hi_to_f16x2(hi01);
-        aT[4 * j + 0][1] = e4m3x2_lo_to_f16x2(lo89);
-        aT[4 * j + 1][1] = e4m3x2_hi_to_f16x2(lo89);
-        aT[4 * j + 2][1] = e4m3x2_lo_to_f16x2(hi89);
-        aT[4 * j + 3][1] = e4m3x2_hi_to_f16x2(hi89);
+      for (int r = 0; r < R; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
       }
-    }
+      const int lph = (qcnt >> 1) & 1;
+      for (int i = 0; i < nt; ++i) {
+        const int start = (part + (i >> 1) * P) * TG + (i & 1) * TILE;
+        const bool last = i == nt - 1;
+        const int b = j & 1;
+        // ---- softmax of tile j
+        if (!warp_wait(&sfull[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
+        tc_fence_after();
+        float v[NQ];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      // S^T (16 tokens x 8 rows) = K q^T; k-step ks covers dims 32c+4ks+{0,1} | {2,3},
-      // i.e. K word ks of rows g and g+8 (two chains)
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int h = 0; h < NT; ++h) tmem_ld32(tl + b * NQ + 32 * h, *reinterpret_cast<float(*)[32]>(v + 32 * h));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfree[b]);
+        const bool valid = start + t < L;
+        float x[R], xr[R];
 #pragma unroll
-      for (int ks = 0; ks < 8; ks += 2) {
-        mma_f16_16816(sa, e4m3x2_lo_to_f16x2(kr0[ks]), e4m3x2_lo_to_f16x2(kr8[ks]), e4m3x2_hi_to_f16x2(kr0[ks]),
-                      e4m3x2_hi_to_f16x2(kr8[ks]), qf[nt][2 * ks], qf[nt][2 * ks + 1]);
-        mma_f16_16816(sb, e4m3x2_lo_to_f16x2(kr0[ks + 1]), e4m3x2_lo_to_f16x2(kr8[ks + 1]),
-                      e4m3x2_hi_to_f16x2(kr0[ks + 1]), e4m3x2_hi_to_f16x2(kr8[ks + 1]), qf[nt][2 * ks + 2],
-                      qf[nt][2 * ks + 3]);
-      }
-      // logits (log2 units): token t0+g -> x0, x1; t0+g+8 -> x2, x3
-      float x0 = (sa[0] + sb[0]) * rowc[nt][0];
-      float x1 = (sa[1] + sb[1]) * rowc[nt][1];
-      float x2 = (sa[2] + sb[2]) * rowc[nt][0];
-      float x3 = (sa[3] + sb[3]) * rowc[nt][1];
-      if (partial) {
-        if (t0 + g >= L) { x0 = -INFINITY; x1 = -INFINITY; }
-        if (t0 + g + 8 >= L) { x2 = -INFINITY; x3 = -INFINITY; }
-      }
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-      for (int sh = 4; sh < 32; sh <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
-      }
-      const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-      if (__any_sync(0xffffffffu, (mn0 > m_run[nt][0]) || (mn1 > m_run[nt][1]))) {
-        const float a0 = ex2(m_run[nt][0] - mn0), a1 = ex2(m_run[nt][1] - mn1);
-        l_run[nt][0] *= a0;
-        l_run[nt][1] *= a1;
-#pragma unroll
-        for (int mi = 0; mi < 8; ++mi) {
-          o[nt][mi][0] *= a0; o[nt][mi][1] *= a1;
-          o[nt][mi][2] *= a0; o[nt][mi][3] *= a1;
+        for (int r = 0; r < R; ++r) {
+          const float s = fmaf(fmaf(fmaf(v[3 * R + r], 0.0625f, v[2 * R + r]), 0.0625f, v[R + r]), 0.0625f, v[r]);
+          x[r] = valid ? s * c[r] : -INFINITY;
+          xr[r] = x[r];
         }
-        m_run[nt][0] = mn0;
-        m_run[nt][1] = mn1;
-      }
-      const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
-      const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
-      const uint32_t P01 = f32x2_to_f16x2(p0, p1);
-      const uint32_t P23 = f32x2_to_f16x2(p2, p3);
-      // the sum uses the same f16-rounded probabilities the PV product sees
-      l_run[nt][0] += f16_lo_to_f32(P01) + f16_lo_to_f32(P23);
-      l_run[nt][1] += f16_hi_to_f32(P01) + f16_hi_to_f32(P23);
-      const uint32_t b0 = movmatrix_trans(P01);   // tokens 2c, 2c+1 of row g
-      const uint32_t b1 = movmatrix_trans(P23);   // tokens 2c+8, 2c+9 of row g
-      // O^T (dims x 8 rows) += V^T (dims x 16 tokens) P^T; m-tile mi holds
-      // dims 16g+mi (row g) and 16g+8+mi (row g+8)
+        {
+          const float mx = transpose_reduce<R, true>(xr, lane);
+          if ((lane & (32 / R - 1)) == 0) stsf(red_s + 4 * ((b * 4 + warp) * R + lane / (32 / R)), mx);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xbar[b]);
+        if (!warp_wait(&xbar[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
+        {
+          const uint32_t rb = red_s + b * 4 * R * 4;
 #pragma unroll
-      for (int mi = 0; mi < 8; ++mi)
-        mma_f16_16816(o[nt][mi], aT[mi][0], aT[mi + 8][0], aT[mi][1], aT[mi + 8][1], b0, b1);
+          for (int q4 = 0; q4 < R / 4; ++q4) {
+            const float4 a0 = lds_f4(rb + 16 * q4), a1 = lds_f4(rb + 16 * (R / 4 + q4));
+            const float4 a2 = lds_f4(rb + 16 * (2 * R / 4 + q4)), a3 = lds_f4(rb + 16 * (3 * R / 4 + q4));
+            const float tm[4] = {fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x)), fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y)),
+                                 fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z)), fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w))};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int r = 4 * q4 + u;
+              const float mn = fmaxf(m[r], tm[u]);
+              alpha[r] = ex2(m[r] - mn);
+              m[r] = mn;
+            }
+          }
+        }
+        // probabilities (f16), the row sums, and P' = 3 e4m3 terms of 256 p
+        uint32_t tw[3][R / 4];
+#pragma unroll
+        for (int k = 0; k < R / 2; ++k) {
+          const uint32_t p16 = f32x2_to_f16x2(ex2(x[2 * k] - m[2 * k]), ex2(x[2 * k + 1] - m[2 * k + 1]));
+          l[2 * k] = fmaf(l[2 * k], alpha[2 * k], f16_lo_to_f32(p16));
+          l[2 * k + 1] = fmaf(l[2 * k + 1], alpha[2 * k + 1], f16_hi_to_f32(p16));
+          uint32_t h = hmul2(p16, 0x5C005C00u);                      // x 256
+          const uint32_t e0 = f16x2_to_e4m3x2(h);
+          h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e0)), 0x4C004C00u);   // residual x 16
+          const uint32_t e1 = f16x2_to_e4m3x2(h);
+          h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e1)), 0x4C004C00u);
+          const uint32_t e2 = f16x2_to_e4m3x2(h);
+          if (k & 1) {
+            tw[0][k >> 1] |= e0 << 16;
+            tw[1][k >> 1] |= e1 << 16;
+            tw[2][k >> 1] |= e2 << 16;
+          } else {
+            tw[0][k >> 1] = e0;
+            tw[1][k >> 1] = e1;
+            tw[2][k >> 1] = e2;
+          }
+        }
+        {
+          const uint32_t pb = ptok + b * S::pBytes;
+          if constexpr (NT == 1) {
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(tw[0][0]), "r"(tw[0][1]),
+                         "r"(tw[1][0]), "r"(tw[1][1]) : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(tw[2][0]), "r"(tw[2][1]),
+                         "r"(0u), "r"(0u) : "memory");
+          } else {
+#pragma unroll
+            for (int q = 0; q < 3; ++q)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128 * q), "r"(tw[q][0]),
+                           "r"(tw[q][1]), "r"(tw[q][2]), "r"(tw[q][3]) : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 384), "r"(0u), "r"(0u), "r"(0u),
+                         "r"(0u) : "memory");
+          }
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull[b]);
+        if (last) {
+          // row sums over the item's 128 token lanes, and the final maxima
+          float lr[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r) lr[r] = l[r];
+          const float ls = transpose_reduce<R, false>(lr, lane);
+          if ((lane & (32 / R - 1)) == 0) stsf(lred_s + 4 * ((qb * 4 + warp) * R + lane / (32 / R)), ls);
+          if (t == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) stsf(msm_s + 4 * (qb * R + r), m[r]);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&lbar[qb]);
+        }
+        // ---- fold the previous O tile
+        if (pend_j >= 0 && !correction()) { ok = false; break; }
+        pend_j = j;
+        pend_last = last;
+        pend_item = item;
+        pend_kpar = qb;
+        pend_lph = lph;
+#pragma unroll
+        for (int r = 0; r < R; ++r) pend_alpha[r] = alpha[r];
+        ++j;
+      }
+      ++qcnt;
+    }
+    if (ok && pend_j >= 0) correction();
+  } else if (warp < WARP_MMA) {
+    // ======================================================== copy warps
+    const int pw = warp - WARP_PROD0;
+    const uint64_t pol = policy_evict_first();
+    const int l3 = lane >> 3, c8 = lane & 7;
+    const uint32_t doff_e = (uint32_t)((32 * pw + l3) * D + ((c8 ^ l3) << 4));
+    const uint32_t doff_o = (uint32_t)((32 * pw + l3) * D + ((c8 ^ (l3 + 4)) << 4));
+    const size_t head_bytes = size_t(bs) * D;
+    const size_t v_off = size_t(Hk) * head_bytes;
+    const size_t blk_bytes = 2 * v_off;
+    const int pt = 32 * pw + lane;                  // query-operand thread: row pt >> 4, dims 8 (pt & 15) ..
+    const int qrow = pt >> 4, h16 = pt & 15;
+    const float base_scale = __ldg(p.k_scale) * p.softmax_scale * kLog2e;
+    int j = 0, qcnt = 0;
+    bool ok = true;
+
+    auto load_q = [&](int item, uint4 (&qv)[NT]) {
+#pragma unroll
+      for (int h = 0; h < NT; ++h) qv[h] = make_uint4(0, 0, 0, 0);
+      if (item >= num_items) return;
+      const int t2 = item / P;
+      const int kvh = t2 % Hk, seq = t2 / Hk;
+#pragma unroll
+      for (int h = 0; h < NT; ++h) {
+        const int row = qrow + 8 * h;
+        if (row < p.qg)
+          qv[h] = __ldg(reinterpret_cast<const uint4*>(p.q + seq * p.q_stride_seq +
+                                                       (long long)(kvh * p.qg + row) * p.q_stride_head) + h16);
+      }
+    };
+    auto load_entries = [&](int item, int tg) -> int32_t {
+      if (item >= num_items) return 0;
+      const int seq = item / (P * Hk);
+      const int e = tg * bpt + lane;
+      return (lane < bpt && e < p.max_blocks) ? __ldg(p.block_table + (long long)seq * p.max_blocks + e) : 0;
+    };
+
+    int L = load_len(blockIdx.x);
+    uint4 qv[NT];
+    load_q(blockIdx.x, qv);
+    int32_t ent0 = load_entries(blockIdx.x, blockIdx.x % P);
+    for (int item = blockIdx.x; item < num_items && ok; item += G) {
+      const int part = item % P;
+      const int kvh = (item / P) % Hk;
+      const int nt = item_tiles(part, P, L);
+      // next item's length, query rows and first table entries
+      const int Lnext = load_len(item + G);
+      uint4 qn[NT];
+      load_q(item + G, qn);
+      const int32_t ent0n = load_entries(item + G, (item + G) % P);
+      if (nt == 0) {
+        // an empty partition (starts past the length): weight 0 in the combine
+        const long long row0 = (long long)item * p.qg;
+        for (int r = 0; r < p.qg; ++r) p.part_o[(row0 + r) * D + pt] = 0.f;
+        if (pt < p.qg) {
+          p.part_m[row0 + pt] = -INFINITY;
+          p.part_l[row0 + pt] = 0.f;
+        }
+      } else {
+        // ---- query operand: 4 e4m3 terms of q 2^a (a per row: max |q| 2^a in [128, 256))
+        const int qb = qcnt & 1;
+        if (qcnt >= 2 && !warp_wait(&qempty[qb], ((qcnt >> 1) - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int h = 0; h < NT; ++h) {
+          const int row = qrow + 8 * h;
+          const uint32_t ws[4] = {qv[h].x, qv[h].y, qv[h].z, qv[h].w};
+          float x[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            x[2 * k] = __uint_as_float(ws[k] << 16);
+            x[2 * k + 1] = __uint_as_float(ws[k] & 0xffff0000u);
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
+#pragma unroll
+          for (int sh = 1; sh < 16; sh <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
+          int a = 0;
+          if (amax > 0.f) {
+            int ex;
+            frexpf(amax, &ex);
+            a = max(-126, min(126, 8 - ex));
+          }
+          const float up = __uint_as_float(uint32_t(127 + a) << 23);
+          const float down = __uint_as_float(uint32_t(127 - a) << 23);   // 1 / up, exact
+#pragma unroll
+          for (int k = 0; k < 8; ++k) x[k] *= up;
+#pragma unroll
+          for (int term = 0; term < 4; ++term) {
+            uint32_t e[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              e[k] = f32x2_to_e4m3x2(x[2 * k], x[2 * k + 1]);
+              if (term < 3) {
+                const uint32_t back = e4m3x2_lo_to_f16x2(e[k]);
+                x[2 * k] = (x[2 * k] - f16_lo_to_f32(back)) * 16.f;
+                x[2 * k + 1] = (x[2 * k + 1] - f16_hi_to_f32(back)) * 16.f;
+              }
+            }
+            const int rr = term * R + row;
+            const uint32_t addr = qsm + qb * S::qBytes + rr * D + (((h16 >> 1) ^ (rr & 7)) << 4) + 8 * (h16 & 1);
+            asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(e[0] | (e[1] << 16)),
+                         "r"(e[2] | (e[3] << 16)) : "memory");
+          }
+          if (h16 == 0) stsf(cbuf_s + 4 * (qb * R + row), row < p.qg ? base_scale * down : 0.f);
+        }
+        if (pt == 0) sts_i4(info_s + 16 * qb, make_int4(item, L, nt, part));
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qfull[qb]);
+        ++qcnt;
+
+        // ---- K/V tiles: this warp copies tokens [32 pw, 32 pw + 32) of each
+        const size_t kvh_off = size_t(kvh) * head_bytes;
+        int32_t ent = ent0, nent = 0;
+        for (int i = 0; i < nt; ++i) {
+          const int tg = part + (i >> 1) * P;
+          if ((i & 1) == 0) {
+            if (i > 0) ent = nent;
+            nent = (i + 2 < nt) ? load_entries(item, tg + P) : 0;
+          }
+          const int s = j % NS;
+          const int rnd = j / NS;
+          if (rnd > 0 && !warp_wait(&empty[s], (rnd - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const int tok0 = tg * TG + (i & 1) * TILE + 32 * pw;
+          int pa = __shfl_sync(0xffffffffu, ent, (tok0 & (TG - 1)) >> lbs);
+          int pb = __shfl_sync(0xffffffffu, ent, ((tok0 + 16) & (TG - 1)) >> lbs);
+          if (pa < 0 || pa >= p.num_blocks) {
+            if (tok0 < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+            pa = 0;
+          }
+          if (pb < 0 || pb >= p.num_blocks) {
+            if (tok0 + 16 < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+            pb = 0;
+          }
+          const uint8_t* ka = p.kv + size_t(pa) * blk_bytes + kvh_off + size_t(tok0 & (bs - 1)) * D + l3 * D + c8 * 16;
+          const uint8_t* kb = bs == 16 ? p.kv + size_t(pb) * blk_bytes + kvh_off + l3 * D + c8 * 16 : ka + 16 * D;
+          const uint32_t slot = ring + s * TILE_BYTES;
+#pragma unroll
+          for (int ii = 0; ii < 8; ++ii) {
+            const bool valid = tok0 + l3 + 4 * ii < L;
+            const uint8_t* src = ii < 4 ? ka + 512 * ii : kb + 512 * (ii - 4);
+            const uint32_t dst = slot + ((ii & 1) ? doff_o : doff_e) + 512 * ii;
+            cp_async16_zfill(dst, src, valid, pol);
+            cp_async16_zfill(dst + V_OFF, src + v_off, valid, pol);
+          }
+          // the slot's barrier counts this lane once all its copies so far have landed
+          cp_async_arrive_noinc(&full[s]);
+          ++j;
+        }
+      }
+      L = Lnext;
+#pragma unroll
+      for (int h = 0; h < NT; ++h) qv[h] = qn[h];
+      ent0 = ent0n;
+    }
+    if (ok) {
+      // final entry: no more items
+      const int qb = qcnt & 1;
+      if (qcnt < 2 || warp_wait(&qempty[qb], ((qcnt >> 1) - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) {
+        if (pt == 0) sts_i4(info_s + 16 * qb, make_int4(0, 0, 0, 0));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qfull[qb]);
+      }
+    }
+    cp_async_wait_all();
+  } else {
+    // ======================================================== MMA warp
+    // A polling scheduler: issue whichever of the next PV (tile pv_j) and the
+    // next QK (tile qk_j) has its operands ready, so neither waits behind the
+    // other. Gives up after kWaitLimitNs without progress.
+    if (lane == 0) {
+      int qk_j = 0, pv_j = 0, qcnt = 0;
+      int it_i = 0, it_n = 0, qb = 0;      // QK cursor: tile within the item, the item's tiles, its operand buffer
+      bool qk_done = false;
+      unsigned long long t_prog = globaltimer();
+      while (true) {
+        // the next published item, once its query operand is ready
+        if (!qk_done && it_i >= it_n && mbar_test_wait(&qfull[qcnt & 1], (qcnt >> 1) & 1)) {
+          qb = qcnt & 1;
+          it_n = lds_i4(info_s + 16 * qb).z;
+          it_i = 0;
+          if (it_n == 0) qk_done = true;
+          ++qcnt;
+        }
+        if (qk_done && pv_j == qk_j) break;
+        bool progressed = false;
+        if (pv_j < qk_j) {
+          const int b = pv_j & 1, s = pv_j % NS;
+          if (mbar_test_wait(&pfull[b], (pv_j >> 1) & 1) &&
+              (pv_j < 2 || mbar_test_wait(&ofree[b], ((pv_j >> 1) - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t va = ring + s * TILE_BYTES + V_OFF;
+            const uint32_t pa = psm + b * S::pBytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_e4m3(tmem + 2 * NQ + b * NQ, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
+                       umma_desc(pa + k * 32 * NQ, 8 * NQ, 128, kSwizzleNone), IDESC_PV, k);
+            umma_commit(&ofull[b]);
+            umma_commit(&empty[s]);
+            ++pv_j;
+            progressed = true;
+          }
+        }
+        if (!qk_done) {
+          const int s = qk_j % NS, b = qk_j & 1;
+          if (it_i < it_n && mbar_test_wait(&full[s], (qk_j / NS) & 1) &&
+              (qk_j < 2 || mbar_test_wait(&sfree[b], ((qk_j >> 1) - 1) & 1))) {
+            fence_proxy_async();     // the copied bytes (generic proxy) become visible to the tensor core
+            tc_fence_after();
+            const uint32_t ka = ring + s * TILE_BYTES;
+            const uint32_t qa = qsm + qb * S::qBytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_e4m3(tmem + b * NQ, umma_desc(ka + 32 * k, 16, 1024, kSwizzle128B),
+                       umma_desc(qa + 32 * k, 16, 1024, kSwizzle128B), IDESC_QK, k);
+            umma_commit(&sfull[b]);
+            if (it_i == it_n - 1) umma_commit(&qempty[qb]);
+            ++it_i;
+            ++qk_j;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_prog = globaltimer();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer() - t_prog > kWaitLimitNs) {
+            atomicExch(&g_kernel_error, KERR_TIMEOUT_FULL);
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+      // every issued MMA must finish before the tensor memory is released
+      umma_commit(done);
+      if (!mbar_try_wait(done, 0)) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(done, 0)) {
+          if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicExch(&g_kernel_error, KERR_TIMEOUT_FULL);
+            break;
+          }
+        }
+      }
     }
     __syncwarp();
   }
-  cp_async_wait<0>();
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::TMEM_COLS);
+  }
 }
 
 // Flash-combine of the partitions ([PA] reduce kernel): one CTA per query
@@ -507,14 +729,13 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
   p.softmax_scale = a.softmax_scale;
   const long long items = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   if (items <= 0) return cudaSuccess;
+  const int grid = (int)std::min<long long>(items, (long long)a.num_sms);
   if (a.qg <= 8) {
     const int smem = fp8::Smem<1>::total;
-    const int grid = (int)std::min<long long>(items, (long long)fp8::ctas_per_sm<1>() * a.num_sms);
     cudaFuncSetAttribute(pa_fp8_partition_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     pa_fp8_partition_kernel<1><<<grid, fp8::THREADS, smem, stream>>>(p);
   } else {
     const int smem = fp8::Smem<2>::total;
-    const int grid = (int)std::min<long long>(items, (long long)fp8::ctas_per_sm<2>() * a.num_sms);
     cudaFuncSetAttribute(pa_fp8_partition_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     pa_fp8_partition_kernel<2><<<grid, fp8::THREADS, smem, stream>>>(p);
   }
