@@ -41,11 +41,13 @@ constexpr int TG = 256;         // tile-group tokens (partition granule)
 constexpr int TILE = 128;       // tokens per MMA tile
 constexpr int TILE_BYTES = 2 * TILE * D;   // K tile then V tile
 constexpr int V_OFF = TILE * D;
-constexpr int WARP_PROD0 = 4, WARP_MMA = 8;
-constexpr int THREADS = 9 * 32;
 
 template <int NT>
 struct Smem {
+  static constexpr int NWG = NT == 1 ? 2 : 1;      // softmax warp groups
+  static constexpr int WARP_PROD0 = 4 * NWG;       // 4 copy warps
+  static constexpr int WARP_MMA = WARP_PROD0 + 4;  // 1 MMA warp
+  static constexpr int THREADS = (WARP_MMA + 1) * 32;
   static constexpr int NS = NT == 1 ? 6 : 5;       // ring slots (tiles)
   static constexpr int R = 8 * NT;                 // query rows (padded)
   static constexpr int NQ = 32 * NT;               // MMA N: 4 term slots x R rows
@@ -54,15 +56,17 @@ struct Smem {
   static constexpr int ringOff = 0;
   static constexpr int qOff = NS * TILE_BYTES;
   static constexpr int pOff = qOff + 2 * qBytes;
-  static constexpr int cOff = pOff + 2 * pBytes;           // [2][R] logit multiplier per row
+  static constexpr int stgOff = pOff + 2 * pBytes;         // [2][R][128] f32 second group's O
+  static constexpr int cOff = stgOff + (NWG == 2 ? 2 * R * D * 4 : 0);   // [2][R] logit multiplier per row
   static constexpr int redOff = cOff + 2 * R * 4;          // [2][4][R] tile maxima per warp
-  static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][4][R] row sums per warp
-  static constexpr int msmOff = lredOff + 2 * 4 * R * 4;   // [2][R] final row maxima
-  static constexpr int infoOff = msmOff + 2 * R * 4;       // [2] {item, L, tiles, partition}
+  static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][4 NWG][R] row sums per warp
+  static constexpr int msmOff = lredOff + 2 * 4 * NWG * R * 4;   // [2][NWG][R] row maxima per group
+  static constexpr int infoOff = msmOff + 2 * NWG * R * 4; // [2] {item, L, tiles, partition}
   static constexpr int barOff = (infoOff + 2 * 16 + 7) & ~7;
   static constexpr int NBAR = 2 * NS + 2 * 10 + 1;
   static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag
   static constexpr int total = miscOff + 16 + 1024;        // + alignment slack
+  static_assert(total <= 227 * 1024, "shared memory");
   static constexpr int TMEM_COLS = 4 * NQ;                 // S[2], O[2]
 };
 }  // namespace fp8
@@ -140,11 +144,12 @@ __device__ __forceinline__ int item_tiles(int part, int P, int L) {
 }
 
 template <int NT>
-__global__ void __launch_bounds__(fp8::THREADS, 1)
+__global__ void __launch_bounds__(fp8::Smem<NT>::THREADS, 1)
 pa_fp8_partition_kernel(const Fp8Params p) {
   using namespace fp8;
   using S = Smem<NT>;
-  constexpr int R = S::R, NQ = S::NQ;
+  constexpr int R = S::R, NQ = S::NQ, NWG = S::NWG;
+  constexpr int WARP_PROD0 = S::WARP_PROD0, WARP_MMA = S::WARP_MMA;
   constexpr uint32_t IDESC_QK = idesc_e4m3(128, NQ, false, false);
   constexpr uint32_t IDESC_PV = idesc_e4m3(128, NQ, true, true);
   extern __shared__ uint8_t smem_raw[];
@@ -156,15 +161,15 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   uint64_t* full = bars;              // [NS] tile copied (128 copy lanes)
   uint64_t* empty = full + NS;        // [NS] tile consumed (MMA commit)
   uint64_t* qfull = empty + NS;       // [2] Q' built (4 copy warps)
-  uint64_t* qempty = qfull + 2;       // [2] Q' consumed (MMA commit + 4 softmax warps)
+  uint64_t* qempty = qfull + 2;       // [2] Q' consumed (MMA commit + softmax warps)
   uint64_t* sfull = qempty + 2;       // [2] S tile ready (MMA commit)
   uint64_t* sfree = sfull + 2;        // [2] S tile read (4 softmax warps)
   uint64_t* pfull = sfree + 2;        // [2] P' tile written (4 softmax warps)
   uint64_t* ofull = pfull + 2;        // [2] O tile ready (MMA commit)
-  uint64_t* ofree = ofull + 2;        // [2] O tile read (4 softmax warps)
-  uint64_t* xbar = ofree + 2;         // [2] tile maxima exchanged (4 softmax warps)
-  uint64_t* lbar = xbar + 2;          // [2] row sums exchanged (4 softmax warps)
-  uint64_t* done = lbar + 2;          // [1] all MMAs finished
+  uint64_t* xbar = ofull + 2;         // [2] tile maxima exchanged (4 softmax warps)
+  uint64_t* merge = xbar + 2;         // [2] item states published (softmax warps)
+  uint64_t* mfree = merge + 2;        // [2] item states read (first group's 4 warps)
+  uint64_t* done = mfree + 2;         // [1] all MMAs finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::miscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::miscOff + 4);
   const uint32_t cbuf_s = sbase + S::cOff;
@@ -172,6 +177,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   const uint32_t lred_s = sbase + S::lredOff;
   const uint32_t msm_s = sbase + S::msmOff;
   const uint32_t info_s = sbase + S::infoOff;
+  const uint32_t stg_s = sbase + S::stgOff;
   const uint32_t ring = sbase + S::ringOff;
   const uint32_t qsm = sbase + S::qOff;
   const uint32_t psm = sbase + S::pOff;
@@ -185,16 +191,16 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 4);
-      mbar_init(&qempty[i], 5);
+      mbar_init(&qempty[i], 1 + 4 * NWG);
       mbar_init(&sfull[i], 1);
       mbar_init(&sfree[i], 4);
       mbar_init(&pfull[i], 4);
       mbar_init(&ofull[i], 1);
-      mbar_init(&ofree[i], 4);
       mbar_init(&xbar[i], 4);
-      mbar_init(&lbar[i], 4);
+      mbar_init(&merge[i], 4 * NWG);
+      mbar_init(&mfree[i], 4);
     }
-    mbar_init(done, 1);
+    mbar_init(done, 1 + NWG);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -220,63 +226,19 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 
   if (warp < WARP_PROD0) {
     // ======================================================== softmax warps
-    const int t = threadIdx.x;                         // tensor-memory lane
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    // NWG groups of 4 warps; with two groups, group g takes the tiles j with
+    // j & 1 == g (buffer b = g) and the groups merge their states per item.
+    const int wg = warp >> 2;
+    const int wq = warp & 3;                           // lane quarter of tensor memory
+    const int t = threadIdx.x & 127;                   // tensor-memory lane
+    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
     const float vscale = __ldg(p.v_scale);
     const uint32_t ptok = psm + (t >> 3) * (8 * NQ) + (t & 7) * 16;   // this token's P' row
-    float m[R], l[R], o[R], c[R], alpha[R], pend_alpha[R];
+    float m[R], l[R], o[R], c[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) { o[r] = 0.f; m[r] = -INFINITY; l[r] = 0.f; c[r] = 0.f; pend_alpha[r] = 0.f; }
+    for (int r = 0; r < R; ++r) { o[r] = 0.f; m[r] = -INFINITY; l[r] = 0.f; c[r] = 0.f; }
     int j = 0, qcnt = 0;
-    int pend_j = -1, pend_item = 0, pend_kpar = 0, pend_lph = 0;
-    bool pend_last = false, ok = true;
-
-    // O tile pend_j into the accumulators; at an item's last tile, write the
-    // item's partials.
-    auto correction = [&]() -> bool {
-      const int b = pend_j & 1;
-      if (!warp_wait(&ofull[b], (pend_j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) return false;
-      tc_fence_after();
-      float w[NQ];
-#pragma unroll
-      for (int h = 0; h < NT; ++h) tmem_ld32(tl + 2 * NQ + b * NQ + 32 * h, *reinterpret_cast<float(*)[32]>(w + 32 * h));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ofree[b]);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float s = fmaf(fmaf(w[2 * R + r], 0.0625f, w[R + r]), 0.0625f, w[r]);
-        o[r] = fmaf(s, 0.00390625f, o[r] * pend_alpha[r]);
-      }
-      if (pend_last) {
-        if (!warp_wait(&lbar[pend_kpar], pend_lph, abort_flag, KERR_TIMEOUT_FULL)) return false;
-        const uint32_t lr = lred_s + pend_kpar * 4 * R * 4;
-        const long long row0 = (long long)pend_item * p.qg;
-        float lt[R];
-#pragma unroll
-        for (int q4 = 0; q4 < R / 4; ++q4) {
-          const float4 a0 = lds_f4(lr + 16 * q4), a1 = lds_f4(lr + 16 * (R / 4 + q4));
-          const float4 a2 = lds_f4(lr + 16 * (2 * R / 4 + q4)), a3 = lds_f4(lr + 16 * (3 * R / 4 + q4));
-          lt[4 * q4] = (a0.x + a1.x) + (a2.x + a3.x);
-          lt[4 * q4 + 1] = (a0.y + a1.y) + (a2.y + a3.y);
-          lt[4 * q4 + 2] = (a0.z + a1.z) + (a2.z + a3.z);
-          lt[4 * q4 + 3] = (a0.w + a1.w) + (a2.w + a3.w);
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          // (lt >= 1: the row maximum's own term is exactly 1)
-          if (r < p.qg) p.part_o[(row0 + r) * D + t] = o[r] * (vscale * rcp_approx(lt[r]));
-          o[r] = 0.f;
-        }
-        if (t < p.qg) {
-          const float lrow = (ldsf(lr + 4 * t) + ldsf(lr + 4 * (R + t))) + (ldsf(lr + 4 * (2 * R + t)) + ldsf(lr + 4 * (3 * R + t)));
-          p.part_m[row0 + t] = ldsf(msm_s + pend_kpar * R * 4 + 4 * t) * kLn2;
-          p.part_l[row0 + t] = lrow;
-        }
-      }
-      return true;
-    };
+    bool ok = true;
 
     // the copy warps publish each non-empty item (and a final entry with no
     // tiles) with its query operand
@@ -301,10 +263,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         m[r] = -INFINITY;
         l[r] = 0.f;
       }
-      const int lph = (qcnt >> 1) & 1;
-      for (int i = 0; i < nt; ++i) {
+      for (int i = 0; i < nt; ++i, ++j) {
+        if (NWG == 2 && (j & 1) != wg) continue;
         const int start = (part + (i >> 1) * P) * TG + (i & 1) * TILE;
-        const bool last = i == nt - 1;
         const int b = j & 1;
         // ---- softmax of tile j
         if (!warp_wait(&sfull[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
@@ -320,17 +281,18 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         float x[R], xr[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          const float s = fmaf(fmaf(fmaf(v[3 * R + r], 0.0625f, v[2 * R + r]), 0.0625f, v[R + r]), 0.0625f, v[r]);
-          x[r] = valid ? s * c[r] : -INFINITY;
+          const float sv = fmaf(fmaf(fmaf(v[3 * R + r], 0.0625f, v[2 * R + r]), 0.0625f, v[R + r]), 0.0625f, v[r]);
+          x[r] = valid ? sv * c[r] : -INFINITY;
           xr[r] = x[r];
         }
         {
           const float mx = transpose_reduce<R, true>(xr, lane);
-          if ((lane & (32 / R - 1)) == 0) stsf(red_s + 4 * ((b * 4 + warp) * R + lane / (32 / R)), mx);
+          if ((lane & (32 / R - 1)) == 0) stsf(red_s + 4 * ((b * 4 + wq) * R + lane / (32 / R)), mx);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&xbar[b]);
         if (!warp_wait(&xbar[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
+        float alpha[R];
         {
           const uint32_t rb = red_s + b * 4 * R * 4;
 #pragma unroll
@@ -390,34 +352,120 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(&pfull[b]);
-        if (last) {
-          // row sums over the item's 128 token lanes, and the final maxima
-          float lr[R];
+        if (t == 0) {
+          // ---- O^T = V^T P'^T for tile j, issued by the group once its 4 warps wrote P'
+          if (role_wait(&pfull[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) {
+            tc_fence_after();
+            const uint32_t va = ring + (j % NS) * TILE_BYTES + V_OFF;
+            const uint32_t pa = psm + b * S::pBytes;
 #pragma unroll
-          for (int r = 0; r < R; ++r) lr[r] = l[r];
-          const float ls = transpose_reduce<R, false>(lr, lane);
-          if ((lane & (32 / R - 1)) == 0) stsf(lred_s + 4 * ((qb * 4 + warp) * R + lane / (32 / R)), ls);
-          if (t == 0) {
-#pragma unroll
-            for (int r = 0; r < R; ++r) stsf(msm_s + 4 * (qb * R + r), m[r]);
+            for (int k = 0; k < 4; ++k)
+              mma_e4m3(tmem + 2 * NQ + b * NQ, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
+                       umma_desc(pa + k * 32 * NQ, 8 * NQ, 128, kSwizzleNone), IDESC_PV, k);
+            umma_commit(&ofull[b]);
+            umma_commit(&empty[j % NS]);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&lbar[qb]);
         }
-        // ---- fold the previous O tile
-        if (pend_j >= 0 && !correction()) { ok = false; break; }
-        pend_j = j;
-        pend_last = last;
-        pend_item = item;
-        pend_kpar = qb;
-        pend_lph = lph;
+        // ---- fold O tile j into the accumulators
+        if (!warp_wait(&ofull[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
+        tc_fence_after();
+        float w[NQ];
 #pragma unroll
-        for (int r = 0; r < R; ++r) pend_alpha[r] = alpha[r];
-        ++j;
+        for (int h = 0; h < NT; ++h) tmem_ld32(tl + 2 * NQ + b * NQ + 32 * h, *reinterpret_cast<float(*)[32]>(w + 32 * h));
+        tmem_wait_ld();
+        tc_fence_before();
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float sv = fmaf(fmaf(w[2 * R + r], 0.0625f, w[R + r]), 0.0625f, w[r]);
+          o[r] = fmaf(sv, 0.00390625f, o[r] * alpha[r]);
+        }
       }
+      if (!ok) break;
+
+      // ---- item done: row sums over the group's 128 token lanes, merge of the
+      // groups' (m, l, O) to a common maximum, partials of the item. The group
+      // that owns the item's last tile merges (the other one finished first).
+      const uint32_t kph = (qcnt >> 1) & 1;
+      const int merger = NWG == 2 ? ((j - 1) & 1) : 0;
+      // (the buffers of item qcnt - 2 must have been read by its merger)
+      if (NWG == 2 && qcnt >= 2 &&
+          !warp_wait(&mfree[qb], ((qcnt >> 1) - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) { ok = false; break; }
+      {
+        float lr[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) lr[r] = l[r];
+        const float ls = transpose_reduce<R, false>(lr, lane);
+        if ((lane & (32 / R - 1)) == 0) stsf(lred_s + 4 * ((qb * 4 * NWG + warp) * R + lane / (32 / R)), ls);
+      }
+      if (t == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) stsf(msm_s + 4 * ((qb * NWG + wg) * R + r), m[r]);
+      }
+      if (NWG == 2 && wg != merger) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) stsf(stg_s + 4 * ((qb * R + r) * D + t), o[r]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&merge[qb]);
+      if (wg == merger) {
+        if (!warp_wait(&merge[qb], kph, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
+        const uint32_t lr = lred_s + qb * 4 * NWG * R * 4;
+        const uint32_t mr = msm_s + qb * NWG * R * 4;
+        const long long row0 = (long long)item * p.qg;
+        float lsum[NWG][R], mg[NWG][R];
+#pragma unroll
+        for (int g = 0; g < NWG; ++g)
+#pragma unroll
+          for (int q4 = 0; q4 < R / 4; ++q4) {
+            const float4 a0 = lds_f4(lr + 16 * ((4 * g) * R / 4 + q4)), a1 = lds_f4(lr + 16 * ((4 * g + 1) * R / 4 + q4));
+            const float4 a2 = lds_f4(lr + 16 * ((4 * g + 2) * R / 4 + q4)), a3 = lds_f4(lr + 16 * ((4 * g + 3) * R / 4 + q4));
+            const float4 mm = lds_f4(mr + 16 * (g * R / 4 + q4));
+            lsum[g][4 * q4] = (a0.x + a1.x) + (a2.x + a3.x);
+            lsum[g][4 * q4 + 1] = (a0.y + a1.y) + (a2.y + a3.y);
+            lsum[g][4 * q4 + 2] = (a0.z + a1.z) + (a2.z + a3.z);
+            lsum[g][4 * q4 + 3] = (a0.w + a1.w) + (a2.w + a3.w);
+            mg[g][4 * q4] = mm.x;
+            mg[g][4 * q4 + 1] = mm.y;
+            mg[g][4 * q4 + 2] = mm.z;
+            mg[g][4 * q4 + 3] = mm.w;
+          }
+        float other[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) other[r] = NWG == 2 ? ldsf(stg_s + 4 * ((qb * R + r) * D + t)) : 0.f;
+        float lt_mine = 0.f, mt_mine = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          float mt = mg[0][r], lt = lsum[0][r], ot = o[r];
+          if (NWG == 2) {
+            // (each group's maximum is -inf only if it saw no token of the item)
+            const float m_me = wg == 0 ? mg[0][r] : mg[NWG - 1][r], m_ot = wg == 0 ? mg[NWG - 1][r] : mg[0][r];
+            const float l_me = wg == 0 ? lsum[0][r] : lsum[NWG - 1][r], l_ot = wg == 0 ? lsum[NWG - 1][r] : lsum[0][r];
+            mt = fmaxf(m_me, m_ot);
+            const float a0 = ex2(m_me - mt), a1 = ex2(m_ot - mt);
+            lt = l_me * a0 + l_ot * a1;
+            ot = o[r] * a0 + other[r] * a1;
+          }
+          // (lt >= 1: the row maximum's own term is exactly 1)
+          if (r < p.qg) p.part_o[(row0 + r) * D + t] = ot * (vscale * rcp_approx(lt));
+          if (t == r) {
+            lt_mine = lt;
+            mt_mine = mt;
+          }
+        }
+        if (t < p.qg) {
+          p.part_m[row0 + t] = mt_mine * kLn2;
+          p.part_l[row0 + t] = lt_mine;
+        }
+        if (NWG == 2) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&mfree[qb]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) o[r] = 0.f;
       ++qcnt;
     }
-    if (ok && pend_j >= 0) correction();
+    if (t == 0) umma_commit(done);    // this group's PVs, before the tensor memory is released
   } else if (warp < WARP_MMA) {
     // ======================================================== copy warps
     const int pw = warp - WARP_PROD0;
@@ -592,73 +640,38 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     cp_async_wait_all();
   } else {
     // ======================================================== MMA warp
-    // A polling scheduler: issue whichever of the next PV (tile pv_j) and the
-    // next QK (tile qk_j) has its operands ready, so neither waits behind the
-    // other. Gives up after kWaitLimitNs without progress.
+    // S^T = K Q'^T for every tile in ring order (the softmax groups issue their
+    // own PV products).
     if (lane == 0) {
-      int qk_j = 0, pv_j = 0, qcnt = 0;
-      int it_i = 0, it_n = 0, qb = 0;      // QK cursor: tile within the item, the item's tiles, its operand buffer
-      bool qk_done = false;
-      unsigned long long t_prog = globaltimer();
-      while (true) {
-        // the next published item, once its query operand is ready
-        if (!qk_done && it_i >= it_n && mbar_test_wait(&qfull[qcnt & 1], (qcnt >> 1) & 1)) {
-          qb = qcnt & 1;
-          it_n = lds_i4(info_s + 16 * qb).z;
-          it_i = 0;
-          if (it_n == 0) qk_done = true;
-          ++qcnt;
-        }
-        if (qk_done && pv_j == qk_j) break;
-        bool progressed = false;
-        if (pv_j < qk_j) {
-          const int b = pv_j & 1, s = pv_j % NS;
-          if (mbar_test_wait(&pfull[b], (pv_j >> 1) & 1) &&
-              (pv_j < 2 || mbar_test_wait(&ofree[b], ((pv_j >> 1) - 1) & 1))) {
-            tc_fence_after();
-            const uint32_t va = ring + s * TILE_BYTES + V_OFF;
-            const uint32_t pa = psm + b * S::pBytes;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_e4m3(tmem + 2 * NQ + b * NQ, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
-                       umma_desc(pa + k * 32 * NQ, 8 * NQ, 128, kSwizzleNone), IDESC_PV, k);
-            umma_commit(&ofull[b]);
-            umma_commit(&empty[s]);
-            ++pv_j;
-            progressed = true;
-          }
-        }
-        if (!qk_done) {
+      int qk_j = 0, qcnt = 0;
+      bool ok = true;
+      while (ok) {
+        const int qb = qcnt & 1;
+        if (!role_wait(&qfull[qb], (qcnt >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) break;
+        const int nt = lds_i4(info_s + 16 * qb).z;
+        ++qcnt;
+        if (nt == 0) break;
+        const uint32_t qa = qsm + qb * S::qBytes;
+        for (int i = 0; i < nt; ++i, ++qk_j) {
           const int s = qk_j % NS, b = qk_j & 1;
-          if (it_i < it_n && mbar_test_wait(&full[s], (qk_j / NS) & 1) &&
-              (qk_j < 2 || mbar_test_wait(&sfree[b], ((qk_j >> 1) - 1) & 1))) {
-            fence_proxy_async();     // the copied bytes (generic proxy) become visible to the tensor core
-            tc_fence_after();
-            const uint32_t ka = ring + s * TILE_BYTES;
-            const uint32_t qa = qsm + qb * S::qBytes;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_e4m3(tmem + b * NQ, umma_desc(ka + 32 * k, 16, 1024, kSwizzle128B),
-                       umma_desc(qa + 32 * k, 16, 1024, kSwizzle128B), IDESC_QK, k);
-            umma_commit(&sfull[b]);
-            if (it_i == it_n - 1) umma_commit(&qempty[qb]);
-            ++it_i;
-            ++qk_j;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          t_prog = globaltimer();
-        } else {
-          if (*abort_flag) break;
-          if (globaltimer() - t_prog > kWaitLimitNs) {
-            atomicExch(&g_kernel_error, KERR_TIMEOUT_FULL);
-            *abort_flag = 1;
+          if (!role_wait(&full[s], (qk_j / NS) & 1, abort_flag, KERR_TIMEOUT_FULL) ||
+              (qk_j >= 2 && !role_wait(&sfree[b], ((qk_j >> 1) - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY))) {
+            ok = false;
             break;
           }
+          fence_proxy_async();     // the copied bytes (generic proxy) become visible to the tensor core
+          tc_fence_after();
+          const uint32_t ka = ring + s * TILE_BYTES;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_e4m3(tmem + b * NQ, umma_desc(ka + 32 * k, 16, 1024, kSwizzle128B),
+                     umma_desc(qa + 32 * k, 16, 1024, kSwizzle128B), IDESC_QK, k);
+          umma_commit(&sfull[b]);
+          if (i == nt - 1) umma_commit(&qempty[qb]);
         }
       }
-      // every issued MMA must finish before the tensor memory is released
+      // every issued MMA (this thread's and the softmax groups') must finish
+      // before the tensor memory is released
       umma_commit(done);
       if (!mbar_try_wait(done, 0)) {
         const unsigned long long t0 = globaltimer();
@@ -733,11 +746,11 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
   if (a.qg <= 8) {
     const int smem = fp8::Smem<1>::total;
     cudaFuncSetAttribute(pa_fp8_partition_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    pa_fp8_partition_kernel<1><<<grid, fp8::THREADS, smem, stream>>>(p);
+    pa_fp8_partition_kernel<1><<<grid, fp8::Smem<1>::THREADS, smem, stream>>>(p);
   } else {
     const int smem = fp8::Smem<2>::total;
     cudaFuncSetAttribute(pa_fp8_partition_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    pa_fp8_partition_kernel<2><<<grid, fp8::THREADS, smem, stream>>>(p);
+    pa_fp8_partition_kernel<2><<<grid, fp8::Smem<2>::THREADS, smem, stream>>>(p);
   }
   return cudaGetLastError();
 }
