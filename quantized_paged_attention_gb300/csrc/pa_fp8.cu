@@ -46,9 +46,9 @@ template <int NT>
 struct Smem {
   static constexpr int NWG = NT == 1 ? 2 : 1;      // softmax warp groups
   static constexpr int WARP_PROD0 = 4 * NWG;       // 4 copy warps
-  static constexpr int WARP_MMA = WARP_PROD0 + 4;  // 1 MMA warp
-  static constexpr int THREADS = (WARP_MMA + 1) * 32;
-  static constexpr int NS = NT == 1 ? 6 : 5;       // ring slots (tiles)
+  static constexpr int WARP_MMA = WARP_PROD0 + 4;  // QK issuing warp, then the PV issuing warp
+  static constexpr int THREADS = (WARP_MMA + 2) * 32;
+  static constexpr int NS = 5;                     // ring slots (tiles)
   static constexpr int R = 8 * NT;                 // query rows (padded)
   static constexpr int NQ = 32 * NT;               // MMA N: 4 term slots x R rows
   static constexpr int qBytes = NQ * D;            // Q' [NQ rows][128 dims] e4m3
@@ -56,18 +56,18 @@ struct Smem {
   static constexpr int ringOff = 0;
   static constexpr int qOff = NS * TILE_BYTES;
   static constexpr int pOff = qOff + 2 * qBytes;
-  static constexpr int stgOff = pOff + 2 * pBytes;         // [2][R][128] f32 second group's O
+  static constexpr int stgOff = pOff + 4 * pBytes;         // [2][R][128] f32 second group's O
   static constexpr int cOff = stgOff + (NWG == 2 ? 2 * R * D * 4 : 0);   // [2][R] logit multiplier per row
   static constexpr int redOff = cOff + 2 * R * 4;          // [2][4][R] tile maxima per warp
   static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][4 NWG][R] row sums per warp
   static constexpr int msmOff = lredOff + 2 * 4 * NWG * R * 4;   // [2][NWG][R] row maxima per group
   static constexpr int infoOff = msmOff + 2 * NWG * R * 4; // [2] {item, L, tiles, partition}
   static constexpr int barOff = (infoOff + 2 * 16 + 7) & ~7;
-  static constexpr int NBAR = 2 * NS + 2 * 10 + 1;
-  static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag
+  static constexpr int NBAR = 2 * NS + 2 * 10 + 4 + 1;
+  static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag, QK total
   static constexpr int total = miscOff + 16 + 1024;        // + alignment slack
   static_assert(total <= 227 * 1024, "shared memory");
-  static constexpr int TMEM_COLS = 4 * NQ;                 // S[2], O[2]
+  static constexpr int TMEM_COLS = NT == 1 ? 256 : 512;   // S[2] then O[4] (6 NQ columns)
 };
 }  // namespace fp8
 
@@ -164,14 +164,15 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   uint64_t* qempty = qfull + 2;       // [2] Q' consumed (MMA commit + softmax warps)
   uint64_t* sfull = qempty + 2;       // [2] S tile ready (MMA commit)
   uint64_t* sfree = sfull + 2;        // [2] S tile read (4 softmax warps)
-  uint64_t* pfull = sfree + 2;        // [2] P' tile written (4 softmax warps)
-  uint64_t* ofull = pfull + 2;        // [2] O tile ready (MMA commit)
-  uint64_t* xbar = ofull + 2;         // [2] tile maxima exchanged (4 softmax warps)
+  uint64_t* pfull = sfree + 2;        // [4] P' buffer written (4 softmax warps)
+  uint64_t* ofull = pfull + 4;        // [4] O buffer ready (PV commit)
+  uint64_t* xbar = ofull + 4;         // [2] tile maxima exchanged (4 softmax warps)
   uint64_t* merge = xbar + 2;         // [2] item states published (softmax warps)
   uint64_t* mfree = merge + 2;        // [2] item states read (first group's 4 warps)
   uint64_t* done = mfree + 2;         // [1] all MMAs finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::miscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::miscOff + 4);
+  volatile int* qk_total = reinterpret_cast<volatile int*>(sm + S::miscOff + 8);   // tiles, once all QKs are issued
   const uint32_t cbuf_s = sbase + S::cOff;
   const uint32_t red_s = sbase + S::redOff;
   const uint32_t lred_s = sbase + S::lredOff;
@@ -195,13 +196,16 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       mbar_init(&sfull[i], 1);
       mbar_init(&sfree[i], 4);
       mbar_init(&pfull[i], 4);
+      mbar_init(&pfull[2 + i], 4);
       mbar_init(&ofull[i], 1);
+      mbar_init(&ofull[2 + i], 1);
       mbar_init(&xbar[i], 4);
       mbar_init(&merge[i], 4 * NWG);
       mbar_init(&mfree[i], 4);
     }
-    mbar_init(done, 1 + NWG);
+    mbar_init(done, 2);
     *abort_flag = 0;
+    *qk_total = -1;
     fence_mbar_init();
   }
   if (warp == WARP_MMA) tmem_alloc(tmem_slot, S::TMEM_COLS);
@@ -239,6 +243,27 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     for (int r = 0; r < R; ++r) { o[r] = 0.f; m[r] = -INFINITY; l[r] = 0.f; c[r] = 0.f; }
     int j = 0, qcnt = 0;
     bool ok = true;
+    int pend_j = -1;                     // this group's tile whose O is not folded in yet
+    float pend_alpha[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) pend_alpha[r] = 0.f;
+    // O of tile pend_j (rescale factor pend_alpha) into the accumulators
+    auto fold = [&]() -> bool {
+      const int ob = 2 * (pend_j & 1) + ((pend_j >> 1) & 1);
+      if (!warp_wait(&ofull[ob], (pend_j >> 2) & 1, abort_flag, KERR_TIMEOUT_FULL)) return false;
+      tc_fence_after();
+      float w[NQ];
+#pragma unroll
+      for (int h = 0; h < NT; ++h) tmem_ld32(tl + 2 * NQ + ob * NQ + 32 * h, *reinterpret_cast<float(*)[32]>(w + 32 * h));
+      tmem_wait_ld();
+      tc_fence_before();
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float sv = fmaf(fmaf(w[2 * R + r], 0.0625f, w[R + r]), 0.0625f, w[r]);
+        o[r] = fmaf(sv, 0.00390625f, o[r] * pend_alpha[r]);
+      }
+      return true;
+    };
 
     // the copy warps publish each non-empty item (and a final entry with no
     // tiles) with its query operand
@@ -266,7 +291,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       for (int i = 0; i < nt; ++i, ++j) {
         if (NWG == 2 && (j & 1) != wg) continue;
         const int start = (part + (i >> 1) * P) * TG + (i & 1) * TILE;
-        const int b = j & 1;
+        const int b = j & 1;                 // S buffer
+        const int ob = 2 * b + ((j >> 1) & 1);   // P' and O buffer (alternate per group)
         // ---- softmax of tile j
         if (!warp_wait(&sfull[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
         tc_fence_after();
@@ -334,7 +360,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           }
         }
         {
-          const uint32_t pb = ptok + b * S::pBytes;
+          const uint32_t pb = ptok + ob * S::pBytes;
           if constexpr (NT == 1) {
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(tw[0][0]), "r"(tw[0][1]),
                          "r"(tw[1][0]), "r"(tw[1][1]) : "memory");
@@ -351,35 +377,15 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         }
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pfull[b]);
-        if (t == 0) {
-          // ---- O^T = V^T P'^T for tile j, issued by the group once its 4 warps wrote P'
-          if (role_wait(&pfull[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) {
-            tc_fence_after();
-            const uint32_t va = ring + (j % NS) * TILE_BYTES + V_OFF;
-            const uint32_t pa = psm + b * S::pBytes;
+        if (lane == 0) mbar_arrive(&pfull[ob]);
+        // ---- fold this group's previous O tile while the tensor core computes this one
+        if (pend_j >= 0 && !fold()) { ok = false; break; }
+        pend_j = j;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_e4m3(tmem + 2 * NQ + b * NQ, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
-                       umma_desc(pa + k * 32 * NQ, 8 * NQ, 128, kSwizzleNone), IDESC_PV, k);
-            umma_commit(&ofull[b]);
-            umma_commit(&empty[j % NS]);
-          }
-        }
-        // ---- fold O tile j into the accumulators
-        if (!warp_wait(&ofull[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
-        tc_fence_after();
-        float w[NQ];
-#pragma unroll
-        for (int h = 0; h < NT; ++h) tmem_ld32(tl + 2 * NQ + b * NQ + 32 * h, *reinterpret_cast<float(*)[32]>(w + 32 * h));
-        tmem_wait_ld();
-        tc_fence_before();
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float sv = fmaf(fmaf(w[2 * R + r], 0.0625f, w[R + r]), 0.0625f, w[r]);
-          o[r] = fmaf(sv, 0.00390625f, o[r] * alpha[r]);
-        }
+        for (int r = 0; r < R; ++r) pend_alpha[r] = alpha[r];
       }
+      if (ok && pend_j >= 0 && !fold()) ok = false;
+      pend_j = -1;
       if (!ok) break;
 
       // ---- item done: row sums over the group's 128 token lanes, merge of the
@@ -465,7 +471,6 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       for (int r = 0; r < R; ++r) o[r] = 0.f;
       ++qcnt;
     }
-    if (t == 0) umma_commit(done);    // this group's PVs, before the tensor memory is released
   } else if (warp < WARP_MMA) {
     // ======================================================== copy warps
     const int pw = warp - WARP_PROD0;
@@ -638,7 +643,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       }
     }
     cp_async_wait_all();
-  } else {
+  } else if (warp == WARP_MMA) {
     // ======================================================== MMA warp
     // S^T = K Q'^T for every tile in ring order (the softmax groups issue their
     // own PV products).
@@ -670,8 +675,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           if (i == nt - 1) umma_commit(&qempty[qb]);
         }
       }
-      // every issued MMA (this thread's and the softmax groups') must finish
-      // before the tensor memory is released
+      *qk_total = qk_j;
+      // every issued MMA (this warp's and the PV warp's) must finish before the
+      // tensor memory is released
       umma_commit(done);
       if (!mbar_try_wait(done, 0)) {
         const unsigned long long t0 = globaltimer();
@@ -682,6 +688,50 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           }
         }
       }
+    }
+    __syncwarp();
+  } else {
+    // ======================================================== PV warp
+    // O^T = V^T P'^T for each tile once its softmax group wrote P' (one cursor
+    // per buffer parity, so the two groups never wait for each other); frees
+    // the tile's ring slot.
+    if (lane == 0) {
+      int pv_n[2] = {0, 1};
+      unsigned long long t_prog = globaltimer();
+      while (true) {
+        const int total = *qk_total;
+        if (total >= 0 && pv_n[0] >= total && pv_n[1] >= total) break;
+        bool progressed = false;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int jj = pv_n[b];
+          const int ob = 2 * b + ((jj >> 1) & 1);
+          if ((total < 0 || jj < total) && mbar_test_wait(&pfull[ob], (jj >> 2) & 1)) {
+            tc_fence_after();
+            const uint32_t va = ring + (jj % NS) * TILE_BYTES + V_OFF;
+            const uint32_t pa = psm + ob * S::pBytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_e4m3(tmem + 2 * NQ + ob * NQ, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
+                       umma_desc(pa + k * 32 * NQ, 8 * NQ, 128, kSwizzleNone), IDESC_PV, k);
+            umma_commit(&ofull[ob]);
+            umma_commit(&empty[jj % NS]);
+            pv_n[b] += 2;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_prog = globaltimer();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer() - t_prog > kWaitLimitNs) {
+            atomicExch(&g_kernel_error, KERR_TIMEOUT_FULL);
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+      umma_commit(done);
     }
     __syncwarp();
   }
