@@ -508,21 +508,43 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       return (lane < bpt && e < p.max_blocks) ? __ldg(p.block_table + (long long)seq * p.max_blocks + e) : 0;
     };
 
-    int L = load_len(blockIdx.x);
+    // ---- this CTA's items: round-robin over the items in (sequence, partition,
+    // kv head) order, so that the CTAs working at the same time read all heads
+    // of the same pages. Empty partitions (starting past the length) get zero
+    // partials right away.
+    auto seq_len = [&](int sq) -> int { return max(0, min(__ldg(p.seq_lens + sq), p.max_blocks * bs)); };
+    auto item_of = [&](int k) -> int {      // k-th item in (sequence, partition, kv head) order
+      const int sq = k / (P * Hk), rem = k - sq * (P * Hk);
+      const int part = rem / Hk, kvh = rem - part * Hk;
+      return (sq * Hk + kvh) * P + part;
+    };
     uint4 qv[NT];
-    load_q(blockIdx.x, qv);
-    int32_t ent0 = load_entries(blockIdx.x, blockIdx.x % P);
-    for (int item = blockIdx.x; item < num_items && ok; item += G) {
+    int32_t ent0 = 0;
+    int L = 0;
+    if ((int)blockIdx.x < num_items) {
+      const int it0 = item_of(blockIdx.x);
+      L = seq_len(it0 / (P * Hk));
+      load_q(it0, qv);
+      ent0 = load_entries(it0, it0 % P);
+    }
+    for (int k = blockIdx.x; k < num_items && ok; k += G) {
+      const int item = item_of(k);
       const int part = item % P;
       const int kvh = (item / P) % Hk;
       const int nt = item_tiles(part, P, L);
       // next item's length, query rows and first table entries
-      const int Lnext = load_len(item + G);
+      int Lnext = 0;
       uint4 qn[NT];
-      load_q(item + G, qn);
-      const int32_t ent0n = load_entries(item + G, (item + G) % P);
+#pragma unroll
+      for (int h = 0; h < NT; ++h) qn[h] = make_uint4(0, 0, 0, 0);
+      int32_t ent0n = 0;
+      if (k + G < num_items) {
+        const int itn = item_of(k + G);
+        Lnext = seq_len(itn / (P * Hk));
+        load_q(itn, qn);
+        ent0n = load_entries(itn, itn % P);
+      }
       if (nt == 0) {
-        // an empty partition (starts past the length): weight 0 in the combine
         const long long row0 = (long long)item * p.qg;
         for (int r = 0; r < p.qg; ++r) p.part_o[(row0 + r) * D + pt] = 0.f;
         if (pt < p.qg) {
