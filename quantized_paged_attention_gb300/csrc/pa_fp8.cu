@@ -304,16 +304,23 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfree[b]);
         const bool valid = start + t < L;
-        float x[R], xr[R];
+        float x[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const float sv = fmaf(fmaf(fmaf(v[3 * R + r], 0.0625f, v[2 * R + r]), 0.0625f, v[R + r]), 0.0625f, v[r]);
           x[r] = valid ? sv * c[r] : -INFINITY;
-          xr[r] = x[r];
         }
         {
-          const float mx = transpose_reduce<R, true>(xr, lane);
-          if ((lane & (32 / R - 1)) == 0) stsf(red_s + 4 * ((b * 4 + wq) * R + lane / (32 / R)), mx);
+          // row maxima over the warp's 32 tokens (hardware warp reduction)
+          float mx[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r) mx[r] = warp_max(x[r]);
+          if (lane == 0) {
+#pragma unroll
+            for (int q4 = 0; q4 < R / 4; ++q4)
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red_s + 4 * ((b * 4 + wq) * R + 4 * q4)),
+                           "f"(mx[4 * q4]), "f"(mx[4 * q4 + 1]), "f"(mx[4 * q4 + 2]), "f"(mx[4 * q4 + 3]) : "memory");
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&xbar[b]);
