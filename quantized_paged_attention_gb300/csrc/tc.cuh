@@ -105,4 +105,50 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Bounded mbarrier wait that also gives up as soon as another role aborted.
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int k = 0; k < 16; ++k)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicExch(&g_kernel_error, err);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int err) {
+  return __all_sync(0xffffffffu, role_wait(bar, parity, abort_flag, err));
+}
+
+// Max (or sum) of R values per lane over the warp's 32 lanes, by halving
+// exchanges: lane l ends with row (l >> (5 - log2 R)).
+template <int R, bool MAX>
+__device__ __forceinline__ float transpose_reduce(float (&a)[R], int lane) {
+  constexpr int LOG2R = R == 8 ? 3 : 4;
+#pragma unroll
+  for (int step = 0; step < LOG2R; ++step) {
+    const int off = 16 >> step;
+    const int half = R >> (step + 1);
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = up ? a[k] : a[k + half];
+      const float keep = up ? a[k + half] : a[k];
+      const float got = __shfl_xor_sync(0xffffffffu, send, off);
+      a[k] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+#pragma unroll
+  for (int off = 16 >> LOG2R; off >= 1; off >>= 1) {
+    const float got = __shfl_xor_sync(0xffffffffu, a[0], off);
+    a[0] = MAX ? fmaxf(a[0], got) : a[0] + got;
+  }
+  return a[0];
+}
+
 }  // namespace qpa
