@@ -135,23 +135,6 @@ __device__ __forceinline__ void cp_async_chunk_pair(uint32_t d0, uint32_t d1, co
       ::"r"(d0), "r"(d1), "l"(src_k), "l"(src_v), "l"(pol) : "memory");
 }
 
-// The 272 used bytes of one token slot (17 chunks of 16 B) as two lanes' work:
-// lane half h copies chunks h, h+2, ..., so h = 0 copies 9 chunks and h = 1
-// copies 8. dst / src point at the slot's chunk h.
-__device__ __forceinline__ void cp_async_slot272(uint32_t dst, const void* src, bool h0, uint64_t pol) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %3, 0;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0+32], [%1+32], 16, %2;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0+64], [%1+64], 16, %2;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0+96], [%1+96], 16, %2;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0+128], [%1+128], 16, %2;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0+160], [%1+160], 16, %2;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0+192], [%1+192], 16, %2;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0+224], [%1+224], 16, %2;\n\t"
-      "@p cp.async.cg.shared.global.L2::cache_hint [%0+256], [%1+256], 16, %2; }\n\t"
-      ::"r"(dst), "l"(src), "l"(pol), "r"((int)h0) : "memory");
-}
 // Half a scorer page: 4096 B of codes (lane l copies bytes 16 l + 512 i) and
 // 512 B of scales (lane l copies bytes 16 l).
 __device__ __forceinline__ void cp_async_halfpage(uint32_t dcodes, uint32_t dscales, const void* codes,

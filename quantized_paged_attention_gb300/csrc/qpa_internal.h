@@ -75,6 +75,7 @@ __device__ __forceinline__ void store4(__nv_bfloat16* dst, float a, float b, flo
 cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t stream);
 cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream);
+int uq_warps_per_item(long long items, int max_blocks, int block_size, int num_partitions, int num_sms);
 cudaError_t launch_uq_combine(const CombineLaunch& a, cudaStream_t stream);
 cudaError_t launch_idx_score(const IdxLaunch& a, cudaStream_t stream);
 

@@ -15,13 +15,20 @@
 // centroid table (V = centroid[code] * scale); the page's own V convert
 // (e2m1 * scale) is the case where the table is the e2m1 value table.
 //
-// GB300 design: the fp8 kernel's structure (persistent 4-warp CTAs, per-warp
-// 16-byte cp.async pipelines, deterministic merge) with
+// GB300 design: one persistent 8-warp CTA per SM; each warp runs its own
+// 16-byte cp.async ring of three 32-token slices (8.5 KB each). An item
+// (sequence, KV head, partition) belongs to a group of W warps (W = 1, 2 or
+// 4, picked on the host from the item count), which split its slices and
+// merge deterministically when W > 1; with W = 1 a warp writes its own
+// partials and no CTA-level synchronisation remains. A slice is two 16-token
+// MMA tiles, so the per-slice costs (copy issue, row-max shuffles, pipeline
+// bookkeeping) are paid once per 32 tokens and the two tiles' QK chains
+// overlap. And
 //  * K dequantised in registers: cvt e2m1x2 -> f16x2 (exact) times the
 //    group scale (hmul2, exact in f16), f16 mma.sync against the rotated q;
 //  * V^T fragments built per token pair: the two tokens' nibbles of a dim form
 //    one byte that indexes a 256-entry f16x2 table {c[a], c[b]} in shared
-//    memory (replicated per bank, conflict-free), times the token pair's
+//    memory (16 bank copies: at most two lanes share a bank), times the token pair's
 //    scale; when the centroid table is exactly the e2m1 table the byte is
 //    converted with cvt e2m1x2 instead (detected in the kernel);
 //  * a lane's 32 output dims form one scale group, so one scale pair serves
@@ -35,21 +42,23 @@ namespace qpa {
 namespace uq {
 constexpr int D = 256;
 constexpr int TG = 256;
-constexpr int SLICE = 16;
-constexpr int NW = 4;
+constexpr int SLICE = 32;                        // tokens per ring slot: two 16-token MMA tiles
+constexpr int NW = 8;
 constexpr int THREADS = NW * 32;
-constexpr int DEPTH = 4;
+constexpr int DEPTH = 3;
 constexpr int CONTENT = 272;                     // used bytes of a slot
-constexpr int SLOT_BYTES = SLICE * CONTENT;      // 4352: one slice, or 8 query rows (4096)
+constexpr int SLOT_BYTES = SLICE * CONTENT;      // 8704: one slice, or 8 query rows (4096)
 constexpr int KS_OFF = 128, VC_OFF = 136, VS_OFF = 264;
-constexpr int LUT_BYTES = 256 * 32 * 4;          // [code pair][bank copy] f16x2
+constexpr int LUT_COPIES = 16;                   // bank copies of each table entry
+constexpr int LUT_BYTES = 256 * LUT_COPIES * 4;  // [code pair][bank copy] f16x2
 constexpr int ringOff = 0;
-constexpr int lutOff = NW * DEPTH * SLOT_BYTES;  // 69632 (a multiple of 128)
+constexpr int lutOff = NW * DEPTH * SLOT_BYTES;  // 208896 (a multiple of 128)
 constexpr int mOff = lutOff + LUT_BYTES;
 constexpr int lOff = mOff + NW * 8 * 4;
 constexpr int fOff = lOff + NW * 8 * 4;
-constexpr int SMEM = fOff + NW * 4;
-constexpr int CTAS_PER_SM = 2;
+constexpr int SMEM = fOff + NW * 4;              // 225824 bytes: one CTA per SM
+constexpr int CTAS_PER_SM = 1;
+static_assert(SMEM <= 232448, "shared memory");
 }  // namespace uq
 
 struct UqParams {
@@ -74,13 +83,20 @@ __device__ __forceinline__ float e2m1_value(int k) {
   return (k & 8) ? -mag[k & 7] : mag[k & 7];
 }
 
+template <int W>
 __global__ void __launch_bounds__(uq::THREADS, uq::CTAS_PER_SM)
 uq_partition_kernel(const UqParams p) {
   using namespace uq;
+  static_assert(W == 1 || W == 2 || W == 4, "warps per item");
+  constexpr int GROUPS = NW / W;              // item groups per CTA
+  constexpr int SLICES_PER_WARP = TG / SLICE / W;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int grp = warp / W;                   // this warp's item group
+  const int wi = warp % W;                    // rank within the group
   const int num_items = p.num_seqs * p.num_kv_heads * p.num_partitions;
+  const int item_stride = gridDim.x * GROUPS;
   const int P = p.num_partitions;
   const int bs = p.block_size;
   const int lbs = p.log2_bs;
@@ -88,7 +104,7 @@ uq_partition_kernel(const UqParams p) {
   float* ms = reinterpret_cast<float*>(smem + mOff);
   float* ls = reinterpret_cast<float*>(smem + lOff);
   uint32_t* fslot = reinterpret_cast<uint32_t*>(smem + fOff);
-  const uint32_t lut = smem_u32(smem + lutOff) + lane * 4;   // this lane's bank copy
+  const uint32_t lut = smem_u32(smem + lutOff) + (lane & (LUT_COPIES - 1)) * 4;   // this lane's bank copy
 
   // ---- centroid table: the e2m1 table takes the cvt path, anything else the
   // shared-memory pair table (f16 values of the fp32 centroids)
@@ -102,8 +118,8 @@ uq_partition_kernel(const UqParams p) {
     }
     if (!e2m1_table) {
       uint32_t* t = reinterpret_cast<uint32_t*>(smem + lutOff);
-      for (int i = threadIdx.x; i < 256 * 32; i += THREADS) {
-        const int e = i >> 5;
+      for (int i = threadIdx.x; i < 256 * LUT_COPIES; i += THREADS) {
+        const int e = i / LUT_COPIES;
         t[i] = f32x2_to_f16x2(cv[e & 15], cv[e >> 4]);
       }
     }
@@ -116,7 +132,7 @@ uq_partition_kernel(const UqParams p) {
   const size_t tok_stride = size_t(p.num_kv_heads) * p.padded_slot;    // bytes between tokens
 
   // ---------------------------------------------------------------- issue side
-  int ik_item = blockIdx.x;
+  int ik_item = blockIdx.x * GROUPS + grp;
   int i_state = 0, i_tg = 0, i_kk = 0, i_L = 0, i_Lnext = 0, i_seq = 0, i_kvh = 0, i_part = 0;
   int32_t i_ent = 0, i_nent = 0;
   int rec_kind = 0, rec_a = 0, rec_b = 0;
@@ -133,7 +149,7 @@ uq_partition_kernel(const UqParams p) {
     return v;
   };
   if (ik_item < num_items) i_L = load_len(ik_item);
-  i_Lnext = load_len(ik_item + gridDim.x);
+  i_Lnext = load_len(ik_item + item_stride);
 
   auto issue = [&](int e) {
     const uint32_t slot = ring + (e % DEPTH) * SLOT_BYTES;
@@ -141,10 +157,13 @@ uq_partition_kernel(const UqParams p) {
     while (true) {
       if (ik_item >= num_items) break;
       if (i_state == 0) {
-        i_part = ik_item % P;
-        const int t = ik_item / P;
-        i_kvh = t % p.num_kv_heads;
-        i_seq = t / p.num_kv_heads;
+        // items run in (sequence, partition, KV head) order, so the groups
+        // working at the same time read both heads' halves of the same token
+        // records; partials are indexed (sequence, KV head, partition)
+        i_kvh = ik_item % p.num_kv_heads;
+        const int t = ik_item / p.num_kv_heads;
+        i_part = t % P;
+        i_seq = t / P;
         if (i_part * TG < i_L) {
           // query rows: qg rows x 512 B
           const uint16_t* qrow0 = p.q + i_seq * p.q_stride_seq + (long long)(i_kvh * p.qg) * p.q_stride_head;
@@ -158,20 +177,23 @@ uq_partition_kernel(const UqParams p) {
         i_state = 1;
         i_tg = i_part;
         i_kk = 0;
-        kind = UEV_ITEM; a = ik_item; b = i_L;
+        kind = UEV_ITEM; a = (i_seq * p.num_kv_heads + i_kvh) * P + i_part; b = i_L;
         break;
       }
       if (i_tg * TG >= i_L) {
-        ik_item += gridDim.x;
+        ik_item += item_stride;
         i_state = 0;
         i_L = i_Lnext;
-        i_Lnext = load_len(ik_item + gridDim.x);
+        i_Lnext = load_len(ik_item + item_stride);
         continue;
       }
-      const int s = (i_tg * TG) / SLICE + 4 * i_kk + warp;
-      const bool valid = s * SLICE < i_L;
-      int phys = __shfl_sync(0xffffffffu, i_ent, ((s * SLICE) & (TG - 1)) >> lbs);
-      if (++i_kk == 4) {
+      const int s = (i_tg * TG) / SLICE + W * i_kk + wi;
+      const int t0 = s * SLICE;
+      const bool valid = t0 < i_L;
+      // blocks of the slice's tokens 0 and 16
+      int pa = __shfl_sync(0xffffffffu, i_ent, (t0 & (TG - 1)) >> lbs);
+      int pb = __shfl_sync(0xffffffffu, i_ent, ((t0 + 16) & (TG - 1)) >> lbs);
+      if (++i_kk == SLICES_PER_WARP) {
         i_kk = 0;
         i_tg += P;
         if (i_tg * TG < i_L) {
@@ -180,15 +202,42 @@ uq_partition_kernel(const UqParams p) {
         }
       }
       if (!valid) continue;
-      if (phys < 0 || phys >= p.num_blocks) {
-        if (lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
-        phys = 0;
+      if (pa < 0 || pa >= p.num_blocks || pb < 0 || pb >= p.num_blocks) {
+        atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+        pa = (pa < 0 || pa >= p.num_blocks) ? 0 : pa;
+        pb = (pb < 0 || pb >= p.num_blocks) ? 0 : pb;
       }
-      // 16 token slots of this KV head, 272 bytes each: lanes 2r and 2r+1 copy
-      // the alternate 16-byte chunks of token r
-      const uint8_t* tok = p.kv + (size_t(phys) * bs + ((s * SLICE) & (bs - 1)) + (lane >> 1)) * tok_stride +
-                           size_t(i_kvh) * p.padded_slot + 16 * (lane & 1);
-      cp_async_slot272(slot + (lane >> 1) * CONTENT + 16 * (lane & 1), tok, (lane & 1) == 0, pol);
+      // 32 token slots of this KV head, 272 bytes each, copied as whole
+      // 128-byte runs so that the L2 requests cover full sectors of few lines:
+      // eight lanes copy bytes [0, 128) or [128, 256) of one token, four
+      // tokens per instruction (tokens 4i + lane/8), and one instruction
+      // copies every token's last 16 bytes. Tokens 0..15 of the slice lie in
+      // block pa, 16..31 in block pb (the same block unless block_size is 16);
+      // slots past the end of the sequence are read from the blocks the table
+      // names (or block 0) and masked by the consumer.
+      const uint8_t* head = p.kv + size_t(i_kvh) * p.padded_slot;
+      const uint8_t* rowa = head + (size_t(pa) * bs + (t0 & (bs - 1))) * tok_stride;          // token 0
+      const uint8_t* rowb = head + (size_t(pb) * bs + ((t0 + 16) & (bs - 1))) * tok_stride;   // token 16
+      {
+        const int q4 = lane >> 3;
+        const uint32_t off = 16 * (lane & 7);
+        const uint8_t* sa = rowa + size_t(q4) * tok_stride + off;
+        const uint8_t* sb = rowb + size_t(q4) * tok_stride + off;
+        const uint32_t d = slot + q4 * CONTENT + off;
+        const size_t step4 = 4 * tok_stride;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          cp_async16(d + 4 * i * CONTENT, sa + i * step4, pol);
+          cp_async16(d + 4 * i * CONTENT + 128, sa + i * step4 + 128, pol);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          cp_async16(d + (16 + 4 * i) * CONTENT, sb + i * step4, pol);
+          cp_async16(d + (16 + 4 * i) * CONTENT + 128, sb + i * step4 + 128, pol);
+        }
+        const uint8_t* st = (lane < 16 ? rowa + size_t(lane) * tok_stride : rowb + size_t(lane - 16) * tok_stride) + 256;
+        cp_async16(slot + lane * CONTENT + 256, st, pol);
+      }
       kind = UEV_SLICE; a = s; b = i_L;
       break;
     }
@@ -215,75 +264,100 @@ uq_partition_kernel(const UqParams p) {
     const int eb = __shfl_sync(0xffffffffu, rec_b, e % DEPTH);
 
     if (kind != UEV_SLICE && cur_item >= 0) {
-      // ---- merge the four warps' states (fixed order), write partials
       const long long row0 = (long long)cur_item * p.qg;
-      const uint32_t myfree = ring + ((e + DEPTH - 1) % DEPTH) * SLOT_BYTES;
 #pragma unroll
       for (int sh = 4; sh < 32; sh <<= 1) {
         l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], sh);
         l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], sh);
       }
-      if (g == 0) {
-        ms[warp * 8 + 2 * c] = m_run[0];
-        ms[warp * 8 + 2 * c + 1] = m_run[1];
-        ls[warp * 8 + 2 * c] = l_run[0];
-        ls[warp * 8 + 2 * c + 1] = l_run[1];
-      }
-      if (lane == 0) fslot[warp] = myfree;
-      named_barrier(1, THREADS);
-      float sc[2];
+      if constexpr (W == 1) {
+        // ---- the warp's own state is the item's: normalise and write
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float M = -INFINITY;
+        for (int h = 0; h < 2; ++h) {
+          const int r = 2 * c + h;
+          if (r < p.qg) {
+            const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
+            float* dst = p.part_o + (row0 + r) * D + 32 * g;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, ms[w * 8 + 2 * c + h]);
-        sc[h] = (m_run[h] == -INFINITY) ? 0.f : ex2(m_run[h] - M);
-      }
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        // dims [128 half, 128 half + 128) are held by lanes with g in [4 half, 4 half + 4);
-        // stored as fp32 [8 rows][128] with bits 1..4 of the dim XOR-swizzled
-        if ((g >> 2) == half) {
-          const int gg = g & 3;
-          const int sw = ((c | (gg << 2)) << 1);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int d0 = 32 * gg + 2 * i;     // local dim of row g (even), +1 for row g+8
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int row = 2 * c + h;
-              stsf(myfree + (row * 128 + (d0 ^ sw)) * 4, o[i][h] * sc[h]);
-              stsf(myfree + (row * 128 + ((d0 + 1) ^ sw)) * 4, o[i][2 + h] * sc[h]);
+            for (int i = 0; i < 16; ++i)
+              *reinterpret_cast<float2*>(dst + 2 * i) = make_float2(o[i][h] * inv, o[i][2 + h] * inv);
+            if (g == 0) {
+              p.part_m[row0 + r] = m_run[h] == -INFINITY ? -INFINITY : m_run[h] * kLn2;
+              p.part_l[row0 + r] = l_run[h];
             }
           }
         }
-        named_barrier(1, THREADS);
-        {
-          const int tid = threadIdx.x;
-          uint32_t fs[NW];
+      } else {
+        // ---- merge the group's W warp states (fixed order) through their
+        // just-consumed ring slots, write partials
+        const uint32_t myfree = ring + ((e + DEPTH - 1) % DEPTH) * SLOT_BYTES;
+        const int w0 = grp * W;
+        const int bar = 1 + grp;
+        if (g == 0) {
+          ms[warp * 8 + 2 * c] = m_run[0];
+          ms[warp * 8 + 2 * c + 1] = m_run[1];
+          ls[warp * 8 + 2 * c] = l_run[0];
+          ls[warp * 8 + 2 * c + 1] = l_run[1];
+        }
+        if (lane == 0) fslot[warp] = myfree;
+        named_barrier(bar, 32 * W);
+        float sc[2];
 #pragma unroll
-          for (int w = 0; w < NW; ++w) fs[w] = fslot[w];
-          for (int r = 0; r < p.qg; ++r) {
-            float M = -INFINITY;
+        for (int h = 0; h < 2; ++h) {
+          float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) M = fmaxf(M, ms[w * 8 + r]);
-            float lsum = 0.f, acc = 0.f;
-            const int pd = tid ^ ((((r >> 1) | (((tid >> 5) & 3) << 2))) << 1);
+          for (int w = 0; w < W; ++w) M = fmaxf(M, ms[(w0 + w) * 8 + 2 * c + h]);
+          sc[h] = (m_run[h] == -INFINITY) ? 0.f : ex2(m_run[h] - M);
+        }
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-              const float mw = ms[w * 8 + r];
-              const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-              lsum += wt * ls[w * 8 + r];
-              acc += ldsf(fs[w] + (r * 128 + pd) * 4);
-            }
-            p.part_o[(row0 + r) * D + 128 * half + tid] = lsum > 0.f ? acc / lsum : 0.f;
-            if (half == 0 && tid == 0) {
-              p.part_m[row0 + r] = M == -INFINITY ? -INFINITY : M * kLn2;
-              p.part_l[row0 + r] = lsum;
+        for (int half = 0; half < 2; ++half) {
+          // dims [128 half, 128 half + 128) are held by lanes with g in [4 half, 4 half + 4);
+          // stored as fp32 [8 rows][128] with bits 1..4 of the dim XOR-swizzled
+          if ((g >> 2) == half) {
+            const int gg = g & 3;
+            const int sw = ((c | (gg << 2)) << 1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int d0 = 32 * gg + 2 * i;     // local dim of row g (even), +1 for row g+8
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int row = 2 * c + h;
+                stsf(myfree + (row * 128 + (d0 ^ sw)) * 4, o[i][h] * sc[h]);
+                stsf(myfree + (row * 128 + ((d0 + 1) ^ sw)) * 4, o[i][2 + h] * sc[h]);
+              }
             }
           }
+          named_barrier(bar, 32 * W);
+          {
+            uint32_t fs[W];
+#pragma unroll
+            for (int w = 0; w < W; ++w) fs[w] = fslot[w0 + w];
+            for (int r = 0; r < p.qg; ++r) {
+              float M = -INFINITY;
+#pragma unroll
+              for (int w = 0; w < W; ++w) M = fmaxf(M, ms[(w0 + w) * 8 + r]);
+              float lsum = 0.f;
+#pragma unroll
+              for (int w = 0; w < W; ++w) {
+                const float mw = ms[(w0 + w) * 8 + r];
+                lsum += ((mw == -INFINITY) ? 0.f : ex2(mw - M)) * ls[(w0 + w) * 8 + r];
+              }
+#pragma unroll
+              for (int d = wi * 32 + lane; d < 128; d += 32 * W) {
+                const int pd = d ^ ((((r >> 1) | ((d >> 5) << 2))) << 1);
+                float acc = 0.f;
+#pragma unroll
+                for (int w = 0; w < W; ++w) acc += ldsf(fs[w] + (r * 128 + pd) * 4);
+                p.part_o[(row0 + r) * D + 128 * half + d] = lsum > 0.f ? acc / lsum : 0.f;
+              }
+              if (half == 0 && wi == 0 && lane == 0) {
+                p.part_m[row0 + r] = M == -INFINITY ? -INFINITY : M * kLn2;
+                p.part_l[row0 + r] = lsum;
+              }
+            }
+          }
+          named_barrier(bar, 32 * W);
         }
-        named_barrier(1, THREADS);
       }
       cur_item = -1;
     }
@@ -347,74 +421,50 @@ uq_partition_kernel(const UqParams p) {
       continue;
     }
 
-    // ---- UEV_SLICE: tokens [16 ea, 16 ea + 16)
+    // ---- UEV_SLICE: tokens [32 ea, 32 ea + 32) as two 16-token tiles h
     const int t0 = ea * SLICE;
     const int L = eb;
     const bool partial = t0 + SLICE > L;
-    // K: rows g and g+8, code bytes [32c, 32c+32) -> dims [64c, 64c+64)
-    const uint32_t rg = slot + g * CONTENT, rg8 = slot + (g + 8) * CONTENT;
-    const uint4 ka0 = lds128(rg + 32 * c), ka1 = lds128(rg + 32 * c + 16);
-    const uint4 kb0 = lds128(rg8 + 32 * c), kb1 = lds128(rg8 + 32 * c + 16);
-    const uint32_t kra[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
-    const uint32_t krb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
-    // K scales of groups 2c, 2c+1 for rows g, g+8 as {s, s} f16 pairs
-    uint32_t ksa0, ksa1, ksb0, ksb1;
-    {
+
+    // ---- S^T (16 tokens x 8 rows) = K q_r^T per tile; the two tiles' MMA
+    // chains are independent
+    float x[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      // K: rows g and g+8 of tile h, code bytes [32c, 32c+32) -> dims [64c, 64c+64)
+      const uint32_t rg = slot + (16 * h + g) * CONTENT, rg8 = rg + 8 * CONTENT;
+      const uint4 ka0 = lds128(rg + 32 * c), ka1 = lds128(rg + 32 * c + 16);
+      const uint4 kb0 = lds128(rg8 + 32 * c), kb1 = lds128(rg8 + 32 * c + 16);
+      const uint32_t kra[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+      const uint32_t krb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+      // K scales of groups 2c, 2c+1 for rows g, g+8 as {s, s} f16 pairs
       const uint32_t sa = e4m3x2_lo_to_f16x2(lds32(rg + KS_OFF + 4 * (c >> 1)) >> (16 * (c & 1)));
       const uint32_t sb = e4m3x2_lo_to_f16x2(lds32(rg8 + KS_OFF + 4 * (c >> 1)) >> (16 * (c & 1)));
-      ksa0 = prmt(sa, sa, 0x1010); ksa1 = prmt(sa, sa, 0x3232);
-      ksb0 = prmt(sb, sb, 0x1010); ksb1 = prmt(sb, sb, 0x3232);
-    }
-    // V: rows 2c, 2c+1, 2c+8, 2c+9, code bytes [16g, 16g+16) -> dims [32g, 32g+32)
-    uint2 vw[4][2];
-    uint32_t vsc;     // V scale bytes of group g for rows 2c, 2c+1, 2c+8, 2c+9
-    {
-      const int rows[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
-      uint32_t sbytes[4];
+      const uint32_t ksa0 = prmt(sa, sa, 0x1010), ksa1 = prmt(sa, sa, 0x3232);
+      const uint32_t ksb0 = prmt(sb, sb, 0x1010), ksb1 = prmt(sb, sb, 0x3232);
+      float sa4[4] = {0.f, 0.f, 0.f, 0.f}, sb4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t rb = slot + rows[j] * CONTENT;
-        vw[j][0] = lds64(rb + VC_OFF + 16 * g);
-        vw[j][1] = lds64(rb + VC_OFF + 16 * g + 8);
-        sbytes[j] = lds32(rb + VS_OFF + 4 * (g >> 2)) >> (8 * (g & 3));
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t sA = j < 4 ? ksa0 : ksa1, sB = j < 4 ? ksb0 : ksb1;
+        const uint32_t a00 = hmul2(e2m1x2_to_f16x2<0>(kra[j]), sA), a01 = hmul2(e2m1x2_to_f16x2<1>(kra[j]), sA);
+        const uint32_t a02 = hmul2(e2m1x2_to_f16x2<2>(kra[j]), sA), a03 = hmul2(e2m1x2_to_f16x2<3>(kra[j]), sA);
+        const uint32_t b00 = hmul2(e2m1x2_to_f16x2<0>(krb[j]), sB), b01 = hmul2(e2m1x2_to_f16x2<1>(krb[j]), sB);
+        const uint32_t b02 = hmul2(e2m1x2_to_f16x2<2>(krb[j]), sB), b03 = hmul2(e2m1x2_to_f16x2<3>(krb[j]), sB);
+        // k-step 2j: dims 64c+8j+{0,1} | {2,3}; k-step 2j+1: dims +{4,5} | {6,7}
+        mma_f16_16816(sa4, a00, b00, a01, b01, qf[4 * j], qf[4 * j + 1]);
+        mma_f16_16816(sb4, a02, b02, a03, b03, qf[4 * j + 2], qf[4 * j + 3]);
       }
-      vsc = prmt(prmt(sbytes[0], sbytes[1], 0x0040), prmt(sbytes[2], sbytes[3], 0x0040), 0x5410);
-    }
-    if (partial) {
-      // tokens past the end may hold NaN scale bytes: zero their V words and scales
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int tok = t0 + 2 * c + (j & 1) + 8 * (j >> 1);
-        if (tok >= L) {
-          vw[j][0] = make_uint2(0, 0);
-          vw[j][1] = make_uint2(0, 0);
-          vsc &= ~(0xffu << (8 * j));
-        }
+      for (int r = 0; r < 4; ++r) x[h][r] = (sa4[r] + sb4[r]) * rowc;
+      if (partial) {
+        if (t0 + 16 * h + g >= L) { x[h][0] = -INFINITY; x[h][1] = -INFINITY; }
+        if (t0 + 16 * h + g + 8 >= L) { x[h][2] = -INFINITY; x[h][3] = -INFINITY; }
       }
     }
-    const uint32_t vs01 = e4m3x2_lo_to_f16x2(vsc);    // {s[2c], s[2c+1]}
-    const uint32_t vs89 = e4m3x2_hi_to_f16x2(vsc);    // {s[2c+8], s[2c+9]}
 
-    // ---- S^T (16 tokens x 8 rows) = K q_r^T
-    float sa4[4] = {0.f, 0.f, 0.f, 0.f}, sb4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t sA = j < 4 ? ksa0 : ksa1, sB = j < 4 ? ksb0 : ksb1;
-      const uint32_t a00 = hmul2(e2m1x2_to_f16x2<0>(kra[j]), sA), a01 = hmul2(e2m1x2_to_f16x2<1>(kra[j]), sA);
-      const uint32_t a02 = hmul2(e2m1x2_to_f16x2<2>(kra[j]), sA), a03 = hmul2(e2m1x2_to_f16x2<3>(kra[j]), sA);
-      const uint32_t b00 = hmul2(e2m1x2_to_f16x2<0>(krb[j]), sB), b01 = hmul2(e2m1x2_to_f16x2<1>(krb[j]), sB);
-      const uint32_t b02 = hmul2(e2m1x2_to_f16x2<2>(krb[j]), sB), b03 = hmul2(e2m1x2_to_f16x2<3>(krb[j]), sB);
-      // k-step 2j: dims 64c+8j+{0,1} | {2,3}; k-step 2j+1: dims +{4,5} | {6,7}
-      mma_f16_16816(sa4, a00, b00, a01, b01, qf[4 * j], qf[4 * j + 1]);
-      mma_f16_16816(sb4, a02, b02, a03, b03, qf[4 * j + 2], qf[4 * j + 3]);
-    }
-    float x0 = (sa4[0] + sb4[0]) * rowc, x1 = (sa4[1] + sb4[1]) * rowc;
-    float x2 = (sa4[2] + sb4[2]) * rowc, x3 = (sa4[3] + sb4[3]) * rowc;
-    if (partial) {
-      if (t0 + g >= L) { x0 = -INFINITY; x1 = -INFINITY; }
-      if (t0 + g + 8 >= L) { x2 = -INFINITY; x3 = -INFINITY; }
-    }
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+    // ---- online softmax over the 32 tokens (rows 2c, 2c+1 of this lane)
+    float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
+    float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
 #pragma unroll
     for (int sh = 4; sh < 32; sh <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
@@ -433,53 +483,87 @@ uq_partition_kernel(const UqParams p) {
       m_run[0] = mn0;
       m_run[1] = mn1;
     }
-    const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
-    const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
-    const uint32_t P01 = f32x2_to_f16x2(p0, p1);
-    const uint32_t P23 = f32x2_to_f16x2(p2, p3);
-    l_run[0] += f16_lo_to_f32(P01) + f16_lo_to_f32(P23);
-    l_run[1] += f16_hi_to_f32(P01) + f16_hi_to_f32(P23);
-    const uint32_t b0 = movmatrix_trans(P01);
-    const uint32_t b1 = movmatrix_trans(P23);
+    uint32_t bP[2][2];      // P^T B fragments per tile (tokens 2c.., 2c+8.. x row g)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t P01 = f32x2_to_f16x2(ex2(x[h][0] - mn0), ex2(x[h][1] - mn1));
+      const uint32_t P23 = f32x2_to_f16x2(ex2(x[h][2] - mn0), ex2(x[h][3] - mn1));
+      l_run[0] += f16_lo_to_f32(P01) + f16_lo_to_f32(P23);
+      l_run[1] += f16_hi_to_f32(P01) + f16_hi_to_f32(P23);
+      bP[h][0] = movmatrix_trans(P01);
+      bP[h][1] = movmatrix_trans(P23);
+    }
 
-    // ---- O^T += V^T P^T. For byte i of the lane's 16 V-code bytes, the low
-    // nibbles of tokens (2c, 2c+1) form index E (dim 32g+2i, m-tile i row g) and
-    // the high nibbles index O (dim 32g+2i+1, row g+8); likewise tokens 2c+8, 2c+9.
+    // ---- O^T += V^T P^T per tile. For byte i of the lane's 16 V-code bytes,
+    // the low nibbles of tokens (2c, 2c+1) form index E (dim 32g+2i, m-tile i
+    // row g) and the high nibbles index O (dim 32g+2i+1, row g+8); likewise
+    // tokens 2c+8, 2c+9.
 #pragma unroll
-    for (int wq = 0; wq < 4; ++wq) {          // 4 code bytes (m-tiles 4wq..4wq+3) per word
-      const uint32_t w0 = wq < 2 ? (wq == 0 ? vw[0][0].x : vw[0][0].y) : (wq == 2 ? vw[0][1].x : vw[0][1].y);
-      const uint32_t w1 = wq < 2 ? (wq == 0 ? vw[1][0].x : vw[1][0].y) : (wq == 2 ? vw[1][1].x : vw[1][1].y);
-      const uint32_t w8 = wq < 2 ? (wq == 0 ? vw[2][0].x : vw[2][0].y) : (wq == 2 ? vw[2][1].x : vw[2][1].y);
-      const uint32_t w9 = wq < 2 ? (wq == 0 ? vw[3][0].x : vw[3][0].y) : (wq == 2 ? vw[3][1].x : vw[3][1].y);
-      // index bytes: token pair (2c, 2c+1) even/odd dims, token pair (2c+8, 2c+9)
-      const uint32_t Ea = (w0 & 0x0F0F0F0Fu) | ((w1 & 0x0F0F0F0Fu) << 4);
-      const uint32_t Oa = ((w0 >> 4) & 0x0F0F0F0Fu) | (w1 & 0xF0F0F0F0u);
-      const uint32_t Eb = (w8 & 0x0F0F0F0Fu) | ((w9 & 0x0F0F0F0Fu) << 4);
-      const uint32_t Ob = ((w8 >> 4) & 0x0F0F0F0Fu) | (w9 & 0xF0F0F0F0u);
-      uint32_t fa[4][4];    // [byte][a0 a1 a2 a3]
-      if (e2m1_table) {
-        fa[0][0] = e2m1x2_to_f16x2<0>(Ea); fa[0][1] = e2m1x2_to_f16x2<0>(Oa);
-        fa[0][2] = e2m1x2_to_f16x2<0>(Eb); fa[0][3] = e2m1x2_to_f16x2<0>(Ob);
-        fa[1][0] = e2m1x2_to_f16x2<1>(Ea); fa[1][1] = e2m1x2_to_f16x2<1>(Oa);
-        fa[1][2] = e2m1x2_to_f16x2<1>(Eb); fa[1][3] = e2m1x2_to_f16x2<1>(Ob);
-        fa[2][0] = e2m1x2_to_f16x2<2>(Ea); fa[2][1] = e2m1x2_to_f16x2<2>(Oa);
-        fa[2][2] = e2m1x2_to_f16x2<2>(Eb); fa[2][3] = e2m1x2_to_f16x2<2>(Ob);
-        fa[3][0] = e2m1x2_to_f16x2<3>(Ea); fa[3][1] = e2m1x2_to_f16x2<3>(Oa);
-        fa[3][2] = e2m1x2_to_f16x2<3>(Eb); fa[3][3] = e2m1x2_to_f16x2<3>(Ob);
-      } else {
+    for (int h = 0; h < 2; ++h) {
+      // V: rows 2c, 2c+1, 2c+8, 2c+9 of tile h, code bytes [16g, 16g+16) -> dims [32g, 32g+32)
+      uint2 vw[4][2];
+      uint32_t vsc;     // V scale bytes of group g for those rows
+      {
+        uint32_t sbytes[4];
 #pragma unroll
-        for (int bq = 0; bq < 4; ++bq) {
-          fa[bq][0] = lds32(lut + (((Ea >> (8 * bq)) & 0xFFu) << 7));
-          fa[bq][1] = lds32(lut + (((Oa >> (8 * bq)) & 0xFFu) << 7));
-          fa[bq][2] = lds32(lut + (((Eb >> (8 * bq)) & 0xFFu) << 7));
-          fa[bq][3] = lds32(lut + (((Ob >> (8 * bq)) & 0xFFu) << 7));
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t rb = slot + (16 * h + 2 * c + (j & 1) + 8 * (j >> 1)) * CONTENT;
+          vw[j][0] = lds64(rb + VC_OFF + 16 * g);
+          vw[j][1] = lds64(rb + VC_OFF + 16 * g + 8);
+          sbytes[j] = lds32(rb + VS_OFF + 4 * (g >> 2)) >> (8 * (g & 3));
+        }
+        vsc = prmt(prmt(sbytes[0], sbytes[1], 0x0040), prmt(sbytes[2], sbytes[3], 0x0040), 0x5410);
+      }
+      if (partial) {
+        // tokens past the end may hold NaN scale bytes: zero their V words and scales
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int tok = t0 + 16 * h + 2 * c + (j & 1) + 8 * (j >> 1);
+          if (tok >= L) {
+            vw[j][0] = make_uint2(0, 0);
+            vw[j][1] = make_uint2(0, 0);
+            vsc &= ~(0xffu << (8 * j));
+          }
         }
       }
+      const uint32_t vs01 = e4m3x2_lo_to_f16x2(vsc);    // {s[2c], s[2c+1]}
+      const uint32_t vs89 = e4m3x2_hi_to_f16x2(vsc);    // {s[2c+8], s[2c+9]}
 #pragma unroll
-      for (int bq = 0; bq < 4; ++bq) {
-        const int i = 4 * wq + bq;
-        mma_f16_16816(o[i], hmul2(fa[bq][0], vs01), hmul2(fa[bq][1], vs01), hmul2(fa[bq][2], vs89),
-                      hmul2(fa[bq][3], vs89), b0, b1);
+      for (int wq = 0; wq < 4; ++wq) {          // 4 code bytes (m-tiles 4wq..4wq+3) per word
+        const uint32_t w0 = wq < 2 ? (wq == 0 ? vw[0][0].x : vw[0][0].y) : (wq == 2 ? vw[0][1].x : vw[0][1].y);
+        const uint32_t w1 = wq < 2 ? (wq == 0 ? vw[1][0].x : vw[1][0].y) : (wq == 2 ? vw[1][1].x : vw[1][1].y);
+        const uint32_t w8 = wq < 2 ? (wq == 0 ? vw[2][0].x : vw[2][0].y) : (wq == 2 ? vw[2][1].x : vw[2][1].y);
+        const uint32_t w9 = wq < 2 ? (wq == 0 ? vw[3][0].x : vw[3][0].y) : (wq == 2 ? vw[3][1].x : vw[3][1].y);
+        // index bytes: token pair (2c, 2c+1) even/odd dims, token pair (2c+8, 2c+9)
+        const uint32_t Ea = (w0 & 0x0F0F0F0Fu) | ((w1 & 0x0F0F0F0Fu) << 4);
+        const uint32_t Oa = ((w0 >> 4) & 0x0F0F0F0Fu) | (w1 & 0xF0F0F0F0u);
+        const uint32_t Eb = (w8 & 0x0F0F0F0Fu) | ((w9 & 0x0F0F0F0Fu) << 4);
+        const uint32_t Ob = ((w8 >> 4) & 0x0F0F0F0Fu) | (w9 & 0xF0F0F0F0u);
+        uint32_t fa[4][4];    // [byte][a0 a1 a2 a3]
+        if (e2m1_table) {
+          fa[0][0] = e2m1x2_to_f16x2<0>(Ea); fa[0][1] = e2m1x2_to_f16x2<0>(Oa);
+          fa[0][2] = e2m1x2_to_f16x2<0>(Eb); fa[0][3] = e2m1x2_to_f16x2<0>(Ob);
+          fa[1][0] = e2m1x2_to_f16x2<1>(Ea); fa[1][1] = e2m1x2_to_f16x2<1>(Oa);
+          fa[1][2] = e2m1x2_to_f16x2<1>(Eb); fa[1][3] = e2m1x2_to_f16x2<1>(Ob);
+          fa[2][0] = e2m1x2_to_f16x2<2>(Ea); fa[2][1] = e2m1x2_to_f16x2<2>(Oa);
+          fa[2][2] = e2m1x2_to_f16x2<2>(Eb); fa[2][3] = e2m1x2_to_f16x2<2>(Ob);
+          fa[3][0] = e2m1x2_to_f16x2<3>(Ea); fa[3][1] = e2m1x2_to_f16x2<3>(Oa);
+          fa[3][2] = e2m1x2_to_f16x2<3>(Eb); fa[3][3] = e2m1x2_to_f16x2<3>(Ob);
+        } else {
+#pragma unroll
+          for (int bq = 0; bq < 4; ++bq) {
+            fa[bq][0] = lds32(lut + (((Ea >> (8 * bq)) & 0xFFu) * (LUT_COPIES * 4)));
+            fa[bq][1] = lds32(lut + (((Oa >> (8 * bq)) & 0xFFu) * (LUT_COPIES * 4)));
+            fa[bq][2] = lds32(lut + (((Eb >> (8 * bq)) & 0xFFu) * (LUT_COPIES * 4)));
+            fa[bq][3] = lds32(lut + (((Ob >> (8 * bq)) & 0xFFu) * (LUT_COPIES * 4)));
+          }
+        }
+#pragma unroll
+        for (int bq = 0; bq < 4; ++bq) {
+          const int i = 4 * wq + bq;
+          mma_f16_16816(o[i], hmul2(fa[bq][0], vs01), hmul2(fa[bq][1], vs01), hmul2(fa[bq][2], vs89),
+                        hmul2(fa[bq][3], vs89), bP[h][0], bP[h][1]);
+        }
       }
     }
     __syncwarp();
@@ -520,6 +604,24 @@ uq_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ pa
 }
 
 // ------------------------------------------------------------------ host side
+// Warps per item: the smallest W (fewest merges) among those that minimise the
+// per-warp slice count of the launch, rounds x slices per warp per item, with
+// items bounded by the longest sequence the block table allows.
+int uq_warps_per_item(long long items, int max_blocks, int block_size, int num_partitions, int num_sms) {
+  const long long groups_per_tile = (long long)uq::TG / uq::SLICE;
+  const long long tiles = ((long long)max_blocks * block_size + uq::TG - 1) / uq::TG;
+  const long long tiles_per_item = std::max<long long>(1, (tiles + num_partitions - 1) / num_partitions);
+  int best_w = 4;
+  long long best = -1;
+  for (int w = 1; w <= 4; w *= 2) {
+    const long long slots = (long long)uq::CTAS_PER_SM * num_sms * (uq::NW / w);
+    const long long rounds = (items + slots - 1) / slots;
+    const long long cost = rounds * tiles_per_item * groups_per_tile / w;
+    if (best < 0 || cost < best) { best = cost; best_w = w; }
+  }
+  return best_w;
+}
+
 cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream) {
   UqParams p;
   p.q = static_cast<const uint16_t*>(a.q);
@@ -545,9 +647,16 @@ cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream) {
   p.softmax_scale = a.softmax_scale;
   const long long items = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   if (items <= 0) return cudaSuccess;
-  const int grid = (int)std::min<long long>(items, (long long)uq::CTAS_PER_SM * a.num_sms);
-  cudaFuncSetAttribute(uq_partition_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, uq::SMEM);
-  uq_partition_kernel<<<grid, uq::THREADS, uq::SMEM, stream>>>(p);
+  const int W = uq_warps_per_item(items, a.max_blocks, a.block_size, a.num_partitions, a.num_sms);
+  const long long ctas = (items + uq::NW / W - 1) / (uq::NW / W);
+  const int grid = (int)std::min<long long>(ctas, (long long)uq::CTAS_PER_SM * a.num_sms);
+  auto launch = [&](auto kern) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, uq::SMEM);
+    kern<<<grid, uq::THREADS, uq::SMEM, stream>>>(p);
+  };
+  if (W == 1) launch(uq_partition_kernel<1>);
+  else if (W == 2) launch(uq_partition_kernel<2>);
+  else launch(uq_partition_kernel<4>);
   return cudaGetLastError();
 }
 

@@ -73,6 +73,40 @@ def test_bf16_output_and_determinism():
     assert torch.max(torch.abs(o16.float() - a)).item() <= torch.max(torch.abs(a)).item() * 2 ** -8 + 1e-6
 
 
+def _warps_per_item(items, max_tokens, P, sms):
+    """The launcher's choice of warps per item: the smallest W among those with
+    the fewest slices per warp (rounds x slices of an item / W) on one
+    8-warp CTA per SM."""
+    tiles_per_item = max(1, -(-(-(-max_tokens // 256)) // P))
+    best_w, best = 4, None
+    for w in (1, 2, 4):
+        slots = sms * (8 // w)
+        cost = -(-items // slots) * tiles_per_item * 8 // w
+        if best is None or cost < best:
+            best, best_w = cost, w
+    return best_w
+
+
+@pytest.mark.parametrize("lens,P,want_w,rand", [
+    ([64000, 9000], 250, 1, False),     # 1000 items: one warp per item on 152 SMs
+    ([64000, 9000], 250, 1, True),
+    ([30720, 7000], 120, 2, False),     # 480 items: two warps per item
+    ([30720, 7000], 40, 4, False),      # 160 items: four warps per item
+])
+def test_warps_per_item(lens, P, want_w, rand):
+    """Item groups of 1, 2 and 4 warps (the launcher picks W from the item
+    count); ragged lengths leave most partitions of the short sequence empty."""
+    cent = synth.sorted_random_centroids(7) if rand else None
+    c = synth.make_uq_case(260 + P + int(rand), lens, 2, 8, 64, 288, centroids=cent)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    max_tokens = c.block_table.shape[1] * c.block_size
+    w = _warps_per_item(c.num_seqs * c.num_kv_heads * P, max_tokens, P, sms)
+    if sms == 152:
+        assert w == want_w
+    out, _, _ = UqDev(c).run(P)
+    _check(c, out.cpu().double().numpy(), what=f"W={w} P={P}")
+
+
 def _sampled_units(c, n, seed):
     rng = np.random.default_rng(seed)
     all_units = [(s, h) for s in range(c.num_seqs) for h in range(c.num_kv_heads)]
