@@ -1,27 +1,40 @@
-// Flash-combine of split-KV partials for one query row ([PA] "parallel
-// flash-combine reduce kernel"): M = max_p m_p, w_p = l_p exp(m_p - M),
+// Flash-combine of split-KV partials for one query row (the [PA] page's
+// cross-partition reduce): M = max_p m_p, w_p = l_p exp(m_p - M),
 // o = sum_p w_p O_p / sum_p w_p. An empty partition (m_p = -inf) has weight
 // exactly 0; the exponent argument is clamped so no NaN can arise.
 //
-// One 128-thread CTA per row. The first chunk of O loads and all (m, l)
-// loads are issued before any dependent work, so a row costs one global
-// round trip plus one more per further chunk of 8 partitions per thread.
+// One CTA per row. The first chunk of O loads and all (m, l) loads are
+// issued before any dependent work.
 #pragma once
 #include "common.cuh"
 
 namespace qpa {
 
-constexpr int kCombineThreads = 128;
+// Threads of a row CTA are NVEC = D/4 float4 columns times nsub partition
+// subsets; thread (sub, column) takes partitions sub, sub + nsub, ... and
+// issues up to KMAX of those loads at once, so that a row costs one global
+// round trip when P <= nsub * KMAX. nsub grows with P up to
+// kCombineMaxThreads threads.
+constexpr int kCombineMaxThreads = 512;
+constexpr int kCombineKmax128 = 16;     // partitions per thread and round trip, D = 128
+constexpr int kCombineKmax256 = 20;     // D = 256
+
+inline int combine_threads(int d, int kmax, int num_partitions) {
+  const int nvec = d / 4;
+  int nsub = (num_partitions + kmax - 1) / kmax;
+  if (nsub < 1) nsub = 1;
+  if (nsub > kCombineMaxThreads / nvec) nsub = kCombineMaxThreads / nvec;
+  return nvec * nsub;
+}
 
 // Returns in vec[0..D) (shared memory) the combined row. `sw` is dynamic
-// shared scratch of at least 2*P + 4*128 floats (16-byte aligned).
-template <int D>
+// shared scratch of combine_smem_bytes(P, threads) bytes (16-byte aligned).
+template <int D, int KMAX>
 __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, const float* __restrict__ part_m,
                                             const float* __restrict__ part_l, long long rbase, int qg,
                                             int num_partitions, float* sw, float* vec) {
   constexpr int NVEC = D / 4;                  // float4 per row
-  constexpr int NSUB = kCombineThreads / NVEC; // partition subsets
-  constexpr int CH = 8;                        // partitions per thread per chunk
+  const int nsub = blockDim.x / NVEC;          // partition subsets
   const int P = num_partitions;
   const int tid = threadIdx.x, lane = tid & 31;
   const int v4 = tid % NVEC, sub = tid / NVEC;
@@ -30,17 +43,19 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
   float4* part = reinterpret_cast<float4*>(sw + ((2 * P + 3) & ~3));
   // rbase = ((seq * Hk + kvh) * P) * qg + r: partition pp of the row is at rbase + pp * qg
   const float* ob = part_o + rbase * D + 4 * v4;
-  float4 o[CH];
+  const long long pstride = (long long)qg * D;
+  float4 o[KMAX];
 #pragma unroll
-  for (int k = 0; k < CH; ++k) {
-    const int pp = sub + k * NSUB;
-    o[k] = pp < P ? __ldg(reinterpret_cast<const float4*>(ob + (long long)pp * qg * D)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < KMAX; ++k) {
+    const int pp = sub + k * nsub;
+    o[k] = pp < P ? __ldg(reinterpret_cast<const float4*>(ob + pp * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int pp = tid; pp < P; pp += kCombineThreads) {
+  for (int pp = tid; pp < P; pp += blockDim.x) {
     ms[pp] = part_m[rbase + (long long)pp * qg];
     ls[pp] = part_l[rbase + (long long)pp * qg];
   }
   __syncthreads();
+  // every warp reduces the maximum and the denominator over all partitions
   float M = -INFINITY;
   for (int pp = lane; pp < P; pp += 32) M = fmaxf(M, ms[pp]);
 #pragma unroll
@@ -56,22 +71,22 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
   const float inv = den > 0.f ? 1.f / den : 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < CH; ++k) {
-    const int pp = sub + k * NSUB;
+  for (int k = 0; k < KMAX; ++k) {
+    const int pp = sub + k * nsub;
     if (pp < P) {
       const float w = weight(pp);
       acc.x += w * o[k].x; acc.y += w * o[k].y; acc.z += w * o[k].z; acc.w += w * o[k].w;
     }
   }
-  for (int base = CH * NSUB; base < P; base += CH * NSUB) {
+  for (int base = KMAX * nsub; base < P; base += KMAX * nsub) {
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      const int pp = base + sub + k * NSUB;
-      o[k] = pp < P ? __ldg(reinterpret_cast<const float4*>(ob + (long long)pp * qg * D)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < KMAX; ++k) {
+      const int pp = base + sub + k * nsub;
+      o[k] = pp < P ? __ldg(reinterpret_cast<const float4*>(ob + pp * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      const int pp = base + sub + k * NSUB;
+    for (int k = 0; k < KMAX; ++k) {
+      const int pp = base + sub + k * nsub;
       if (pp < P) {
         const float w = weight(pp);
         acc.x += w * o[k].x; acc.y += w * o[k].y; acc.z += w * o[k].z; acc.w += w * o[k].w;
@@ -81,8 +96,7 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
   part[tid] = acc;
   __syncthreads();
   if (sub == 0) {
-#pragma unroll
-    for (int s = 1; s < NSUB; ++s) {
+    for (int s = 1; s < nsub; ++s) {
       const float4 b = part[s * NVEC + v4];
       acc.x += b.x; acc.y += b.y; acc.z += b.z; acc.w += b.w;
     }
@@ -94,8 +108,8 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
   __syncthreads();
 }
 
-inline size_t combine_smem_bytes(int num_partitions) {
-  return (size_t((2 * num_partitions + 3) & ~3) + 4 * kCombineThreads) * sizeof(float);
+inline size_t combine_smem_bytes(int num_partitions, int threads) {
+  return (size_t((2 * num_partitions + 3) & ~3) + 4 * size_t(threads)) * sizeof(float);
 }
 
 }  // namespace qpa

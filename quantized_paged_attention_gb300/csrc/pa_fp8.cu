@@ -730,7 +730,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 // Flash-combine of the partitions ([PA] reduce kernel): one CTA per query
 // row (seq, kv_head, r), see combine_row.
 template <typename OutT>
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineMaxThreads)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
                const float* __restrict__ part_l, OutT* __restrict__ out, int num_kv_heads, int qg,
                int num_partitions, long long out_stride_seq, long long out_stride_head) {
@@ -741,7 +741,8 @@ combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_
   const int r = row % qg;
   const int sk = row / qg;                    // seq * Hk + kvh
   const int seq = sk / num_kv_heads, kvh = sk % num_kv_heads;
-  combine_row<fp8::D>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg, num_partitions, sw, vec);
+  combine_row<fp8::D, kCombineKmax128>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg,
+                                       num_partitions, sw, vec);
   if (threadIdx.x < fp8::D / 4) {
     const int t = threadIdx.x;
     OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + 4 * t;
@@ -791,12 +792,13 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
 template <typename OutT>
 static cudaError_t launch_combine_t(const CombineLaunch& a, OutT* out, cudaStream_t stream) {
   const int grid = a.num_seqs * a.num_kv_heads * a.qg;
-  const size_t smem = combine_smem_bytes(a.num_partitions);
+  const int threads = combine_threads(fp8::D, kCombineKmax128, a.num_partitions);
+  const size_t smem = combine_smem_bytes(a.num_partitions, threads);
   if (smem > 40 * 1024)
     cudaFuncSetAttribute(combine_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kCombineThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -572,9 +572,10 @@ uq_partition_kernel(const UqParams p) {
 }
 
 // Combine the partitions of one query row (combine_row) and rotate it back:
-// out = o_r H/16, 8 butterfly stages over the 256 dims, one pair per thread.
+// out = o_r H/16, 8 butterfly stages over the 256 dims (128 pairs per stage,
+// one or two per thread: a row CTA has at least 64 threads).
 template <typename OutT>
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineMaxThreads)
 uq_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
                   const float* __restrict__ part_l, OutT* __restrict__ out, int num_kv_heads, int qg,
                   int num_partitions, long long out_stride_seq, long long out_stride_head) {
@@ -587,13 +588,18 @@ uq_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ pa
   const int sk = row / qg;
   const int seq = sk / num_kv_heads, kvh = sk % num_kv_heads;
   const int tid = threadIdx.x;
-  combine_row<D>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg, num_partitions, sw, vec);
+  combine_row<D, kCombineKmax256>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg,
+                                  num_partitions, sw, vec);
+  const int pa = tid, pb = tid + blockDim.x;      // this thread's pairs (pb only when blockDim is 64)
   for (int st = 1; st < D; st <<= 1) {
-    const int i = ((tid & ~(st - 1)) << 1) | (tid & (st - 1));   // index with bit `st` clear
-    const float x = vec[i], y = vec[i + st];
+    const int ia = ((pa & ~(st - 1)) << 1) | (pa & (st - 1));   // index with bit `st` clear
+    const int ib = ((pb & ~(st - 1)) << 1) | (pb & (st - 1));
+    float xa = 0.f, ya = 0.f, xb = 0.f, yb = 0.f;
+    if (pa < D / 2) { xa = vec[ia]; ya = vec[ia + st]; }
+    if (pb < D / 2) { xb = vec[ib]; yb = vec[ib + st]; }
     __syncthreads();
-    vec[i] = x + y;
-    vec[i + st] = x - y;
+    if (pa < D / 2) { vec[ia] = xa + ya; vec[ia + st] = xa - ya; }
+    if (pb < D / 2) { vec[ib] = xb + yb; vec[ib + st] = xb - yb; }
     __syncthreads();
   }
   if (tid < D / 4) {
@@ -663,12 +669,13 @@ cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream) {
 template <typename OutT>
 static cudaError_t launch_uq_combine_t(const CombineLaunch& a, OutT* out, cudaStream_t stream) {
   const int grid = a.num_seqs * a.num_kv_heads * a.qg;
-  const size_t smem = combine_smem_bytes(a.num_partitions);
+  const int threads = combine_threads(256, kCombineKmax256, a.num_partitions);
+  const size_t smem = combine_smem_bytes(a.num_partitions, threads);
   if (smem > 40 * 1024)
     cudaFuncSetAttribute(uq_combine_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kCombineThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -56,8 +56,9 @@ def test_tiny_partials_match_oracle_partitions():
             assert np.max(np.abs(O[s, 0, p] - rO[p])) <= 2e-3 * vmax
 
 
-@pytest.mark.parametrize("P", [1, 2, 3, 7, 32, 100])
+@pytest.mark.parametrize("P", [1, 2, 3, 7, 32, 100, 300])
 def test_partition_counts_ragged(P):
+    # P = 300 takes two rounds of the combine kernel's partition loads
     lens = [0, 1, 15, 16, 17, 63, 64, 65, 255, 256, 257, 1000, 2049]
     c = synth.make_fp8_case(40 + P, lens, 2, 8, 128, 16)
     out, _, _ = Fp8Dev(c).run(P)
