@@ -351,9 +351,11 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 
       // ---- item done: row sums over the group's 128 token lanes, merge of the
       // groups' (m, l, O) to a common maximum, partials of the item. The group
-      // that owns the item's last tile merges (the other one finished first).
+      // that does not own the item's last tile merges: it finished first, and
+      // with an even tile count per item the owner of the last tile would
+      // otherwise always be the same group, which then carries every merge.
       const uint32_t kph = (qcnt >> 1) & 1;
-      const int merger = NWG == 2 ? ((j - 1) & 1) : 0;
+      const int merger = NWG == 2 ? (j & 1) : 0;
       // (the buffers of item qcnt - 2 must have been read by its merger)
       if (NWG == 2 && qcnt >= 2 &&
           !warp_wait(&mfree[qb], ((qcnt >> 1) - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) { ok = false; break; }
