@@ -36,6 +36,7 @@
 #include "common.cuh"
 #include "qpa_internal.h"
 #include "combine.cuh"
+#include "tc.cuh"
 
 namespace qpa {
 
@@ -56,9 +57,13 @@ constexpr int lutOff = NW * DEPTH * SLOT_BYTES;  // 208896 (a multiple of 128)
 constexpr int mOff = lutOff + LUT_BYTES;
 constexpr int lOff = mOff + NW * 8 * 4;
 constexpr int fOff = lOff + NW * 8 * 4;
-constexpr int SMEM = fOff + NW * 4;              // 225824 bytes: one CTA per SM
+constexpr int barOff = fOff + NW * 4;            // [NW][DEPTH] slot barriers (8-byte aligned)
+constexpr int abortOff = barOff + NW * DEPTH * 8;
+constexpr int SMEM = abortOff + 16 + 128;        // + alignment slack: one CTA per SM
 constexpr int CTAS_PER_SM = 1;
 static_assert(SMEM <= 232448, "shared memory");
+static_assert(barOff % 8 == 0 && SLOT_BYTES % 128 == 0, "alignment");
+constexpr int TMA_ROWS = 16;                     // token rows per tensor-map box
 }  // namespace uq
 
 struct UqParams {
@@ -85,12 +90,14 @@ __device__ __forceinline__ float e2m1_value(int k) {
 
 template <int W>
 __global__ void __launch_bounds__(uq::THREADS, uq::CTAS_PER_SM)
-uq_partition_kernel(const UqParams p) {
+uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p) {
   using namespace uq;
   static_assert(W == 1 || W == 2 || W == 4, "warps per item");
   constexpr int GROUPS = NW / W;              // item groups per CTA
   constexpr int SLICES_PER_WARP = TG / SLICE / W;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the tensor-map copies need 128-byte aligned destinations
+  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int grp = warp / W;                   // this warp's item group
@@ -104,6 +111,15 @@ uq_partition_kernel(const UqParams p) {
   float* ms = reinterpret_cast<float*>(smem + mOff);
   float* ls = reinterpret_cast<float*>(smem + lOff);
   uint32_t* fslot = reinterpret_cast<uint32_t*>(smem + fOff);
+  uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + barOff) + warp * DEPTH;   // this warp's slot barriers
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + abortOff);
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < DEPTH; ++i) mbar_init(&sbar[i], 1);
+    if (warp == 0) *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0) prefetch_tmap(&kv_map);
   const uint32_t lut = smem_u32(smem + lutOff) + (lane & (LUT_COPIES - 1)) * 4;   // this lane's bank copy
 
   // ---- centroid table: the e2m1 table takes the cvt path, anything else the
@@ -129,7 +145,6 @@ uq_partition_kernel(const UqParams p) {
 
   const uint64_t pol = policy_evict_first();
   const uint32_t ring = smem_u32(smem + ringOff) + warp * DEPTH * SLOT_BYTES;
-  const size_t tok_stride = size_t(p.num_kv_heads) * p.padded_slot;    // bytes between tokens
 
   // ---------------------------------------------------------------- issue side
   int ik_item = blockIdx.x * GROUPS + grp;
@@ -151,9 +166,19 @@ uq_partition_kernel(const UqParams p) {
   if (ik_item < num_items) i_L = load_len(ik_item);
   i_Lnext = load_len(ik_item + item_stride);
 
+  // Event e of this warp's ring: lane 0 arms slot e % DEPTH's barrier with
+  // the bytes it copies (query rows, or the slice's two 16-token boxes of
+  // 272-byte slots through the tensor map) and issues the copies; an event
+  // without copies is a plain arrival. The warp read the slot's previous
+  // contents before (program order and the __syncwarp/named barriers), and
+  // lane 0 orders those generic accesses before the asynchronous writes.
   auto issue = [&](int e) {
     const uint32_t slot = ring + (e % DEPTH) * SLOT_BYTES;
+    uint64_t* bar = &sbar[e % DEPTH];
     int kind = UEV_NONE, a = 0, b = 0;
+    bool armed = false;        // (warp-uniform) lane 0 armed the barrier with copies
+    __syncwarp();
+    if (lane == 0) fence_proxy_async();
     while (true) {
       if (ik_item >= num_items) break;
       if (i_state == 0) {
@@ -167,10 +192,12 @@ uq_partition_kernel(const UqParams p) {
         if (i_part * TG < i_L) {
           // query rows: qg rows x 512 B
           const uint16_t* qrow0 = p.q + i_seq * p.q_stride_seq + (long long)(i_kvh * p.qg) * p.q_stride_head;
-          for (int idx = lane; idx < p.qg * 32; idx += 32) {
-            const int row = idx >> 5, ch = idx & 31;
-            cp_async16(slot + row * 512 + ch * 16, qrow0 + row * p.q_stride_head + ch * 8, pol);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar, p.qg * 512);
+            for (int row = 0; row < p.qg; ++row)
+              bulk_load(slot + row * 512, qrow0 + row * p.q_stride_head, 512, bar);
           }
+          armed = true;
           i_ent = load_entries(i_seq, i_part, i_L);
           if ((i_part + P) * TG < i_L) i_nent = load_entries(i_seq, i_part + P, i_L);
         }
@@ -207,41 +234,22 @@ uq_partition_kernel(const UqParams p) {
         pa = (pa < 0 || pa >= p.num_blocks) ? 0 : pa;
         pb = (pb < 0 || pb >= p.num_blocks) ? 0 : pb;
       }
-      // 32 token slots of this KV head, 272 bytes each, copied as whole
-      // 128-byte runs so that the L2 requests cover full sectors of few lines:
-      // eight lanes copy bytes [0, 128) or [128, 256) of one token, four
-      // tokens per instruction (tokens 4i + lane/8), and one instruction
-      // copies every token's last 16 bytes. Tokens 0..15 of the slice lie in
-      // block pa, 16..31 in block pb (the same block unless block_size is 16);
-      // slots past the end of the sequence are read from the blocks the table
-      // names (or block 0) and masked by the consumer.
-      const uint8_t* head = p.kv + size_t(i_kvh) * p.padded_slot;
-      const uint8_t* rowa = head + (size_t(pa) * bs + (t0 & (bs - 1))) * tok_stride;          // token 0
-      const uint8_t* rowb = head + (size_t(pb) * bs + ((t0 + 16) & (bs - 1))) * tok_stride;   // token 16
-      {
-        const int q4 = lane >> 3;
-        const uint32_t off = 16 * (lane & 7);
-        const uint8_t* sa = rowa + size_t(q4) * tok_stride + off;
-        const uint8_t* sb = rowb + size_t(q4) * tok_stride + off;
-        const uint32_t d = slot + q4 * CONTENT + off;
-        const size_t step4 = 4 * tok_stride;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          cp_async16(d + 4 * i * CONTENT, sa + i * step4, pol);
-          cp_async16(d + 4 * i * CONTENT + 128, sa + i * step4 + 128, pol);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          cp_async16(d + (16 + 4 * i) * CONTENT, sb + i * step4, pol);
-          cp_async16(d + (16 + 4 * i) * CONTENT + 128, sb + i * step4 + 128, pol);
-        }
-        const uint8_t* st = (lane < 16 ? rowa + size_t(lane) * tok_stride : rowb + size_t(lane - 16) * tok_stride) + 256;
-        cp_async16(slot + lane * CONTENT + 256, st, pol);
+      // 32 token slots of this KV head, 272 bytes each: two boxes of 16 token
+      // rows through the tensor map (x = the slot's 2-byte units from 0,
+      // y = KV head, z = token row of the cache). Tokens 0..15 of the slice
+      // lie in block pa, 16..31 in block pb (the same block unless block_size
+      // is 16); slots past the end of the sequence are read from the blocks
+      // the table names (or block 0) and masked by the consumer.
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, SLOT_BYTES);
+        tma_load_3d(slot, &kv_map, 0, i_kvh, pa * bs + (t0 & (bs - 1)), bar, pol);
+        tma_load_3d(slot + TMA_ROWS * CONTENT, &kv_map, 0, i_kvh, pb * bs + ((t0 + 16) & (bs - 1)), bar, pol);
       }
+      armed = true;
       kind = UEV_SLICE; a = s; b = i_L;
       break;
     }
-    cp_async_commit();
+    if (!armed && lane == 0) mbar_arrive(bar);   // no copies: the event's phase completes at once
     if (lane == e % DEPTH) { rec_kind = kind; rec_a = a; rec_b = b; }
   };
 
@@ -364,8 +372,12 @@ uq_partition_kernel(const UqParams p) {
 
     if (kind == UEV_NONE) break;
     issue(e + DEPTH - 1);
-    cp_async_wait<DEPTH - 1>();
-    __syncwarp();
+    if (!warp_wait(&sbar[e % DEPTH], (e / DEPTH) & 1, abort_flag, KERR_TIMEOUT_FULL)) {
+      // give the copies still in flight a bounded time to land before the
+      // CTA's shared memory goes away
+      for (int d = 0; d < DEPTH; ++d) mbar_wait(&sbar[(e + d) % DEPTH], ((e + d) / DEPTH) & 1, KERR_TIMEOUT_FULL);
+      break;
+    }
     const uint32_t slot = ring + (e % DEPTH) * SLOT_BYTES;
 
     if (kind == UEV_ITEM) {
@@ -568,7 +580,6 @@ uq_partition_kernel(const UqParams p) {
     }
     __syncwarp();
   }
-  cp_async_wait<0>();
 }
 
 // Combine the partitions of one query row (combine_row) and rotate it back:
@@ -628,7 +639,40 @@ int uq_warps_per_item(long long items, int max_blocks, int block_size, int num_p
   return best_w;
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link-time dependency on the driver library); null if the driver lacks it.
+static EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
 cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream) {
+  // the slot cache as a 3-D tensor of 2-byte units: x = unit within a
+  // (token, head) slot, y = KV head, z = token row (block * block_size + t);
+  // a box is 136 units (the 272 used bytes) x 1 head x 16 token rows
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap kv_map;
+  const cuuint64_t dims[3] = {(cuuint64_t)(a.padded_slot / 2), (cuuint64_t)a.num_kv_heads,
+                              (cuuint64_t)a.num_blocks * (cuuint64_t)a.block_size};
+  const cuuint64_t strides[2] = {(cuuint64_t)a.padded_slot, (cuuint64_t)a.padded_slot * a.num_kv_heads};
+  const cuuint32_t box[3] = {uq::CONTENT / 2, 1, uq::TMA_ROWS};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&kv_map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint8_t*>(a.kv), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   UqParams p;
   p.q = static_cast<const uint16_t*>(a.q);
   p.kv = a.kv;
@@ -658,7 +702,7 @@ cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream) {
   const int grid = (int)std::min<long long>(ctas, (long long)uq::CTAS_PER_SM * a.num_sms);
   auto launch = [&](auto kern) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, uq::SMEM);
-    kern<<<grid, uq::THREADS, uq::SMEM, stream>>>(p);
+    kern<<<grid, uq::THREADS, uq::SMEM, stream>>>(kv_map, p);
   };
   if (W == 1) launch(uq_partition_kernel<1>);
   else if (W == 2) launch(uq_partition_kernel<2>);
