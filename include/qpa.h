@@ -239,7 +239,7 @@ int nvfp4_index_score(const uint8_t* q, const uint8_t* kv_pages, const int32_t* 
 /* ------------------------------------------------------------------------
  * pa_decode_fp8_static -- pa_decode_fp8 without a workspace argument.
  *
- * The paper has no counterpart; this is a convenience of this library. It is
+ * The source pages describe no counterpart; this is a convenience of this library. It is
  * meant for callers that cannot call cudaMalloc or otherwise obtain device
  * memory: for example a plugin whose host framework hands it only its input
  * and output tensors, with every device allocation owned by the host
