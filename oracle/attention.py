@@ -92,6 +92,52 @@ def pa_decode_fp8(q_bits, kv_cache, block_table, seq_lens, k_scale, v_scale,
     return out
 
 
+def dense_kv_fp8_per_token(kv_cache, block_table, seq, kv_head, L, k_scales, v_scales):
+    """Dequantised K and V [L, D] of one (sequence, KV head) with per-token
+    scales: k_scales / v_scales [num_blocks, Hk, bs] float, gathered through the
+    block table exactly like the codes."""
+    kc = gather_tokens(kv_cache[:, 0, kv_head], block_table[seq], L)
+    vc = gather_tokens(kv_cache[:, 1, kv_head], block_table[seq], L)
+    ks = gather_tokens(np.asarray(k_scales, dtype=np.float64)[:, kv_head], block_table[seq], L)
+    vs = gather_tokens(np.asarray(v_scales, dtype=np.float64)[:, kv_head], block_table[seq], L)
+    return decode_e4m3fn(kc) * ks[:, None], decode_e4m3fn(vc) * vs[:, None]
+
+
+def pa_decode_fp8_ext(q_bits, kv_cache, block_table, seq_lens, k_scale, v_scale,
+                      query_group: int, query_len: int, softmax_scale: float | None = None,
+                      units=None) -> np.ndarray:
+    """Decode of query_len new tokens per sequence ([PA] "per_token_kv" and MTP
+    query_length 1..4 commits): reference output [B, QL, Hq, D] (float64).
+
+    q_bits [B, QL, Hq, D] bf16 bits. Query position qoff of a sequence of
+    length L (L counts the QL new tokens) sees the tokens t <= L - QL + qoff
+    (causal inside the query block); a row that sees no token gives 0.
+    k_scale / v_scale are floats (per-tensor, as in ``pa_decode_fp8``) or
+    arrays [num_blocks, Hk, bs] (one scale per cached token and KV head)."""
+    q = decode_bf16(q_bits)
+    B, QL, Hq, D = q.shape
+    assert QL == query_len
+    Hk = kv_cache.shape[2]
+    assert Hq == Hk * query_group
+    per_token = np.ndim(k_scale) > 0
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    out = np.zeros((B, QL, Hq, D))
+    if units is None:
+        units = [(s, h) for s in range(B) for h in range(Hk)]
+    for s, h in units:
+        L = int(seq_lens[s])
+        if per_token:
+            k, v = dense_kv_fp8_per_token(kv_cache, block_table, s, h, L, k_scale, v_scale)
+        else:
+            k, v = dense_kv_fp8(kv_cache, block_table, s, h, L, k_scale, v_scale)
+        heads = slice(h * query_group, (h + 1) * query_group)
+        for qoff in range(QL):
+            n = max(0, L - QL + 1 + qoff)
+            out[s, qoff, heads] = attend(q[s, qoff, heads], k[:n], v[:n], softmax_scale)
+    return out
+
+
 # ----------------------------------------------------------------------------
 # split-KV partitions and their flash-combine
 # ----------------------------------------------------------------------------

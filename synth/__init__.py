@@ -187,6 +187,77 @@ def make_fp8_case(seed: int, seq_lens, num_kv_heads: int, query_group: int,
                    num_kv_heads, query_group, head_dim, block_size, float(softmax_scale))
 
 
+@dataclasses.dataclass
+class Fp8ExtCase:
+    q_bits: np.ndarray        # [B, QL, Hq, D] uint16 (bf16 bits)
+    kv_cache: np.ndarray      # [NB, 2, Hk, bs, D] uint8 (e4m3fn)
+    block_table: np.ndarray   # [B, max_blocks] int32 (unused entries -1)
+    seq_lens: np.ndarray      # [B] int32 (including the QL query tokens)
+    k_scale: object           # float, or [NB, Hk, bs] float32 per token
+    v_scale: object
+    num_kv_heads: int
+    query_group: int
+    query_len: int
+    head_dim: int
+    block_size: int
+    softmax_scale: float
+
+    @property
+    def num_seqs(self):
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def per_token(self):
+        return np.ndim(self.k_scale) > 0
+
+    @property
+    def kv_bytes(self):
+        """Cache bytes read: 2 x 128 code bytes per (token, KV head), plus the
+        two 4-byte scales per (token, KV head) with per-token scales."""
+        tok = int(np.sum(self.seq_lens.astype(np.int64)))
+        return tok * self.num_kv_heads * (2 * self.head_dim + (8 if self.per_token else 0))
+
+
+def make_fp8_ext_case(seed: int, seq_lens, num_kv_heads: int, query_group: int, query_len: int,
+                      per_token: bool, head_dim: int = 128, block_size: int = 16,
+                      max_blocks: int | None = None, poison: bool = True) -> Fp8ExtCase:
+    """As make_fp8_case with query_len query tokens per sequence. With
+    per_token, every (token, KV head) has its own K and V scale, drawn
+    log-uniform in [0.01, 0.2] and rounded to float32, and its codes are the
+    e4m3 of N(0,1) / scale."""
+    r = rng(seed)
+    base = make_fp8_case(seed, seq_lens, num_kv_heads, query_group, head_dim, block_size,
+                         max_blocks=max_blocks, poison=poison)
+    B = base.num_seqs
+    Hq = num_kv_heads * query_group
+    q = r.standard_normal((B, query_len, Hq, head_dim), dtype=np.float32)
+    q_bits = round_to_bf16_bits(q)
+    cache = base.kv_cache
+    if per_token:
+        NB = cache.shape[0]
+        ks = np.exp(r.uniform(np.log(0.01), np.log(0.2), size=(NB, num_kv_heads, block_size))).astype(np.float32)
+        vs = np.exp(r.uniform(np.log(0.01), np.log(0.2), size=(NB, num_kv_heads, block_size))).astype(np.float32)
+        cache = cache.copy()
+        cache[:, 0] = round_to_e4m3_bytes(
+            r.standard_normal(cache[:, 0].shape, dtype=np.float32) / ks[..., None])
+        cache[:, 1] = round_to_e4m3_bytes(
+            r.standard_normal(cache[:, 1].shape, dtype=np.float32) / vs[..., None])
+        if poison:
+            for s in range(B):
+                L = int(base.seq_lens[s])
+                nb = (L + block_size - 1) // block_size
+                if L % block_size and nb:
+                    blk = base.block_table[s, nb - 1]
+                    cache[blk, :, :, L % block_size:, :] = 0x7F
+                    ks[blk, :, L % block_size:] = np.nan
+                    vs[blk, :, L % block_size:] = np.nan
+        k_scale, v_scale = ks, vs
+    else:
+        k_scale, v_scale = base.k_scale, base.v_scale
+    return Fp8ExtCase(q_bits, cache, base.block_table, base.seq_lens, k_scale, v_scale,
+                      num_kv_heads, query_group, query_len, head_dim, block_size, base.softmax_scale)
+
+
 def fp8_tiny(seed: int = 1000) -> Fp8Case:
     """2 seqs (37, 200), 1 KV head, group 8, D 128, block 16, 32 blocks in a
     seeded random permutation."""

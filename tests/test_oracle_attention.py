@@ -177,3 +177,76 @@ def test_partition_map_is_strided_tile_groups():
     assert oracle.tile_groups_of_partition(16384, 31, 32) == [31, 63]
     assert oracle.tile_groups_of_partition(1024, 5, 32) == []
     assert oracle.tile_groups_of_partition(1025, 4, 32) == [4]
+
+
+# ---------------------------------------------------------------- multi-token queries, per-token scales
+def _ext(c):
+    return oracle.pa_decode_fp8_ext(c.q_bits, c.kv_cache, c.block_table, c.seq_lens, c.k_scale,
+                                    c.v_scale, c.query_group, c.query_len, c.softmax_scale)
+
+
+def test_ext_single_query_token_is_plain_decode():
+    c = synth.make_fp8_ext_case(31, [0, 1, 37, 300], 2, 4, 1, False)
+    ref = oracle.pa_decode_fp8(c.q_bits[:, 0], c.kv_cache, c.block_table, c.seq_lens, c.k_scale,
+                               c.v_scale, c.query_group, c.softmax_scale)
+    assert np.max(np.abs(_ext(c)[:, 0] - ref)) < 1e-12
+
+
+def test_ext_query_rows_are_prefix_decodes():
+    """Query position qoff of a length-L sequence decodes the prefix of
+    length L - QL + 1 + qoff: the plain decode on that shorter length."""
+    c = synth.make_fp8_ext_case(32, [2, 5, 40, 257], 2, 4, 3, False)
+    out = _ext(c)
+    for qoff in range(3):
+        lens = np.maximum(0, c.seq_lens - 3 + 1 + qoff).astype(np.int32)
+        ref = oracle.pa_decode_fp8(c.q_bits[:, qoff], c.kv_cache, c.block_table, lens, c.k_scale,
+                                   c.v_scale, c.query_group, c.softmax_scale)
+        assert np.max(np.abs(out[:, qoff] - ref)) < 1e-12
+    # the first row of the 2-token sequence sees nothing
+    assert np.all(out[0, 0] == 0.0)
+
+
+def test_ext_constant_per_token_scales_equal_per_tensor():
+    c = synth.make_fp8_ext_case(33, [1, 100, 333], 2, 8, 2, False, poison=False)
+    NB, Hk, bs = c.kv_cache.shape[0], c.num_kv_heads, c.block_size
+    ks = np.full((NB, Hk, bs), c.k_scale, dtype=np.float32)
+    vs = np.full((NB, Hk, bs), c.v_scale, dtype=np.float32)
+    per_token = oracle.pa_decode_fp8_ext(c.q_bits, c.kv_cache, c.block_table, c.seq_lens, ks, vs,
+                                         c.query_group, c.query_len, c.softmax_scale)
+    # (the per-tensor scalars rounded to float32 like the arrays)
+    per_tensor = oracle.pa_decode_fp8_ext(c.q_bits, c.kv_cache, c.block_table, c.seq_lens,
+                                          float(np.float32(c.k_scale)), float(np.float32(c.v_scale)),
+                                          c.query_group, c.query_len, c.softmax_scale)
+    assert np.max(np.abs(per_token - per_tensor)) < 1e-12
+
+
+def test_ext_per_token_brute_force():
+    """Scalar loops over a tiny case: every logit and output element written
+    out from the decoded bytes and each token's own scales."""
+    c = synth.make_fp8_ext_case(34, [5, 3], 1, 2, 2, True, head_dim=128, block_size=16)
+    out = _ext(c)
+    q = oracle.decode_bf16(c.q_bits)
+    kc = oracle.decode_e4m3fn(c.kv_cache[:, 0])
+    vc = oracle.decode_e4m3fn(c.kv_cache[:, 1])
+    bs = c.block_size
+    for s in range(c.num_seqs):
+        L = int(c.seq_lens[s])
+        for qoff in range(2):
+            n = L - 2 + 1 + qoff
+            for g in range(2):
+                logits = []
+                for t in range(n):
+                    blk, sl = int(c.block_table[s, t // bs]), t % bs
+                    dot = 0.0
+                    for d in range(128):
+                        dot += float(q[s, qoff, g, d]) * float(kc[blk, 0, sl, d]) * float(c.k_scale[blk, 0, sl])
+                    logits.append(dot * c.softmax_scale)
+                mx = max(logits)
+                w = [math.exp(x - mx) for x in logits]
+                den = sum(w)
+                for d in range(0, 128, 17):
+                    num = 0.0
+                    for t in range(n):
+                        blk, sl = int(c.block_table[s, t // bs]), t % bs
+                        num += w[t] * float(vc[blk, 0, sl, d]) * float(c.v_scale[blk, 0, sl])
+                    assert abs(out[s, qoff, g, d] - num / den) < 1e-12
