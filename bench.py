@@ -235,6 +235,45 @@ def time_fp8(c, P, steps, warmup, dev, sampler=None):
     return total / steps, part, total / steps - part, 2 * steps, clocks, total
 
 
+def time_fp8_ext(c, P, steps, warmup, dev):
+    """Times `steps` calls of pa_decode_fp8_ext (partition + combine) back to
+    back between two CUDA events (the cache, 537 MB, is larger than L2)."""
+    import numpy as np
+    import torch
+    import quantized_paged_attention_gb300 as qpa
+    q = torch.from_numpy(c.q_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    kv = torch.from_numpy(c.kv_cache).to(dev)
+    bt = torch.from_numpy(c.block_table).to(dev)
+    sl = torch.from_numpy(c.seq_lens).to(dev)
+    if c.per_token:
+        ks = torch.from_numpy(np.ascontiguousarray(c.k_scale)).to(dev)
+        vs = torch.from_numpy(np.ascontiguousarray(c.v_scale)).to(dev)
+    else:
+        ks = torch.tensor([c.k_scale], dtype=torch.float32, device=dev)
+        vs = torch.tensor([c.v_scale], dtype=torch.float32, device=dev)
+    desc = qpa.fp8_ext_desc(q, kv, bt, c.query_group, c.per_token, c.softmax_scale)
+    ws = qpa.alloc_workspace(qpa.pa_decode_fp8_ext_workspace_size(desc, P), dev)
+    out = torch.empty(tuple(q.shape), dtype=torch.float32, device=dev)
+
+    def step():
+        qpa.pa_decode_fp8_ext(q, kv, bt, sl, ks, vs, P, c.query_group, out=out, workspace=ws, desc=desc)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier()
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    _barrier()
+    if qpa.kernel_error() != 0:
+        raise RuntimeError("device error word raised during the benchmark")
+    return a.elapsed_time(b) / steps
+
+
 def _time_loop(step_a, step_b, steps, warmup):
     """Times `steps` steps (step_a = partition or whole kernel, step_b =
     combine or None) with L2 flushed before every step: a 256 MB buffer, larger
@@ -491,6 +530,19 @@ def main():
                 "l2": "flushed (256 MB write, then read) before every timed step", "kv_bytes": cu.kv_bytes, "gbs": round(cu.kv_bytes / (u_ms * 1e-3) / 1e9, 1),
                 "frac_of_peak": round(cu.kv_bytes / (u_ms * 1e-3) / 1e9 / peak, 4)}
             del cu
+        for name, ql, qg, pt in (("fp8_ext_b16_16k_ql4_qg4_per_token", 4, 4, True),
+                                 ("fp8_ext_b16_16k_ql2_qg8", 2, 8, False)):
+            ce = synth.fp8_ext_long(seed=1005 + rank, query_group=qg, query_len=ql, per_token=pt)
+            x_ms = _max_over_ranks(time_fp8_ext(ce, 32, esteps, a.warmup, dev))
+            extra[name] = {
+                "workload": f"fp8 decode of {ql} query tokens per sequence (causal inside the query block), "
+                            f"16 seqs x 16384 tokens, 8 KV heads, group {qg}, block 16, P=32, "
+                            + ("per-token K/V scales" if pt else "per-tensor K/V scales"),
+                "us_per_step": round(x_ms * 1e3, 2), "kv_bytes": ce.kv_bytes,
+                "gbs": round(ce.kv_bytes / (x_ms * 1e-3) / 1e9, 1),
+                "frac_of_peak": round(ce.kv_bytes / (x_ms * 1e-3) / 1e9 / peak, 4),
+                "l2": "no flush: the cache is larger than L2"}
+            del ce
         ci = synth.idx_full(seed=1004 + rank)
         i_ms, _ = time_idx(ci, esteps, a.warmup, dev)
         i_ms = _max_over_ranks(i_ms)

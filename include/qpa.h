@@ -134,6 +134,54 @@ int pa_decode_fp8_combine(int num_partitions, void* out, const qpa_fp8_desc* d,
                           const void* workspace, size_t workspace_bytes, void* stream);
 
 /* ========================================================================
+ * pa_decode_fp8_ext -- fp8 decode of query_len new tokens per sequence
+ * (multi-token prediction), with per-tensor or per-token K/V scales
+ * ([PA] "per_token_kv" quantisation mode and MTP query_length 1..4 commits).
+ *
+ * For sequence s (length L = seq_lens[s], counting the query_len new
+ * tokens), KV head h, query position qoff in [0, query_len) and group row g
+ * (query head h*query_group + g):
+ *     out = sum_t softmax_t(softmax_scale * q . k_t) v_t,
+ *           t = 0 .. L - query_len + qoff       (causal inside the query block;
+ *                                                a row with no token gives 0),
+ *     k_t = e4m3fn(K byte) * ks(t),  v_t = e4m3fn(V byte) * vs(t),
+ * with ks(t) = k_scale[0] (per-tensor) or the scale of token t's slot
+ * (per-token: k_scale[block][h][slot], block and slot of t as for the cache);
+ * likewise vs. The per-token layout is this library's reading; the page names
+ * the mode only.
+ *
+ * Layouts: as pa_decode_fp8, except
+ *   q         bf16 [num_seqs][query_len][num_kv_heads*query_group][128] with
+ *             strides base.q_stride_seq, q_stride_tok and base.q_stride_head
+ *             (elements, multiples of 8; 0 selects the contiguous value);
+ *   k_scale,  float [1] each (kv_scale_per_token = 0), or float
+ *   v_scale   [num_blocks][num_kv_heads][block_size] each, 16-byte aligned
+ *             (kv_scale_per_token = 1);
+ *   out       [num_seqs][query_len][num_kv_heads*query_group][128], float32
+ *             or bf16 per base.out_dtype, contiguous;
+ *   workspace pa_decode_fp8_ext_workspace_size() bytes: float32
+ *             O [num_seqs][num_kv_heads][P][query_len*query_group][128] and m,
+ *             l [num_seqs][num_kv_heads][P][query_len*query_group], row
+ *             qoff*query_group + g (as pa_decode_fp8; O includes the V scale).
+ * Supported: head_dim 128, block_size 16..256, query_len 1..4 with
+ * query_len * query_group <= 16. Errors as pa_decode_fp8; an unsupported
+ * query_len or row count is QPA_ERR_SHAPE.
+ * ====================================================================== */
+typedef struct qpa_fp8_ext_desc {
+  qpa_fp8_desc base;
+  int32_t query_len;            /* 0 or 1 = one query token */
+  int32_t kv_scale_per_token;   /* 0 = per-tensor, 1 = per-token */
+  int64_t q_stride_tok;         /* elements; 0 = num_kv_heads*query_group*head_dim */
+} qpa_fp8_ext_desc;
+
+size_t pa_decode_fp8_ext_workspace_size(const qpa_fp8_ext_desc* d, int num_partitions);
+
+int pa_decode_fp8_ext(const void* q, const uint8_t* kv_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, const float* k_scale, const float* v_scale,
+                      int num_partitions, void* out, const qpa_fp8_ext_desc* d, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* ========================================================================
  * UltraQuant head_dim=256 4-bit decode ([UQ] steps A..G)
  *
  * For every sequence s, KV head h and query row g (query head h*qg + g):

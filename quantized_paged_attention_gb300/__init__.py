@@ -38,6 +38,11 @@ class Fp8Desc(ctypes.Structure):
                 ("softmax_scale", ctypes.c_float)]
 
 
+class Fp8ExtDesc(ctypes.Structure):
+    _fields_ = [("base", Fp8Desc), ("query_len", ctypes.c_int32), ("kv_scale_per_token", ctypes.c_int32),
+                ("q_stride_tok", ctypes.c_int64)]
+
+
 class UqDesc(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("query_group", ctypes.c_int32), ("head_dim", ctypes.c_int32),
@@ -72,6 +77,9 @@ _SIGS = {
                                              ctypes.c_size_t, _P]),
     "pa_decode_fp8_static": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, _P,
                                             ctypes.POINTER(Fp8Desc), _P]),
+    "pa_decode_fp8_ext_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Fp8ExtDesc), ctypes.c_int]),
+    "pa_decode_fp8_ext": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, _P,
+                                         ctypes.POINTER(Fp8ExtDesc), _P, ctypes.c_size_t, _P]),
     "uq_decode_hd256_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(UqDesc), ctypes.c_int]),
     "uq_decode_hd256": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.POINTER(UqDesc), _P,
                                        ctypes.c_size_t, _P]),
@@ -189,6 +197,54 @@ def pa_decode_fp8_combine(num_partitions, out, desc, workspace, stream=None):
     st = load_library().pa_decode_fp8_combine(num_partitions, _ptr(out), ctypes.byref(desc),
                                               _ptr(workspace), workspace.numel(), _stream(stream))
     _check("pa_decode_fp8_combine", st)
+
+
+def fp8_ext_desc(q, kv_cache, block_table, query_group, per_token, softmax_scale=None,
+                 out_dtype=torch.float32):
+    """Descriptor of pa_decode_fp8_ext for q bf16 [B, QL, Hq, 128]."""
+    B, QL, Hq, D = q.shape
+    NB, two, Hk, bs, D2 = kv_cache.shape
+    assert two == 2 and D2 == D and Hq == Hk * query_group
+    if q.stride(3) != 1:
+        raise ValueError("q must be contiguous along head_dim")
+    d = Fp8ExtDesc()
+    b = d.base
+    b.num_seqs, b.num_kv_heads, b.query_group, b.head_dim = B, Hk, query_group, D
+    b.block_size, b.num_blocks, b.max_blocks_per_seq = bs, NB, block_table.shape[1]
+    b.out_dtype = QPA_OUT_BF16 if out_dtype == torch.bfloat16 else QPA_OUT_F32
+    b.q_stride_seq, b.q_stride_head = q.stride(0), q.stride(2)
+    b.softmax_scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    d.query_len = QL
+    d.kv_scale_per_token = 1 if per_token else 0
+    d.q_stride_tok = q.stride(1)
+    return d
+
+
+def pa_decode_fp8_ext_workspace_size(desc: Fp8ExtDesc, num_partitions: int) -> int:
+    return int(load_library().pa_decode_fp8_ext_workspace_size(ctypes.byref(desc), num_partitions))
+
+
+def pa_decode_fp8_ext(q, kv_cache, block_table, seq_lens, k_scale, v_scale, num_partitions: int,
+                      query_group: int, out=None, workspace=None, softmax_scale=None,
+                      out_dtype=torch.float32, stream=None, desc=None):
+    """fp8 decode of QL query tokens per sequence. q bf16 [B, QL, Hq, 128];
+    k_scale / v_scale float32 [1] (per-tensor) or [NB, Hk, bs] (per-token) on
+    the device. Returns out [B, QL, Hq, 128]."""
+    lib = load_library()
+    _need_cuda(q, kv_cache, block_table, seq_lens, k_scale, v_scale)
+    per_token = k_scale.numel() > 1 or k_scale.dim() == 3
+    if desc is None:
+        desc = fp8_ext_desc(q, kv_cache, block_table, query_group, per_token, softmax_scale, out_dtype)
+    if out is None:
+        odt = torch.bfloat16 if desc.base.out_dtype == QPA_OUT_BF16 else torch.float32
+        out = torch.empty(tuple(q.shape), dtype=odt, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(pa_decode_fp8_ext_workspace_size(desc, num_partitions), q.device)
+    st = lib.pa_decode_fp8_ext(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), _ptr(k_scale),
+                               _ptr(v_scale), num_partitions, _ptr(out), ctypes.byref(desc),
+                               _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("pa_decode_fp8_ext", st)
+    return out
 
 
 def fp8_workspace_views(workspace, desc: Fp8Desc, num_partitions: int):

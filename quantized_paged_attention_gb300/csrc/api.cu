@@ -69,6 +69,23 @@ int fp8_check(const void* q, const uint8_t* kv, const int32_t* bt, const int32_t
   return QPA_OK;
 }
 
+// ------------------------------------------------------------------ fp8, extended
+int fp8x_query_len(const qpa_fp8_ext_desc* d) { return d->query_len > 1 ? d->query_len : 1; }
+
+bool fp8x_shape_ok(const qpa_fp8_ext_desc* d) {
+  if (!fp8_shape_ok(&d->base)) return false;
+  if (d->query_len < 0 || d->query_len > 4) return false;
+  if (fp8x_query_len(d) * d->base.query_group > 16) return false;
+  if (d->kv_scale_per_token != 0 && d->kv_scale_per_token != 1) return false;
+  return true;
+}
+
+Fp8Layout fp8x_layout(const qpa_fp8_ext_desc* d, int P) {
+  qpa_fp8_desc rows = d->base;
+  rows.query_group = d->base.query_group * fp8x_query_len(d);   // partial rows per (seq, head, partition)
+  return fp8_layout(&rows, P);
+}
+
 // ------------------------------------------------------------------ uq hd256
 bool uq_shape_ok(const qpa_uq_desc* d) {
   if (d->num_seqs < 0 || d->num_kv_heads < 1 || d->query_group < 1 || d->query_group > 8) return false;
@@ -236,6 +253,80 @@ int pa_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t* block_t
                                workspace, workspace_bytes, stream);
   if (st != QPA_OK) return st;
   return pa_decode_fp8_combine(num_partitions, out, d, workspace, workspace_bytes, stream);
+}
+
+size_t pa_decode_fp8_ext_workspace_size(const qpa_fp8_ext_desc* d, int num_partitions) {
+  if (!d || num_partitions < 1 || !fp8x_shape_ok(d)) return 0;
+  return fp8x_layout(d, num_partitions).total;
+}
+
+int pa_decode_fp8_ext(const void* q, const uint8_t* kv_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, const float* k_scale, const float* v_scale,
+                      int num_partitions, void* out, const qpa_fp8_ext_desc* d, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!d) return QPA_ERR_NULL;
+  if (!fp8x_shape_ok(d)) return QPA_ERR_SHAPE;
+  const qpa_fp8_desc* b = &d->base;
+  const int QL = fp8x_query_len(d);
+  if (num_partitions < 1) return QPA_ERR_PARTITIONS;
+  if ((long long)b->num_seqs * b->num_kv_heads * num_partitions * b->query_group * QL > 0x7fffffffLL)
+    return QPA_ERR_SHAPE;
+  if (b->num_seqs == 0) return QPA_OK;
+  if (!q || !kv_cache || !block_table || !seq_lens || !k_scale || !v_scale || !workspace || !out)
+    return QPA_ERR_NULL;
+  const long long hq = (long long)b->num_kv_heads * b->query_group;
+  const long long sh = b->q_stride_head ? b->q_stride_head : b->head_dim;
+  const long long st = d->q_stride_tok ? d->q_stride_tok : hq * b->head_dim;
+  const long long ss = b->q_stride_seq ? b->q_stride_seq : QL * hq * b->head_dim;
+  if (sh < 0 || st < 0 || ss < 0 || (sh % 8) || (st % 8) || (ss % 8)) return QPA_ERR_ALIGN;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(workspace, 256) || !aligned(out, 16))
+    return QPA_ERR_ALIGN;
+  if (d->kv_scale_per_token && (!aligned(k_scale, 16) || !aligned(v_scale, 16))) return QPA_ERR_ALIGN;
+  const Fp8Layout L = fp8x_layout(d, num_partitions);
+  if (workspace_bytes < L.total) return QPA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Fp8ExtLaunch a;
+  a.q = q;
+  a.kv = kv_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.part_o = reinterpret_cast<float*>(ws + L.o_off);
+  a.part_m = reinterpret_cast<float*>(ws + L.m_off);
+  a.part_l = reinterpret_cast<float*>(ws + L.l_off);
+  a.q_stride_seq = ss;
+  a.q_stride_tok = st;
+  a.q_stride_head = sh;
+  a.num_seqs = b->num_seqs;
+  a.num_kv_heads = b->num_kv_heads;
+  a.qg = b->query_group;
+  a.query_len = QL;
+  a.per_token = d->kv_scale_per_token;
+  a.block_size = b->block_size;
+  a.num_blocks = b->num_blocks;
+  a.max_blocks = b->max_blocks_per_seq;
+  a.num_partitions = num_partitions;
+  a.softmax_scale = b->softmax_scale != 0.f ? b->softmax_scale : 1.0f / std::sqrt((float)b->head_dim);
+  a.num_sms = num_sms_current();
+  if (a.num_sms <= 0) return QPA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_fp8x_partition(a, s) != cudaSuccess) return QPA_ERR_CUDA;
+  Fp8ExtCombineLaunch c;
+  c.part_o = a.part_o;
+  c.part_m = a.part_m;
+  c.part_l = a.part_l;
+  c.out = out;
+  c.out_bf16 = b->out_dtype == QPA_OUT_BF16;
+  c.num_seqs = b->num_seqs;
+  c.num_kv_heads = b->num_kv_heads;
+  c.qg = b->query_group;
+  c.query_len = QL;
+  c.num_partitions = num_partitions;
+  c.out_stride_head = b->head_dim;
+  c.out_stride_tok = hq * b->head_dim;
+  c.out_stride_seq = QL * hq * b->head_dim;
+  return launch_fp8x_combine(c, s) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;
 }
 
 size_t uq_decode_hd256_workspace_size(const qpa_uq_desc* d, int num_partitions) {

@@ -24,6 +24,32 @@ struct Fp8Launch {
   int num_sms;
 };
 
+struct Fp8ExtLaunch {
+  const void* q;
+  const uint8_t* kv;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const float* k_scale;
+  const float* v_scale;
+  float* part_o;
+  float* part_m;
+  float* part_l;
+  long long q_stride_seq, q_stride_tok, q_stride_head;
+  int num_seqs, num_kv_heads, qg, query_len, per_token, block_size, num_blocks, max_blocks, num_partitions;
+  float softmax_scale;
+  int num_sms;
+};
+
+struct Fp8ExtCombineLaunch {
+  const float* part_o;
+  const float* part_m;
+  const float* part_l;
+  void* out;
+  int out_bf16;
+  int num_seqs, num_kv_heads, qg, query_len, num_partitions;
+  long long out_stride_seq, out_stride_tok, out_stride_head;
+};
+
 struct CombineLaunch {
   const float* part_o;
   const float* part_m;
@@ -74,6 +100,8 @@ __device__ __forceinline__ void store4(__nv_bfloat16* dst, float a, float b, flo
 
 cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t stream);
+cudaError_t launch_fp8x_partition(const Fp8ExtLaunch& a, cudaStream_t stream);
+cudaError_t launch_fp8x_combine(const Fp8ExtCombineLaunch& a, cudaStream_t stream);
 cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream);
 int uq_warps_per_item(long long items, int max_blocks, int block_size, int num_partitions, int num_sms);
 cudaError_t launch_uq_combine(const CombineLaunch& a, cudaStream_t stream);

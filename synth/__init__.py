@@ -258,6 +258,28 @@ def make_fp8_ext_case(seed: int, seq_lens, num_kv_heads: int, query_group: int, 
                       num_kv_heads, query_group, query_len, head_dim, block_size, base.softmax_scale)
 
 
+def fp8_ext_long(seed: int = 1005, batch: int = 16, seq_len: int = 16384, query_group: int = 4,
+                 query_len: int = 4, per_token: bool = True) -> Fp8ExtCase:
+    """Throughput workload of the multi-token decode: 16 seqs x 16384 tokens, 8
+    KV heads, group 4, 4 query tokens. The codes are the per-tensor draw of
+    fp8_gqa (e4m3 of N(0,1)/0.05 and N(0,1)/0.04); with per_token, the K and V
+    scales of every (token, head) are drawn log-uniform in [0.01, 0.2]
+    independently of the codes (a throughput input, not a quantisation of a
+    common logical cache)."""
+    r = rng(seed)
+    base = make_fp8_case(seed, [seq_len] * batch, 8, query_group, 128, 16, poison=False)
+    Hq = 8 * query_group
+    q_bits = round_to_bf16_bits(r.standard_normal((batch, query_len, Hq, 128), dtype=np.float32))
+    if per_token:
+        NB = base.kv_cache.shape[0]
+        ks = np.exp(r.uniform(np.log(0.01), np.log(0.2), size=(NB, 8, 16))).astype(np.float32)
+        vs = np.exp(r.uniform(np.log(0.01), np.log(0.2), size=(NB, 8, 16))).astype(np.float32)
+    else:
+        ks, vs = base.k_scale, base.v_scale
+    return Fp8ExtCase(q_bits, base.kv_cache, base.block_table, base.seq_lens, ks, vs, 8, query_group,
+                      query_len, 128, 16, base.softmax_scale)
+
+
 def fp8_tiny(seed: int = 1000) -> Fp8Case:
     """2 seqs (37, 200), 1 KV head, group 8, D 128, block 16, 32 blocks in a
     seeded random permutation."""

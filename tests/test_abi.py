@@ -77,3 +77,37 @@ def test_workspace_size(lib):
     rows = 2 * 1 * 2 * 8
     assert n >= rows * 130 * 4 and n % 256 == 0
     assert lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc(head_dim=64)), 2) == 0
+
+
+def _ext_desc(query_len=2, per_token=1, **kw):
+    import quantized_paged_attention_gb300 as qpa
+    d = qpa.Fp8ExtDesc()
+    d.base = _desc(**kw)
+    d.query_len = query_len
+    d.kv_scale_per_token = per_token
+    return d
+
+
+def _call_ext(lib, d, P=2, ws_bytes=1 << 20, ks=FAKE):
+    return lib.pa_decode_fp8_ext(FAKE, FAKE, FAKE, FAKE, ks, FAKE, P, FAKE, ctypes.byref(d), FAKE, ws_bytes, None)
+
+
+def test_ext_host_validation(lib):
+    assert _call_ext(lib, _ext_desc(), P=0) == -5
+    assert _call_ext(lib, _ext_desc(query_len=5)) == -2
+    assert _call_ext(lib, _ext_desc(query_len=4, query_group=8)) == -2      # 32 rows
+    assert _call_ext(lib, _ext_desc(query_len=4, query_group=4), ws_bytes=16) == -4
+    assert _call_ext(lib, _ext_desc(per_token=2)) == -2
+    assert _call_ext(lib, _ext_desc(), ks=ctypes.c_void_p(0x100004)) == -3    # per-token scales need 16 B
+    assert _call_ext(lib, _ext_desc(per_token=0), ks=ctypes.c_void_p(0x100004), ws_bytes=16) == -4
+    assert _call_ext(lib, _ext_desc(), ks=ctypes.c_void_p(0)) == -1
+
+
+def test_ext_workspace_size(lib):
+    n = lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=2, query_group=8)), 3)
+    rows = 2 * 1 * 3 * 16
+    assert n >= rows * 130 * 4 and n % 256 == 0
+    assert lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=3, query_group=8)), 3) == 0
+    # query_len 0 means one query token
+    one = lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=0)), 2)
+    assert one == lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc()), 2)
