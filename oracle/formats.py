@@ -12,7 +12,11 @@ TEST INFRASTRUCTURE (see the package header).
 * UE8M0: the byte b is the power 2^(b-127); [UQ] STEP F decodes b=0 to +0.
 * bf16: the upper 16 bits of an IEEE binary32.
 
-Pins: all 256 e4m3 codes against torch's float8_e4m3fn; all 16 e2m1 codes
+Encoder: ``round_e4m3`` rounds to the nearest e4m3fn value, ties to the
+even code, saturating at +-448.
+
+Pins: all 256 e4m3 codes against torch's float8_e4m3fn (and the encoder
+against torch's round-to-nearest-even cast, its fixed points and ties); all 16 e2m1 codes
 against the OCP value table in tests/golden; bf16 against torch.bfloat16;
 UE8M0 against powers of two and the zero sentinel.
 """
@@ -29,6 +33,23 @@ def decode_e4m3fn(codes) -> np.ndarray:
                    (1.0 + man / 8.0) * np.exp2(exp.astype(np.float64) - 7.0))
     mag = np.where((exp == 0xF) & (man == 0x7), np.nan, mag)
     return np.where(sign == 1, -mag, mag)
+
+
+def round_e4m3(x) -> np.ndarray:
+    """Values -> nearest e4m3fn value (round to nearest, ties to the even
+    code), saturating to +-448; NaN stays NaN. Used for the [UQ] STEP B'
+    query haircut (cvt_pk_fp8_f32 of q_r / sqrt(D))."""
+    x = np.asarray(x, dtype=np.float64)
+    vals = decode_e4m3fn(np.arange(256, dtype=np.uint8))
+    pos = np.arange(0, 0x7F)                       # codes 0x00..0x7E: 0 .. 448, increasing
+    grid = vals[pos]
+    a = np.minimum(np.abs(x), 448.0)
+    i = np.clip(np.searchsorted(grid, a), 1, len(grid) - 1)   # grid[i-1] <= a <= grid[i] (a > 0)
+    lo, hi = grid[i - 1], grid[i]
+    pick_hi = (a - lo > hi - a) | ((a - lo == hi - a) & ((pos[i] & 1) == 0))
+    mag = np.where(a == 0, 0.0, np.where(pick_hi, hi, lo))
+    out = np.where(np.signbit(x), -mag, mag)
+    return np.where(np.isnan(x), np.nan, out)
 
 
 def decode_e2m1(nibbles) -> np.ndarray:

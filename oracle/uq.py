@@ -23,20 +23,30 @@ the same R, attention runs in the rotated domain with scale 1/sqrt(256)
 (the builder's default softmax scale), and the output is rotated back:
 o = softmax(scale q_r K_r^T) V_r R.
 
+Query haircut ([UQ] STEP B' "1/sqrt(D) normalization + E4M3 haircut"), the
+``q_haircut`` option: q_h = e4m3(scale * q_r), rounded to nearest even and
+saturating at +-448, and the logits are q_h K_r^T with no further scale. The
+rotation feeding this rounding is computed in float32 by butterfly stages of
+strides 1, 2, ..., 128 (``rotate_q_fp32``), so that the rounding decision is
+taken on the same float32 value as in the kernel.
+
 Pins (tests/test_oracle_uq.py): R R^T = I, R = R^T, R R = I, the +-1 entries
 against the recursive Sylvester construction, a fast butterfly transform
 against R to within the fp32 difference the page reports (1.8e-6); a
 hand-built slot against its expected dequantised vector (tests/golden); the
 page's 81.6 MB slot byte count at B=4, seq 75k, one KV head; the whole
 rotated pipeline against plain attention on the logical K = K_r R,
-V = V_r R.
+V = V_r R (e4m3 and UE8M0 scales). The float32 rotation exactly against
+x H on integer inputs and within the page's fp32 bound on random ones; the
+haircut as the identity on queries whose scaled rotation is already e4m3, and
+against torch's e4m3 cast plus a written-out softmax.
 """
 import math
 
 import numpy as np
 
 from .attention import attend, gather_tokens
-from .formats import decode_bf16, decode_e2m1, decode_e4m3fn, decode_ue8m0, unpack_nibbles
+from .formats import decode_bf16, decode_e2m1, decode_e4m3fn, decode_ue8m0, round_e4m3, unpack_nibbles
 
 HEAD = 256
 K_CODES, K_SCALES, V_CODES, V_SCALES, CONTENT = 0, 128, 136, 264, 272
@@ -54,6 +64,23 @@ def wht_matrix(n: int = HEAD) -> np.ndarray:
         parity ^= x & 1
         x = x >> 1
     return np.where(parity == 1, -1.0, 1.0) / math.sqrt(n)
+
+
+def rotate_q_fp32(q: np.ndarray) -> np.ndarray:
+    """q [..., 256] -> q H in float32 by butterfly stages of strides 1, 2, ...,
+    128 (x, y) -> (x + y, x - y), i.e. 16 q R rounded as the kernel computes
+    it. Only the query haircut uses it: there the e4m3 rounding decision has to
+    be taken on the same float32 value the kernel rounds."""
+    v = np.asarray(q, dtype=np.float32).copy()
+    st = 1
+    while st < HEAD:
+        v = v.reshape(v.shape[:-1] + (HEAD // (2 * st), 2, st))
+        x, y = v[..., 0, :].copy(), v[..., 1, :].copy()
+        v[..., 0, :] = x + y
+        v[..., 1, :] = x - y
+        v = v.reshape(v.shape[:-3] + (HEAD,))
+        st *= 2
+    return v
 
 
 def decode_uq_slots(slots: np.ndarray, centroids, scale_format: str = "e4m3"):
@@ -75,11 +102,14 @@ def dense_kv_uq(kv_cache, centroids, block_table, seq, kv_head, L, scale_format=
 
 def uq_decode_hd256(q_bits, kv_cache, centroids, block_table, seq_lens, query_group: int,
                     softmax_scale: float | None = None, units=None,
-                    scale_format: str = "e4m3") -> np.ndarray:
+                    scale_format: str = "e4m3", q_haircut: bool = False) -> np.ndarray:
     """Reference output [B, Hq, 256] in the un-rotated (logical) domain.
 
     q_bits [B, Hq, 256] uint16 bf16 bits (un-rotated); kv_cache [NB, bs, Hk,
-    padded_slot] uint8; centroids [16] float32."""
+    padded_slot] uint8; centroids [16] float32. With q_haircut ([UQ] STEP B'
+    "1/sqrt(D) normalization + E4M3 haircut"), the rotated query times the
+    softmax scale is rounded to e4m3 (float32 rotation, as the kernel) and the
+    logits are that rounded query times K_r, with no further scale."""
     q = decode_bf16(q_bits)
     B, Hq, D = q.shape
     assert D == HEAD
@@ -95,7 +125,13 @@ def uq_decode_hd256(q_bits, kv_cache, centroids, block_table, seq_lens, query_gr
         L = int(seq_lens[s])
         k_r, v_r = dense_kv_uq(kv_cache, centroids, block_table, s, h, L, scale_format)
         rows = slice(h * query_group, (h + 1) * query_group)
-        q_r = q[s, rows] @ R
-        o_r = attend(q_r, k_r, v_r, softmax_scale)
+        if q_haircut:
+            q16 = rotate_q_fp32(q[s, rows])                                    # 16 q R in float32
+            qs = (q16 * np.float32(0.0625)) * np.float32(softmax_scale)         # float32 products
+            q_h = round_e4m3(qs.astype(np.float64))
+            o_r = attend(q_h, k_r, v_r, 1.0)
+        else:
+            q_r = q[s, rows] @ R
+            o_r = attend(q_r, k_r, v_r, softmax_scale)
         out[s, rows] = o_r @ R
     return out

@@ -94,6 +94,20 @@ def group_scales_e4m3(x: np.ndarray, group: int, qmax: float) -> np.ndarray:
     return s
 
 
+# UE8M0 scale bytes the generators emit: 2^-23 .. 2^13, the powers of two for
+# which every e2m1 code times the scale is an exact f16 value.
+UE8M0_MIN_BYTE, UE8M0_MAX_BYTE = 104, 140
+
+
+def group_scales_ue8m0(x: np.ndarray, group: int, qmax: float) -> np.ndarray:
+    """Per-group UE8M0 scale bytes for x[..., D]: the smallest power of two
+    2^(byte-127) with absmax / 2^(byte-127) <= qmax, clipped to the window."""
+    shp = x.shape[:-1] + (x.shape[-1] // group, group)
+    amax = np.abs(x.reshape(shp)).max(axis=-1).astype(np.float64)
+    e = np.ceil(np.log2(np.maximum(amax / qmax, 2.0 ** -30)))
+    return np.clip(127 + e, UE8M0_MIN_BYTE, UE8M0_MAX_BYTE).astype(np.uint8)
+
+
 def e2m1_table() -> np.ndarray:
     """16-entry e2m1 value table in code order (a centroid table choice)."""
     return np.concatenate([_E2M1_POS, -_E2M1_POS]).astype(np.float32)
@@ -323,6 +337,7 @@ class UqCase:
     block_size: int
     padded_slot: int
     softmax_scale: float
+    scale_format: str = "e4m3"   # group scale bytes: "e4m3" (e4m3fn) or "ue8m0" (2^(b-127))
 
     @property
     def num_seqs(self):
@@ -346,7 +361,10 @@ def sylvester_pm1(n: int) -> np.ndarray:
 def make_uq_case(seed: int, seq_lens, num_kv_heads: int = 2, query_group: int = 8,
                  block_size: int = 64, padded_slot: int = 288, centroids=None,
                  num_blocks: int | None = None, softmax_scale: float | None = None,
-                 poison: bool = True, chunk_tokens: int = 1 << 15) -> UqCase:
+                 poison: bool = True, chunk_tokens: int = 1 << 15,
+                 scale_format: str = "e4m3") -> UqCase:
+    if scale_format not in ("e4m3", "ue8m0"):
+        raise ValueError(scale_format)
     r = rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     B = seq_lens.shape[0]
@@ -367,10 +385,16 @@ def make_uq_case(seed: int, seq_lens, num_kv_heads: int = 2, query_group: int = 
         n = min(chunk_tokens, ntok - o)
         kl = r.standard_normal((n, UQ_D), dtype=np.float32) @ rot
         vl = r.standard_normal((n, UQ_D), dtype=np.float32) @ rot
-        ks = group_scales_e4m3(kl, 32, 6.0)
-        vs = group_scales_e4m3(vl, 32, cmax)
-        ksf = np.repeat(e4m3_bytes_to_float(ks), 32, axis=1)
-        vsf = np.repeat(e4m3_bytes_to_float(vs), 32, axis=1)
+        if scale_format == "e4m3":
+            ks = group_scales_e4m3(kl, 32, 6.0)
+            vs = group_scales_e4m3(vl, 32, cmax)
+            ksf = np.repeat(e4m3_bytes_to_float(ks), 32, axis=1)
+            vsf = np.repeat(e4m3_bytes_to_float(vs), 32, axis=1)
+        else:
+            ks = group_scales_ue8m0(kl, 32, 6.0)
+            vs = group_scales_ue8m0(vl, 32, cmax)
+            ksf = np.repeat(np.ldexp(1.0, ks.astype(np.int32) - 127), 32, axis=1)
+            vsf = np.repeat(np.ldexp(1.0, vs.astype(np.int32) - 127), 32, axis=1)
         cache[o:o + n, 0:128] = pack_nibbles(round_to_e2m1_codes(kl / ksf))
         cache[o:o + n, 128:136] = ks
         cache[o:o + n, 136:264] = pack_nibbles(round_to_centroid_codes(vl / vsf, centroids))
@@ -385,13 +409,14 @@ def make_uq_case(seed: int, seq_lens, num_kv_heads: int = 2, query_group: int = 
             L = int(seq_lens[s])
             if L % block_size and nblk[s]:
                 blk = bt[s, nblk[s] - 1]
-                # NaN scale bytes and random codes past the end of the sequence.
-                cache[blk, L % block_size:, :, 128:136] = 0x7F
+                # NaN (e4m3) / 2^128 (ue8m0) scale bytes and random codes past
+                # the end of the sequence.
+                cache[blk, L % block_size:, :, 128:136] = 0x7F if scale_format == "e4m3" else 0xFF
                 cache[blk, L % block_size:, :, 264:272] = 0xFF
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(UQ_D)
     return UqCase(q_bits, cache, centroids, bt, seq_lens, num_kv_heads, query_group,
-                  block_size, padded_slot, float(softmax_scale))
+                  block_size, padded_slot, float(softmax_scale), scale_format)
 
 
 def sorted_random_centroids(seed: int) -> np.ndarray:

@@ -73,3 +73,30 @@ def test_ue8m0_powers_and_sentinel():
 def test_nibble_order():
     from oracle.formats import unpack_nibbles
     assert unpack_nibbles(np.array([0x21, 0xF0], dtype=np.uint8)).tolist() == [1, 2, 0, 15]
+
+
+def test_round_e4m3_against_torch_cast():
+    # torch's float32 -> float8_e4m3fn cast rounds to nearest even; it has no
+    # saturation, so the values are clipped to +-448 first.
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(50000) * 40, rng.standard_normal(20000) * 0.01,
+                        rng.uniform(-600, 600, 5000)]).astype(np.float32)
+    got = oracle.round_e4m3(x)
+    ref = torch.from_numpy(np.clip(x, -448, 448)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_round_e4m3_fixed_points_ties_saturation():
+    vals = oracle.decode_e4m3fn(np.arange(256, dtype=np.uint8))
+    fin = ~np.isnan(vals)
+    assert np.array_equal(oracle.round_e4m3(vals[fin]), vals[fin])          # every code is a fixed point
+    # halfway cases of the e4m3fn grid go to the even code
+    cases = [(1.0625, 1.0),            # between 1.0 (0x38) and 1.125 (0x39)
+             (1.1875, 1.25),           # between 1.125 (0x39) and 1.25 (0x3A)
+             (2.0 ** -10, 0.0),        # between 0 and the smallest subnormal 2^-9
+             (3 * 2.0 ** -10, 2.0 ** -8),
+             (240.0, 240.0), (232.0, 224.0), (248.0, 256.0),
+             (-1.0625, -1.0), (460.0, 448.0), (1e9, 448.0), (-1e9, -448.0)]
+    for x, want in cases:
+        assert float(oracle.round_e4m3(x)) == want, x
+    assert np.isnan(oracle.round_e4m3(np.nan))

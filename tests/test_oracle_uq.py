@@ -4,6 +4,7 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import synth
@@ -138,3 +139,96 @@ def test_ue8m0_variant_is_powers_of_two():
     slot[128] = 127 + 3                # K scale 2^3 for dims 0..31
     K, _ = decode_uq_slots(slot, synth.e2m1_table(), scale_format="ue8m0")
     assert K[0] == 8.0 and K[1] == 8.0 and np.all(K[2:] == 0)
+
+
+def test_rotate_q_fp32_exact_on_small_integers():
+    # integer inputs keep every butterfly sum exact in float32, so the result
+    # is exactly x H with the Sylvester matrix built here by recursion
+    h = np.array([[1.0]])
+    while h.shape[0] < 256:
+        h = np.block([[h, h], [h, -h]])
+    x = np.random.default_rng(4).integers(-50, 51, size=(5, 256)).astype(np.float32)
+    assert np.array_equal(oracle.rotate_q_fp32(x).astype(np.float64), x.astype(np.float64) @ h)
+
+
+def test_rotate_q_fp32_within_page_bound(golden_dir):
+    x = np.random.default_rng(6).standard_normal((64, 256)).astype(np.float32)
+    y = oracle.rotate_q_fp32(x).astype(np.float64) / 16.0
+    ref = x.astype(np.float64) @ oracle.wht_matrix(256)
+    assert np.max(np.abs(y - ref)) <= _facts(golden_dir)["wht_butterfly_vs_matmul_fp32_max_abs"]
+
+
+def _bf16_bits(x):
+    return synth.round_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def test_haircut_is_identity_on_e4m3_exact_rotated_queries():
+    # q = (a e_i + b e_j) R has entries +-(a +- b)/16: with a/16, b/16 on the
+    # e4m3 grid and few mantissa bits the query is exact in bf16, its rotation
+    # is exactly 16 (a e_i + b e_j), and q_r / 16 is already e4m3, so the
+    # haircut changes nothing and the logits keep the single softmax scale.
+    c = synth.make_uq_case(31, [40, 7], 1, 2, 64, 288)
+    R = oracle.wht_matrix(256)
+    q = np.zeros((2, 2, 256))
+    for s in range(2):
+        for g in range(2):
+            e = np.zeros(256)
+            e[3 + 17 * g + s] = 5.0 * (1 + g)       # q_r entries 5 or 10 and -3: 5/16, 10/16, -3/16 are e4m3
+            e[200 - g] = -3.0
+            q[s, g] = e @ R
+    qb = _bf16_bits(q)
+    assert np.array_equal(oracle.decode_bf16(qb), q)
+    a = oracle.uq_decode_hd256(qb, c.kv_cache, c.centroids, c.block_table, c.seq_lens, 2, 1 / 16)
+    b = oracle.uq_decode_hd256(qb, c.kv_cache, c.centroids, c.block_table, c.seq_lens, 2, 1 / 16,
+                               q_haircut=True)
+    assert np.max(np.abs(a - b)) < 1e-13
+
+
+def test_haircut_against_torch_cast_and_softmax():
+    # The haircut query built another way (float64 matrix rotation, torch's
+    # e4m3 cast), then softmax attention written out over the decoded tokens.
+    c = synth.make_uq_case(33, [90, 5], 2, 4, 64, 288)
+    sc = 1 / 16
+    out = oracle.uq_decode_hd256(c.q_bits, c.kv_cache, c.centroids, c.block_table, c.seq_lens, 4, sc,
+                                 q_haircut=True)
+    R = oracle.wht_matrix(256)
+    q = oracle.decode_bf16(c.q_bits)
+    for s in range(2):
+        for h in range(2):
+            rows = slice(4 * h, 4 * h + 4)
+            qr = (q[s, rows] @ R * sc).astype(np.float32)
+            qh = torch.from_numpy(np.clip(qr, -448, 448)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+            k_r, v_r = dense_kv_uq(c.kv_cache, c.centroids, c.block_table, s, h, int(c.seq_lens[s]))
+            logits = qh @ k_r.T
+            w = np.exp(logits - logits.max(axis=1, keepdims=True))
+            ref = (w / w.sum(axis=1, keepdims=True)) @ v_r @ R
+            assert np.max(np.abs(out[s, rows] - ref)) < 1e-11
+    plain = oracle.uq_decode_hd256(c.q_bits, c.kv_cache, c.centroids, c.block_table, c.seq_lens, 4, sc)
+    assert np.max(np.abs(out - plain)) > 1e-2          # the haircut is visible at this size
+
+
+@pytest.mark.parametrize("QG", [8, 3])
+def test_ue8m0_case_pipeline_equals_logical_attention(QG):
+    c = synth.make_uq_case(35, [130, 64, 1], 2, QG, 64, 288, scale_format="ue8m0")
+    slots = c.kv_cache.reshape(-1, 288)
+    for off in (128, 264):
+        sb = slots[:, off:off + 8]
+        live = sb[sb != 0xFF]
+        assert live.min() >= synth.UE8M0_MIN_BYTE and live.max() <= synth.UE8M0_MAX_BYTE
+    out = oracle.uq_decode_hd256(c.q_bits, c.kv_cache, c.centroids, c.block_table, c.seq_lens,
+                                 QG, c.softmax_scale, scale_format="ue8m0")
+    assert np.all(np.isfinite(out))
+    R = oracle.wht_matrix(256)
+    q = oracle.decode_bf16(c.q_bits)
+    for s in range(3):
+        for h in range(2):
+            L = int(c.seq_lens[s])
+            k_r, v_r = dense_kv_uq(c.kv_cache, c.centroids, c.block_table, s, h, L, "ue8m0")
+            # a power-of-two scale keeps the e2m1 mantissas: every nonzero K
+            # value is 1 or 1.5 times a power of two
+            nz = np.abs(k_r[k_r != 0])
+            mant = nz / np.exp2(np.floor(np.log2(nz)))
+            assert np.all((mant == 1.0) | (mant == 1.5))
+            rows = slice(h * QG, (h + 1) * QG)
+            ref = attend(q[s, rows], k_r @ R, v_r @ R, 1.0 / 16.0)
+            assert np.max(np.abs(out[s, rows] - ref)) < 1e-11
