@@ -208,7 +208,24 @@ int pa_decode_fp8_ext(const void* q, const uint8_t* kv_cache, const int32_t* blo
  *   block_table, seq_lens, out, workspace: as for pa_decode_fp8 (head_dim 256)
  * Supported: head_dim 256, query_group 1..8, block_size 16/32/64/128/256.
  * Alignment: q, kv_cache and out 16-byte aligned; workspace 256-byte aligned.
+ *
+ * flags (other bits: QPA_ERR_SHAPE):
+ *   QPA_UQ_UE8M0_SCALES  K and V scale bytes are UE8M0, the group scale
+ *       format of [UQ] STEP C/F: scale = 2^(byte - 127), byte 0 = 0. The
+ *       kernel multiplies codes by the scale in f16, so results are exact
+ *       for bytes 104..140 (2^-23 .. 2^13); outside that window the product
+ *       overflows or flushes and the result is not defined.
+ *   QPA_UQ_Q_HAIRCUT  the e4m3 query rounding of [UQ] STEP B' (after the
+ *       rotation): the rotated query times softmax_scale is rounded to e4m3
+ *       (nearest even, saturating at +-448) and the logits are that rounded
+ *       query times k_t, with no further scale:
+ *           o_r = sum_t softmax_t(e4m3(softmax_scale * q_r) . k_t) v_t
+ *       The rotation feeding the rounding is float32 butterfly stages of
+ *       strides 1, 2, ..., 128 (x, y) -> (x + y, x - y), then * 1/16.
  * ====================================================================== */
+#define QPA_UQ_UE8M0_SCALES 1
+#define QPA_UQ_Q_HAIRCUT 2
+
 typedef struct qpa_uq_desc {
   int32_t num_seqs;
   int32_t num_kv_heads;
@@ -219,7 +236,7 @@ typedef struct qpa_uq_desc {
   int32_t max_blocks_per_seq;
   int32_t padded_slot;      /* bytes per (token, KV head) slot */
   int32_t out_dtype;        /* QPA_OUT_F32 or QPA_OUT_BF16 */
-  int32_t reserved;
+  int32_t flags;            /* 0, or QPA_UQ_UE8M0_SCALES | QPA_UQ_Q_HAIRCUT */
   int64_t q_stride_seq;     /* elements; 0 = num_kv_heads*query_group*256 */
   int64_t q_stride_head;    /* elements; 0 = 256 */
   float softmax_scale;      /* 0 = 1/sqrt(256) */

@@ -23,7 +23,7 @@ the same R, attention runs in the rotated domain with scale 1/sqrt(256)
 (the builder's default softmax scale), and the output is rotated back:
 o = softmax(scale q_r K_r^T) V_r R.
 
-Query haircut ([UQ] STEP B' "1/sqrt(D) normalization + E4M3 haircut"), the
+Query haircut (the e4m3 rounding that closes [UQ] STEP B'), the
 ``q_haircut`` option: q_h = e4m3(scale * q_r), rounded to nearest even and
 saturating at +-448, and the logits are q_h K_r^T with no further scale. The
 rotation feeding this rounding is computed in float32 by butterfly stages of
@@ -106,8 +106,8 @@ def uq_decode_hd256(q_bits, kv_cache, centroids, block_table, seq_lens, query_gr
     """Reference output [B, Hq, 256] in the un-rotated (logical) domain.
 
     q_bits [B, Hq, 256] uint16 bf16 bits (un-rotated); kv_cache [NB, bs, Hk,
-    padded_slot] uint8; centroids [16] float32. With q_haircut ([UQ] STEP B'
-    "1/sqrt(D) normalization + E4M3 haircut"), the rotated query times the
+    padded_slot] uint8; centroids [16] float32. With q_haircut (the e4m3
+    rounding that closes [UQ] STEP B'), the rotated query times the
     softmax scale is rounded to e4m3 (float32 rotation, as the kernel) and the
     logits are that rounded query times K_r, with no further scale."""
     q = decode_bf16(q_bits)

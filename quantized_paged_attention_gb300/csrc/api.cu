@@ -96,6 +96,7 @@ bool uq_shape_ok(const qpa_uq_desc* d) {
   if (d->padded_slot < 272 || d->padded_slot % 16) return false;
   if (d->out_dtype != QPA_OUT_F32 && d->out_dtype != QPA_OUT_BF16) return false;
   if ((long long)d->max_blocks_per_seq * bs > 0x7fffffffLL) return false;
+  if (d->flags & ~(QPA_UQ_UE8M0_SCALES | QPA_UQ_Q_HAIRCUT)) return false;
   return true;
 }
 
@@ -361,6 +362,7 @@ int uq_decode_hd256_partition(const void* q, const uint8_t* kv_cache, const floa
   a.num_partitions = num_partitions;
   a.padded_slot = d->padded_slot;
   a.softmax_scale = d->softmax_scale != 0.f ? d->softmax_scale : 1.0f / 16.0f;
+  a.flags = d->flags;
   a.num_sms = num_sms_current();
   if (a.num_sms <= 0) return QPA_ERR_CUDA;
   return launch_uq_partition(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;

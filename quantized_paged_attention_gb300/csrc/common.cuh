@@ -272,6 +272,12 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
   return r;
 }
+// Bytes 0 and 1 of x as UE8M0 scales -> f16x2 {2^(b0-127), 2^(b1-127)}: the
+// byte placed in a float32 exponent field is that power of two (byte 0 gives
+// 0). Exact for bytes 103..142, the powers of two f16 holds.
+__device__ __forceinline__ uint32_t ue8m0x2_lo_to_f16x2(uint32_t x) {
+  return f32x2_to_f16x2(__uint_as_float((x & 0xffu) << 23), __uint_as_float((x & 0xff00u) << 15));
+}
 __device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
   float r;
   asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %1; cvt.f32.f16 %0, lo; }" : "=f"(r) : "r"(h2));

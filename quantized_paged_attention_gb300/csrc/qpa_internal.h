@@ -72,6 +72,7 @@ struct UqLaunch {
   long long q_stride_seq, q_stride_head;
   int num_seqs, num_kv_heads, qg, block_size, num_blocks, max_blocks, num_partitions, padded_slot;
   float softmax_scale;
+  int flags;        // QPA_UQ_UE8M0_SCALES | QPA_UQ_Q_HAIRCUT
   int num_sms;
 };
 

@@ -13,10 +13,14 @@
 //  * the combine merges partitions and rotates the output back (o = o_r H/16).
 // Readings: the group scales are e4m3 and V decodes through a 16-entry fp32
 // centroid table (V = centroid[code] * scale); the page's own V convert
-// (e2m1 * scale) is the case where the table is the e2m1 value table.
+// (e2m1 * scale) is the case where the table is the e2m1 value table. Two
+// descriptor flags select the page's own formats: UE8M0 group scales
+// (2^(byte-127), built as f16 from the byte placed in a float32 exponent
+// field) and the e4m3 rounding of softmax_scale * q_r after the rotation
+// (the logits then take no further scale).
 //
 // GB300 design: one persistent 8-warp CTA per SM; each warp runs its own
-// 16-byte cp.async ring of three 32-token slices (8.5 KB each). An item
+// ring of three 32-token slices (8.5 KB each) filled by tensor-map copies. An item
 // (sequence, KV head, partition) belongs to a group of W warps (W = 1, 2 or
 // 4, picked on the host from the item count), which split its slices and
 // merge deterministically when W > 1; with W = 1 a warp writes its own
@@ -33,6 +37,7 @@
 //    converted with cvt e2m1x2 instead (detected in the kernel);
 //  * a lane's 32 output dims form one scale group, so one scale pair serves
 //    all of its V fragments of a token pair.
+#include "qpa.h"
 #include "common.cuh"
 #include "qpa_internal.h"
 #include "combine.cuh"
@@ -78,6 +83,7 @@ struct UqParams {
   long long q_stride_seq, q_stride_head;
   int num_seqs, num_kv_heads, qg, block_size, log2_bs, num_blocks, max_blocks, num_partitions, padded_slot;
   float softmax_scale;
+  int flags;        // QPA_UQ_UE8M0_SCALES | QPA_UQ_Q_HAIRCUT
 };
 
 enum : int { UEV_NONE = 0, UEV_ITEM = 1, UEV_SLICE = 2 };
@@ -256,7 +262,10 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
   // ---------------------------------------------------------------- consume side
   const int g = lane >> 2;
   const int c = lane & 3;
-  const float rowc = p.softmax_scale * kLog2e;
+  const bool ue8m0 = (p.flags & QPA_UQ_UE8M0_SCALES) != 0;
+  const bool haircut = (p.flags & QPA_UQ_Q_HAIRCUT) != 0;
+  // with the haircut the softmax scale is already inside the e4m3 query
+  const float rowc = haircut ? kLog2e : p.softmax_scale * kLog2e;
   uint32_t qf[32];          // rotated query row g, dims [64c, 64c+64), f16x2
   float o[16][4];           // O^T: m-tile i rows g, g+8 = dims 32g+2i, 32g+2i+1
   float m_run[2], l_run[2];
@@ -421,8 +430,16 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
           v[k] = upper ? pv - v[k] : v[k] + pv;
         }
       }
+      if (haircut) {
+        // e4m3(softmax_scale * q_r), nearest even, saturating; e4m3 -> f16 is exact
 #pragma unroll
-      for (int j = 0; j < 32; ++j) qf[j] = f32x2_to_f16x2(v[2 * j] * 0.0625f, v[2 * j + 1] * 0.0625f);
+        for (int j = 0; j < 32; ++j)
+          qf[j] = e4m3x2_lo_to_f16x2(f32x2_to_e4m3x2(v[2 * j] * 0.0625f * p.softmax_scale,
+                                                     v[2 * j + 1] * 0.0625f * p.softmax_scale));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) qf[j] = f32x2_to_f16x2(v[2 * j] * 0.0625f, v[2 * j + 1] * 0.0625f);
+      }
       m_run[0] = m_run[1] = -INFINITY;
       l_run[0] = l_run[1] = 0.f;
 #pragma unroll
@@ -450,8 +467,10 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
       const uint32_t kra[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
       const uint32_t krb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
       // K scales of groups 2c, 2c+1 for rows g, g+8 as {s, s} f16 pairs
-      const uint32_t sa = e4m3x2_lo_to_f16x2(lds32(rg + KS_OFF + 4 * (c >> 1)) >> (16 * (c & 1)));
-      const uint32_t sb = e4m3x2_lo_to_f16x2(lds32(rg8 + KS_OFF + 4 * (c >> 1)) >> (16 * (c & 1)));
+      const uint32_t swa = lds32(rg + KS_OFF + 4 * (c >> 1)) >> (16 * (c & 1));
+      const uint32_t swb = lds32(rg8 + KS_OFF + 4 * (c >> 1)) >> (16 * (c & 1));
+      const uint32_t sa = ue8m0 ? ue8m0x2_lo_to_f16x2(swa) : e4m3x2_lo_to_f16x2(swa);
+      const uint32_t sb = ue8m0 ? ue8m0x2_lo_to_f16x2(swb) : e4m3x2_lo_to_f16x2(swb);
       const uint32_t ksa0 = prmt(sa, sa, 0x1010), ksa1 = prmt(sa, sa, 0x3232);
       const uint32_t ksb0 = prmt(sb, sb, 0x1010), ksb1 = prmt(sb, sb, 0x3232);
       float sa4[4] = {0.f, 0.f, 0.f, 0.f}, sb4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -538,8 +557,9 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
           }
         }
       }
-      const uint32_t vs01 = e4m3x2_lo_to_f16x2(vsc);    // {s[2c], s[2c+1]}
-      const uint32_t vs89 = e4m3x2_hi_to_f16x2(vsc);    // {s[2c+8], s[2c+9]}
+      // {s[2c], s[2c+1]} and {s[2c+8], s[2c+9]}; a zeroed byte is 0 in both formats
+      const uint32_t vs01 = ue8m0 ? ue8m0x2_lo_to_f16x2(vsc) : e4m3x2_lo_to_f16x2(vsc);
+      const uint32_t vs89 = ue8m0 ? ue8m0x2_lo_to_f16x2(vsc >> 16) : e4m3x2_hi_to_f16x2(vsc);
 #pragma unroll
       for (int wq = 0; wq < 4; ++wq) {          // 4 code bytes (m-tiles 4wq..4wq+3) per word
         const uint32_t w0 = wq < 2 ? (wq == 0 ? vw[0][0].x : vw[0][0].y) : (wq == 2 ? vw[0][1].x : vw[0][1].y);
@@ -695,6 +715,7 @@ cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream) {
   p.num_partitions = a.num_partitions;
   p.padded_slot = a.padded_slot;
   p.softmax_scale = a.softmax_scale;
+  p.flags = a.flags;
   const long long items = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   if (items <= 0) return cudaSuccess;
   const int W = uq_warps_per_item(items, a.max_blocks, a.block_size, a.num_partitions, a.num_sms);

@@ -425,10 +425,10 @@ def sorted_random_centroids(seed: int) -> np.ndarray:
     return np.sort(rng(seed).standard_normal(16).astype(np.float32) * 2.0)
 
 
-def uq_full(seed: int = 1003, query_group: int = 8, centroids=None) -> UqCase:
+def uq_full(seed: int = 1003, query_group: int = 8, centroids=None, scale_format: str = "e4m3") -> UqCase:
     """4 seqs x 75000 tokens, 2 KV heads, block 64, 288-byte slots."""
     return make_uq_case(seed, [75000] * 4, 2, query_group, 64, 288, centroids=centroids,
-                        poison=False)
+                        poison=False, scale_format=scale_format)
 
 
 # ----------------------------------------------------------------------------

@@ -87,11 +87,12 @@ class UqDev:
         self.bt = torch.from_numpy(c.block_table).to(device)
         self.sl = torch.from_numpy(c.seq_lens).to(device)
 
-    def desc(self, out_dtype=torch.float32):
-        return qpa.uq_desc(self.q, self.kv, self.bt, self.c.query_group, self.c.softmax_scale, out_dtype)
+    def desc(self, out_dtype=torch.float32, q_haircut=False):
+        return qpa.uq_desc(self.q, self.kv, self.bt, self.c.query_group, self.c.softmax_scale, out_dtype,
+                           self.c.scale_format, q_haircut)
 
-    def run(self, P, out_dtype=torch.float32, workspace=None):
-        desc = self.desc(out_dtype)
+    def run(self, P, out_dtype=torch.float32, workspace=None, q_haircut=False):
+        desc = self.desc(out_dtype, q_haircut)
         if workspace is None:
             workspace = qpa.alloc_workspace(qpa.uq_decode_hd256_workspace_size(desc, P), self.q.device)
         out = qpa.uq_decode_hd256(self.q, self.kv, self.cent, self.bt, self.sl, P, self.c.query_group,
@@ -105,7 +106,7 @@ def uq_v_absmax(c, s, h):
     L = int(c.seq_lens[s])
     if L == 0:
         return 0.0
-    _, v = oracle.uq.dense_kv_uq(c.kv_cache, c.centroids, c.block_table, s, h, L)
+    _, v = oracle.uq.dense_kv_uq(c.kv_cache, c.centroids, c.block_table, s, h, L, c.scale_format)
     return float(np.abs(v).max())
 
 

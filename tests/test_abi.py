@@ -111,3 +111,25 @@ def test_ext_workspace_size(lib):
     # query_len 0 means one query token
     one = lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=0)), 2)
     assert one == lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc()), 2)
+
+
+def _uq_desc(**kw):
+    import quantized_paged_attention_gb300 as qpa
+    d = qpa.UqDesc()
+    d.num_seqs, d.num_kv_heads, d.query_group, d.head_dim = 2, 2, 8, 256
+    d.block_size, d.num_blocks, d.max_blocks_per_seq, d.padded_slot = 64, 8, 4, 288
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_uq_flags_validation(lib):
+    import quantized_paged_attention_gb300 as qpa
+    assert qpa.UqDesc.flags.offset == 36 and ctypes.sizeof(qpa.UqDesc) == 64
+    for f in (0, 1, 2, 3):
+        assert lib.uq_decode_hd256_workspace_size(ctypes.byref(_uq_desc(flags=f)), 3) > 0
+    for f in (4, 8, -1):
+        assert lib.uq_decode_hd256_workspace_size(ctypes.byref(_uq_desc(flags=f)), 3) == 0
+        st = lib.uq_decode_hd256(FAKE, FAKE, FAKE, FAKE, FAKE, 3, FAKE, ctypes.byref(_uq_desc(flags=f)), FAKE,
+                                 1 << 20, None)
+        assert st == -2

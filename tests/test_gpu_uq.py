@@ -17,9 +17,10 @@ def _lib():
     __graft_entry__.build()
 
 
-def _check(c, got, units=None, what=""):
+def _check(c, got, units=None, what="", q_haircut=False):
     ref = oracle.uq_decode_hd256(c.q_bits, c.kv_cache, c.centroids, c.block_table, c.seq_lens,
-                                 c.query_group, c.softmax_scale, units=units)
+                                 c.query_group, c.softmax_scale, units=units, scale_format=c.scale_format,
+                                 q_haircut=q_haircut)
     return check_attention(got, ref, lambda s, h: uq_v_absmax(c, s, h), c, units, what)
 
 
@@ -123,3 +124,44 @@ def test_full_config_sampled(qg):
     got = out.cpu().double().numpy()
     assert np.all(np.isfinite(got))
     _check(c, got, units=_sampled_units(c, 3, qg), what=f"uq-full qg={qg}")
+
+
+# ---- page formats: UE8M0 group scales and the e4m3 query haircut
+@pytest.mark.parametrize("haircut", [False, True])
+@pytest.mark.parametrize("fmt", ["e4m3", "ue8m0"])
+@pytest.mark.parametrize("P", [1, 5])
+def test_scale_format_and_haircut(fmt, haircut, P):
+    c = synth.make_uq_case(260 + P + (3 if haircut else 0), LENS, 2, 8, 64, 288, scale_format=fmt)
+    out, _, _ = UqDev(c).run(P, q_haircut=haircut)
+    _check(c, out.cpu().double().numpy(), what=f"{fmt} haircut={haircut} P={P}", q_haircut=haircut)
+
+
+def test_haircut_result_differs_from_plain():
+    """The haircut test above discriminates: the oracle's plain result misses
+    the kernel's haircut result by more than the tolerance."""
+    c = synth.make_uq_case(270, [5, 40], 2, 8, 64, 288, scale_format="ue8m0")
+    out, _, _ = UqDev(c).run(3, q_haircut=True)
+    got = out.cpu().double().numpy()
+    plain = oracle.uq_decode_hd256(c.q_bits, c.kv_cache, c.centroids, c.block_table, c.seq_lens, 8,
+                                   c.softmax_scale, scale_format="ue8m0")
+    tol = max(uq_v_absmax(c, s, h) for s in range(2) for h in range(2)) * 2e-3
+    assert np.max(np.abs(got - plain)) > 3 * tol
+    _check(c, got, what="ue8m0 haircut", q_haircut=True)
+
+
+@pytest.mark.parametrize("qg,bs", [(6, 16), (3, 256)])
+def test_page_formats_with_lut_groups_and_blocks(qg, bs):
+    c = synth.make_uq_case(280 + qg, [1, bs + 1, 900], 2, qg, bs, 288,
+                           centroids=synth.sorted_random_centroids(7), scale_format="ue8m0")
+    out, _, _ = UqDev(c).run(4, q_haircut=True)
+    _check(c, out.cpu().double().numpy(), what=f"ue8m0 haircut lut qg={qg} bs={bs}", q_haircut=True)
+
+
+def test_page_formats_full_config_sampled():
+    """4 seqs x 75000 tokens with UE8M0 scales and the query haircut, P=147;
+    3 sampled (seq, head) units against the oracle."""
+    c = synth.make_uq_case(1013, [75000] * 4, 2, 8, 64, 288, poison=False, scale_format="ue8m0")
+    out, _, _ = UqDev(c).run(147, q_haircut=True)
+    got = out.cpu().double().numpy()
+    assert np.all(np.isfinite(got))
+    _check(c, got, units=_sampled_units(c, 3, 9), what="uq-full ue8m0 haircut", q_haircut=True)
