@@ -27,5 +27,6 @@ header of each module for what pins it.
 from .formats import decode_bf16, decode_e2m1, decode_e4m3fn, decode_ue8m0, round_e4m3  # noqa: F401
 from .attention import (attend, combine_partials, partition_partials, pa_decode_fp8, pa_decode_fp8_ext,  # noqa: F401
                         tile_groups_of_partition)
-from .uq import decode_uq_slots, rotate_q_fp32, uq_decode_hd256, wht_matrix  # noqa: F401
+from .uq import (decode_uq_slots, perm_dest, perm_source, rotate_q_fp32, rotation_matrix,  # noqa: F401
+                 uq_decode_hd256, wht_matrix)
 from .scorer import nvfp4_index_score, nvfp4_token_dots  # noqa: F401

@@ -23,6 +23,11 @@ the same R, attention runs in the rotated domain with scale 1/sqrt(256)
 (the builder's default softmax scale), and the output is rotated back:
 o = softmax(scale q_r K_r^T) V_r R.
 
+Column permutation ([UQ] STEP B', the permutation folded into the rotation
+constant): with ``rot_perm`` the rotation is M, R with its columns permuted
+so that the value at butterfly position d lands at dim perm_dest(d); K_r, V_r
+are in that domain and the output is o_r M^T.
+
 Query haircut (the e4m3 rounding that closes [UQ] STEP B'), the
 ``q_haircut`` option: q_h = e4m3(scale * q_r), rounded to nearest even and
 saturating at +-448, and the logits are q_h K_r^T with no further scale. The
@@ -39,7 +44,10 @@ rotated pipeline against plain attention on the logical K = K_r R,
 V = V_r R (e4m3 and UE8M0 scales). The float32 rotation exactly against
 x H on integer inputs and within the page's fp32 bound on random ones; the
 haircut as the identity on queries whose scaled rotation is already e4m3, and
-against torch's e4m3 cast plus a written-out softmax.
+against torch's e4m3 cast plus a written-out softmax. The permutation against
+the page's second, per-lane form of it; a bijection moving single bits; the
+permuted rotation orthonormal and a column permutation of R; the permuted
+pipeline (with and without the haircut) against logical-domain attention.
 """
 import math
 
@@ -64,6 +72,32 @@ def wht_matrix(n: int = HEAD) -> np.ndarray:
         parity ^= x & 1
         x = x >> 1
     return np.where(parity == 1, -1.0, 1.0) / math.sqrt(n)
+
+
+def perm_dest(d):
+    """The page's column permutation of the rotation ([UQ] STEP B', the
+    inverse query permutation): the rotated value at butterfly position d is
+    stored at dim (d & 0x8F) | ((d >> 2) & 0x10) | ((d << 1) & 0x60), i.e.
+    bits 4, 5, 6 of the index move to 5, 6, 4."""
+    d = np.asarray(d)
+    return (d & 0x8F) | ((d >> 2) & 0x10) | ((d << 1) & 0x60)
+
+
+def perm_source(j):
+    """Inverse of perm_dest: the butterfly position whose value lands at dim j."""
+    j = np.asarray(j)
+    return (j & 0x8F) | ((j & 0x10) << 2) | ((j >> 1) & 0x30)
+
+
+def rotation_matrix(rot_perm: bool = False) -> np.ndarray:
+    """q_r = q M. Without the permutation M = R = H/16; with it, column
+    perm_dest(d) of M is column d of R (q_r[perm_dest(d)] = (q R)[d])."""
+    R = wht_matrix(HEAD)
+    if not rot_perm:
+        return R
+    M = np.empty_like(R)
+    M[:, perm_dest(np.arange(HEAD))] = R
+    return M
 
 
 def rotate_q_fp32(q: np.ndarray) -> np.ndarray:
@@ -102,14 +136,17 @@ def dense_kv_uq(kv_cache, centroids, block_table, seq, kv_head, L, scale_format=
 
 def uq_decode_hd256(q_bits, kv_cache, centroids, block_table, seq_lens, query_group: int,
                     softmax_scale: float | None = None, units=None,
-                    scale_format: str = "e4m3", q_haircut: bool = False) -> np.ndarray:
+                    scale_format: str = "e4m3", q_haircut: bool = False,
+                    rot_perm: bool = False) -> np.ndarray:
     """Reference output [B, Hq, 256] in the un-rotated (logical) domain.
 
     q_bits [B, Hq, 256] uint16 bf16 bits (un-rotated); kv_cache [NB, bs, Hk,
     padded_slot] uint8; centroids [16] float32. With q_haircut (the e4m3
     rounding that closes [UQ] STEP B'), the rotated query times the
     softmax scale is rounded to e4m3 (float32 rotation, as the kernel) and the
-    logits are that rounded query times K_r, with no further scale."""
+    logits are that rounded query times K_r, with no further scale. With
+    rot_perm the rotation is M = R with the page's column permutation
+    (rotation_matrix) and the output is o_r M^T."""
     q = decode_bf16(q_bits)
     B, Hq, D = q.shape
     assert D == HEAD
@@ -117,7 +154,7 @@ def uq_decode_hd256(q_bits, kv_cache, centroids, block_table, seq_lens, query_gr
     assert Hq == Hk * query_group
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(HEAD)
-    R = wht_matrix(HEAD)
+    M = rotation_matrix(rot_perm)
     out = np.zeros((B, Hq, D))
     if units is None:
         units = [(s, h) for s in range(B) for h in range(Hk)]
@@ -126,12 +163,15 @@ def uq_decode_hd256(q_bits, kv_cache, centroids, block_table, seq_lens, query_gr
         k_r, v_r = dense_kv_uq(kv_cache, centroids, block_table, s, h, L, scale_format)
         rows = slice(h * query_group, (h + 1) * query_group)
         if q_haircut:
-            q16 = rotate_q_fp32(q[s, rows])                                    # 16 q R in float32
+            # q M = (q permuted by perm_source) R, since the permutation only
+            # moves index bits: the float32 butterfly runs on the permuted q
+            qin = q[s, rows][:, perm_source(np.arange(HEAD))] if rot_perm else q[s, rows]
+            q16 = rotate_q_fp32(qin)                                           # 16 q M in float32
             qs = (q16 * np.float32(0.0625)) * np.float32(softmax_scale)         # float32 products
             q_h = round_e4m3(qs.astype(np.float64))
             o_r = attend(q_h, k_r, v_r, 1.0)
         else:
-            q_r = q[s, rows] @ R
+            q_r = q[s, rows] @ M
             o_r = attend(q_r, k_r, v_r, softmax_scale)
-        out[s, rows] = o_r @ R
+        out[s, rows] = o_r @ M.T
     return out

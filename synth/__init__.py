@@ -338,6 +338,7 @@ class UqCase:
     padded_slot: int
     softmax_scale: float
     scale_format: str = "e4m3"   # group scale bytes: "e4m3" (e4m3fn) or "ue8m0" (2^(b-127))
+    rot_perm: bool = False       # K/V rotated with the page's column-permuted rotation
 
     @property
     def num_seqs(self):
@@ -347,6 +348,17 @@ class UqCase:
     def kv_bytes(self) -> int:
         """Slot content bytes read once (272 per token and KV head)."""
         return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * UQ_CONTENT
+
+
+def page_rotation_perm() -> np.ndarray:
+    """The dim each butterfly position d = 32 c + t of the rotation lands on
+    when the page's column permutation is folded in, from the page's per-lane
+    split of it: (t & 0x0F) | ((t & 0x10) << 1) | ((c & 2) << 3) |
+    ((c & 1) << 6) | ((c & 4) << 5). Producer side: used only to put the
+    synthetic K/V into the permuted rotated domain."""
+    c = np.arange(256) // 32
+    t = np.arange(256) % 32
+    return (t & 0x0F) | ((t & 0x10) << 1) | ((c & 2) << 3) | ((c & 1) << 6) | ((c & 4) << 5)
 
 
 def sylvester_pm1(n: int) -> np.ndarray:
@@ -362,7 +374,7 @@ def make_uq_case(seed: int, seq_lens, num_kv_heads: int = 2, query_group: int = 
                  block_size: int = 64, padded_slot: int = 288, centroids=None,
                  num_blocks: int | None = None, softmax_scale: float | None = None,
                  poison: bool = True, chunk_tokens: int = 1 << 15,
-                 scale_format: str = "e4m3") -> UqCase:
+                 scale_format: str = "e4m3", rot_perm: bool = False) -> UqCase:
     if scale_format not in ("e4m3", "ue8m0"):
         raise ValueError(scale_format)
     r = rng(seed)
@@ -379,6 +391,10 @@ def make_uq_case(seed: int, seq_lens, num_kv_heads: int = 2, query_group: int = 
     Hq = num_kv_heads * query_group
     q_bits = round_to_bf16_bits(r.standard_normal((B, Hq, UQ_D), dtype=np.float32))
     rot = (sylvester_pm1(UQ_D) / 16.0).astype(np.float32)
+    if rot_perm:
+        prm = np.empty_like(rot)
+        prm[:, page_rotation_perm()] = rot
+        rot = prm
     ntok = num_blocks * block_size * num_kv_heads
     cache = np.zeros((ntok, padded_slot), dtype=np.uint8)
     for o in range(0, ntok, chunk_tokens):
@@ -416,7 +432,7 @@ def make_uq_case(seed: int, seq_lens, num_kv_heads: int = 2, query_group: int = 
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(UQ_D)
     return UqCase(q_bits, cache, centroids, bt, seq_lens, num_kv_heads, query_group,
-                  block_size, padded_slot, float(softmax_scale), scale_format)
+                  block_size, padded_slot, float(softmax_scale), scale_format, rot_perm)
 
 
 def sorted_random_centroids(seed: int) -> np.ndarray:
@@ -425,10 +441,11 @@ def sorted_random_centroids(seed: int) -> np.ndarray:
     return np.sort(rng(seed).standard_normal(16).astype(np.float32) * 2.0)
 
 
-def uq_full(seed: int = 1003, query_group: int = 8, centroids=None, scale_format: str = "e4m3") -> UqCase:
+def uq_full(seed: int = 1003, query_group: int = 8, centroids=None, scale_format: str = "e4m3",
+            rot_perm: bool = False) -> UqCase:
     """4 seqs x 75000 tokens, 2 KV heads, block 64, 288-byte slots."""
     return make_uq_case(seed, [75000] * 4, 2, query_group, 64, 288, centroids=centroids,
-                        poison=False, scale_format=scale_format)
+                        poison=False, scale_format=scale_format, rot_perm=rot_perm)
 
 
 # ----------------------------------------------------------------------------

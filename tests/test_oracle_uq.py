@@ -232,3 +232,61 @@ def test_ue8m0_case_pipeline_equals_logical_attention(QG):
             rows = slice(h * QG, (h + 1) * QG)
             ref = attend(q[s, rows], k_r @ R, v_r @ R, 1.0 / 16.0)
             assert np.max(np.abs(out[s, rows] - ref)) < 1e-11
+
+
+# ---- the page's column permutation of the rotation
+def test_perm_dest_agrees_with_the_pages_per_lane_split():
+    # the page gives the permutation twice: as one formula on the dim, and as
+    # a sum of a part in the element t and a part in the 32-dim chunk c
+    for c in range(8):
+        for t in range(32):
+            ct = (t & 0x0F) | ((t & 0x10) << 1)
+            rt = ((c & 2) << 3) | ((c & 1) << 6) | ((c & 4) << 5)
+            assert int(oracle.perm_dest(32 * c + t)) == ct | rt
+
+
+def test_perm_is_a_bit_permutation_and_inverse():
+    d = np.arange(256)
+    p = oracle.perm_dest(d)
+    assert sorted(p.tolist()) == list(range(256))
+    assert np.array_equal(oracle.perm_source(p), d)
+    for b in range(8):                      # a single set bit goes to a single set bit
+        assert bin(int(oracle.perm_dest(1 << b))).count("1") == 1
+    assert np.array_equal(p & 0x8F, d & 0x8F)
+
+
+def test_permuted_rotation_orthonormal_and_a_column_permutation():
+    M = oracle.rotation_matrix(True)
+    R = oracle.wht_matrix(256)
+    assert np.max(np.abs(M @ M.T - np.eye(256))) < 1e-13
+    q = np.random.default_rng(8).standard_normal((3, 256))
+    qr = q @ R
+    assert np.allclose((q @ M)[:, oracle.perm_dest(np.arange(256))], qr, atol=1e-13, rtol=0)
+    # M is no longer symmetric, so the output needs M^T, not M
+    assert not np.array_equal(M, M.T)
+
+
+@pytest.mark.parametrize("haircut", [False, True])
+def test_permuted_pipeline_equals_logical_attention(haircut):
+    c = synth.make_uq_case(37, [120, 9], 2, 4, 64, 288, rot_perm=True)
+    out = oracle.uq_decode_hd256(c.q_bits, c.kv_cache, c.centroids, c.block_table, c.seq_lens, 4,
+                                 c.softmax_scale, rot_perm=True, q_haircut=haircut)
+    M = oracle.rotation_matrix(True)
+    q = oracle.decode_bf16(c.q_bits)
+    for s in range(2):
+        for h in range(2):
+            k_r, v_r = dense_kv_uq(c.kv_cache, c.centroids, c.block_table, s, h, int(c.seq_lens[s]))
+            rows = slice(4 * h, 4 * h + 4)
+            if haircut:
+                # q M rounded to e4m3 after the scale, built from the float64 matrix and torch's cast
+                qr = (q[s, rows] @ M * (1 / 16)).astype(np.float32)
+                qh = torch.from_numpy(qr).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+                lg = qh @ k_r.T
+                w = np.exp(lg - lg.max(axis=1, keepdims=True))
+                ref = (w / w.sum(axis=1, keepdims=True)) @ v_r @ M.T
+            else:
+                ref = attend(q[s, rows], k_r @ M.T, v_r @ M.T, 1.0 / 16.0)     # logical domain
+            assert np.max(np.abs(out[s, rows] - ref)) < 1e-11
+    plain = oracle.uq_decode_hd256(c.q_bits, c.kv_cache, c.centroids, c.block_table, c.seq_lens, 4,
+                                   c.softmax_scale, q_haircut=haircut)
+    assert np.max(np.abs(out - plain)) > 1e-2        # the permutation matters on this cache
