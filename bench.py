@@ -327,7 +327,7 @@ def time_uq(c, P, steps, warmup, dev, q_haircut=False):
     bt = torch.from_numpy(c.block_table).to(dev)
     sl = torch.from_numpy(c.seq_lens).to(dev)
     desc = qpa.uq_desc(q, kv, bt, c.query_group, c.softmax_scale, scale_format=c.scale_format,
-                       q_haircut=q_haircut)
+                       q_haircut=q_haircut, rot_perm=c.rot_perm)
     ws = qpa.alloc_workspace(qpa.uq_decode_hd256_workspace_size(desc, P), dev)
     out = torch.empty((q.shape[0], q.shape[1], 256), dtype=torch.float32, device=dev)
     r = _time_loop(lambda: qpa.uq_decode_hd256_partition(q, kv, cent, bt, sl, P, desc, ws),
@@ -521,16 +521,17 @@ def main():
         esteps = max(20, a.steps // 4)
         for name, cent, pagefmt in (("uq_hd256_b4_75k_e2m1", None, False),
                                     ("uq_hd256_b4_75k_randtable", "rand", False),
-                                    ("uq_hd256_b4_75k_ue8m0_q_haircut", None, True)):
+                                    ("uq_hd256_b4_75k_page_formats", None, True)):
             cu = synth.uq_full(seed=1003 + rank, centroids=None if cent is None else synth.sorted_random_centroids(5),
-                               scale_format="ue8m0" if pagefmt else "e4m3")
+                               scale_format="ue8m0" if pagefmt else "e4m3", rot_perm=pagefmt)
             u_ms, u_part = time_uq(cu, 147, esteps, a.warmup, dev, q_haircut=pagefmt)
             u_ms = _max_over_ranks(u_ms)
             extra[name] = {
                 "workload": "4-bit head_dim 256 decode, 4 seqs x 75000 tokens, 2 KV heads, group 8, block 64, "
                             "288-byte slots, P=147, centroid table " + ("e2m1 values" if cent is None else
                                                                          "seeded sorted random")
-                            + (", UE8M0 group scales, e4m3 query haircut" if pagefmt else ", e4m3 group scales"),
+                            + (", UE8M0 group scales, e4m3 query haircut, column-permuted rotation" if pagefmt
+                               else ", e4m3 group scales"),
                 "us_per_step": round(u_ms * 1e3, 2), "partition_us": round(u_part * 1e3, 2),
                 "l2": "flushed (256 MB write, then read) before every timed step", "kv_bytes": cu.kv_bytes, "gbs": round(cu.kv_bytes / (u_ms * 1e-3) / 1e9, 1),
                 "frac_of_peak": round(cu.kv_bytes / (u_ms * 1e-3) / 1e9 / peak, 4)}

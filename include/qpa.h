@@ -222,9 +222,16 @@ int pa_decode_fp8_ext(const void* q, const uint8_t* kv_cache, const int32_t* blo
  *           o_r = sum_t softmax_t(e4m3(softmax_scale * q_r) . k_t) v_t
  *       The rotation feeding the rounding is float32 butterfly stages of
  *       strides 1, 2, ..., 128 (x, y) -> (x + y, x - y), then * 1/16.
+ *   QPA_UQ_ROT_PERM  the rotation carries the column permutation of [UQ]
+ *       STEP B': R is replaced by M with M[:, perm(d)] = R[:, d],
+ *           perm(d) = (d & 0x8F) | ((d >> 2) & 0x10) | ((d << 1) & 0x60),
+ *       so q_r = q M, the cache holds k M and v M, and out = o_r M^T. (With
+ *       the haircut, the butterfly runs on q[perm^-1(m)] at position m, which
+ *       gives 16 q M.)
  * ====================================================================== */
 #define QPA_UQ_UE8M0_SCALES 1
 #define QPA_UQ_Q_HAIRCUT 2
+#define QPA_UQ_ROT_PERM 4
 
 typedef struct qpa_uq_desc {
   int32_t num_seqs;
@@ -236,7 +243,7 @@ typedef struct qpa_uq_desc {
   int32_t max_blocks_per_seq;
   int32_t padded_slot;      /* bytes per (token, KV head) slot */
   int32_t out_dtype;        /* QPA_OUT_F32 or QPA_OUT_BF16 */
-  int32_t flags;            /* 0, or QPA_UQ_UE8M0_SCALES | QPA_UQ_Q_HAIRCUT */
+  int32_t flags;            /* 0 or any of QPA_UQ_UE8M0_SCALES | QPA_UQ_Q_HAIRCUT | QPA_UQ_ROT_PERM */
   int64_t q_stride_seq;     /* elements; 0 = num_kv_heads*query_group*256 */
   int64_t q_stride_head;    /* elements; 0 = 256 */
   float softmax_scale;      /* 0 = 1/sqrt(256) */

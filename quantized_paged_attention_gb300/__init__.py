@@ -21,6 +21,7 @@ QPA_OUT_F32 = 0
 QPA_OUT_BF16 = 1
 QPA_UQ_UE8M0_SCALES = 1
 QPA_UQ_Q_HAIRCUT = 2
+QPA_UQ_ROT_PERM = 4
 _lib = None
 
 
@@ -284,9 +285,10 @@ def pa_decode_fp8_static(q, kv_cache, block_table, seq_lens, k_scale, v_scale, n
 
 # --------------------------------------------------------------------- uq hd256
 def uq_desc(q, kv_cache, block_table, query_group, softmax_scale=None, out_dtype=torch.float32,
-            scale_format="e4m3", q_haircut=False):
+            scale_format="e4m3", q_haircut=False, rot_perm=False):
     """scale_format: "e4m3" or "ue8m0" group scale bytes; q_haircut: round
-    softmax_scale * q_r to e4m3 before the QK product."""
+    softmax_scale * q_r to e4m3 before the QK product; rot_perm: the cache is
+    in the domain of the column-permuted rotation."""
     if scale_format not in ("e4m3", "ue8m0"):
         raise ValueError(f"scale_format {scale_format!r}")
     B, Hq, D = q.shape
@@ -300,7 +302,8 @@ def uq_desc(q, kv_cache, block_table, query_group, softmax_scale=None, out_dtype
     d.out_dtype = QPA_OUT_BF16 if out_dtype == torch.bfloat16 else QPA_OUT_F32
     d.q_stride_seq, d.q_stride_head = q.stride(0), q.stride(1)
     d.softmax_scale = 0.0 if softmax_scale is None else float(softmax_scale)
-    d.flags = (QPA_UQ_UE8M0_SCALES if scale_format == "ue8m0" else 0) | (QPA_UQ_Q_HAIRCUT if q_haircut else 0)
+    d.flags = ((QPA_UQ_UE8M0_SCALES if scale_format == "ue8m0" else 0) | (QPA_UQ_Q_HAIRCUT if q_haircut else 0)
+               | (QPA_UQ_ROT_PERM if rot_perm else 0))
     return d
 
 
@@ -310,14 +313,15 @@ def uq_decode_hd256_workspace_size(desc: UqDesc, num_partitions: int) -> int:
 
 def uq_decode_hd256(q, kv_cache, centroids, block_table, seq_lens, num_partitions: int, query_group: int,
                     out=None, workspace=None, softmax_scale=None, out_dtype=torch.float32, stream=None,
-                    desc=None, scale_format="e4m3", q_haircut=False):
+                    desc=None, scale_format="e4m3", q_haircut=False, rot_perm=False):
     """4-bit head_dim=256 decode. q bf16 [B, Hq, 256] (not rotated); kv_cache
     uint8 [NB, bs, Hk, padded_slot]; centroids float32 [16]; returns the
-    un-rotated out [B, Hq, 256]. scale_format / q_haircut as in uq_desc."""
+    un-rotated out [B, Hq, 256]. scale_format / q_haircut / rot_perm as in uq_desc."""
     lib = load_library()
     _need_cuda(q, kv_cache, centroids, block_table, seq_lens)
     if desc is None:
-        desc = uq_desc(q, kv_cache, block_table, query_group, softmax_scale, out_dtype, scale_format, q_haircut)
+        desc = uq_desc(q, kv_cache, block_table, query_group, softmax_scale, out_dtype, scale_format, q_haircut,
+                       rot_perm)
     if out is None:
         odt = torch.bfloat16 if desc.out_dtype == QPA_OUT_BF16 else torch.float32
         out = torch.empty((q.shape[0], q.shape[1], 256), dtype=odt, device=q.device)

@@ -96,7 +96,7 @@ bool uq_shape_ok(const qpa_uq_desc* d) {
   if (d->padded_slot < 272 || d->padded_slot % 16) return false;
   if (d->out_dtype != QPA_OUT_F32 && d->out_dtype != QPA_OUT_BF16) return false;
   if ((long long)d->max_blocks_per_seq * bs > 0x7fffffffLL) return false;
-  if (d->flags & ~(QPA_UQ_UE8M0_SCALES | QPA_UQ_Q_HAIRCUT)) return false;
+  if (d->flags & ~(QPA_UQ_UE8M0_SCALES | QPA_UQ_Q_HAIRCUT | QPA_UQ_ROT_PERM)) return false;
   return true;
 }
 
@@ -392,6 +392,7 @@ int uq_decode_hd256_combine(int num_partitions, void* out, const qpa_uq_desc* d,
   c.d = 256;
   c.out_stride_head = 256;
   c.out_stride_seq = (long long)d->num_kv_heads * d->query_group * 256;
+  c.rot_perm = (d->flags & QPA_UQ_ROT_PERM) != 0;
   return launch_uq_combine(c, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;
 }
 

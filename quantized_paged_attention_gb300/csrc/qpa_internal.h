@@ -58,6 +58,7 @@ struct CombineLaunch {
   int out_bf16;
   int num_seqs, num_kv_heads, qg, num_partitions, d;
   long long out_stride_seq, out_stride_head;
+  int rot_perm = 0;   // uq only: undo the rotation's column permutation
 };
 
 struct UqLaunch {
@@ -72,7 +73,7 @@ struct UqLaunch {
   long long q_stride_seq, q_stride_head;
   int num_seqs, num_kv_heads, qg, block_size, num_blocks, max_blocks, num_partitions, padded_slot;
   float softmax_scale;
-  int flags;        // QPA_UQ_UE8M0_SCALES | QPA_UQ_Q_HAIRCUT
+  int flags;        // QPA_UQ_UE8M0_SCALES | QPA_UQ_Q_HAIRCUT | QPA_UQ_ROT_PERM
   int num_sms;
 };
 

@@ -16,8 +16,9 @@
 // (e2m1 * scale) is the case where the table is the e2m1 value table. Two
 // descriptor flags select the page's own formats: UE8M0 group scales
 // (2^(byte-127), built as f16 from the byte placed in a float32 exponent
-// field) and the e4m3 rounding of softmax_scale * q_r after the rotation
-// (the logits then take no further scale).
+// field), the e4m3 rounding of softmax_scale * q_r after the rotation
+// (the logits then take no further scale), and the rotation's column
+// permutation (a permuted q load here, a permuted store in the combine).
 //
 // GB300 design: one persistent 8-warp CTA per SM; each warp runs its own
 // ring of three 32-token slices (8.5 KB each) filled by tensor-map copies. An item
@@ -87,6 +88,16 @@ struct UqParams {
 };
 
 enum : int { UEV_NONE = 0, UEV_ITEM = 1, UEV_SLICE = 2 };
+
+// The rotation's column permutation: the value at butterfly position d lands
+// on dim rot_perm_dest(d) (bits 4, 5, 6 of the index move to 5, 6, 4);
+// rot_perm_source is its inverse.
+__device__ __forceinline__ int rot_perm_dest(int d) {
+  return (d & 0x8F) | ((d >> 2) & 0x10) | ((d << 1) & 0x60);
+}
+__device__ __forceinline__ int rot_perm_source(int j) {
+  return (j & 0x8F) | ((j & 0x10) << 2) | ((j >> 1) & 0x30);
+}
 
 // e2m1 values in code order (the table for which V decodes with cvt).
 __device__ __forceinline__ float e2m1_value(int k) {
@@ -264,6 +275,7 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
   const int c = lane & 3;
   const bool ue8m0 = (p.flags & QPA_UQ_UE8M0_SCALES) != 0;
   const bool haircut = (p.flags & QPA_UQ_Q_HAIRCUT) != 0;
+  const bool rot_perm = (p.flags & QPA_UQ_ROT_PERM) != 0;
   // with the haircut the softmax scale is already inside the e4m3 query
   const float rowc = haircut ? kLog2e : p.softmax_scale * kLog2e;
   uint32_t qf[32];          // rotated query row g, dims [64c, 64c+64), f16x2
@@ -393,12 +405,17 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
       cur_item = ea;
       const bool work = (ea % P) * TG < eb;
       // ---- rotated query: row g, dims [64c, 64c+64); butterfly stages with
-      // strides 1..32 in registers, 64 and 128 across lanes c^1 and c^2
+      // strides 1..32 in registers, 64 and 128 across lanes c^1 and c^2. With
+      // the column-permuted rotation, position m takes q[perm^-1(m)] (the
+      // permutation moves index bits 4..6 only, so it commutes through the
+      // Hadamard and 8-dim runs stay contiguous).
       float v[64];
       if (work && g < p.qg) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint4 w4 = lds128(slot + g * 512 + c * 128 + j * 16);
+          const int m = 64 * c + 8 * j;
+          const int src = rot_perm ? rot_perm_source(m) : m;
+          const uint4 w4 = lds128(slot + g * 512 + src * 2);
           const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -609,7 +626,7 @@ template <typename OutT>
 __global__ void __launch_bounds__(kCombineMaxThreads)
 uq_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
                   const float* __restrict__ part_l, OutT* __restrict__ out, int num_kv_heads, int qg,
-                  int num_partitions, long long out_stride_seq, long long out_stride_head) {
+                  int num_partitions, long long out_stride_seq, long long out_stride_head, int rot_perm) {
   constexpr int D = 256;
   extern __shared__ __align__(16) float sw[];
   __shared__ __align__(16) float vec[D];
@@ -634,9 +651,11 @@ uq_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ pa
     __syncthreads();
   }
   if (tid < D / 4) {
+    // with the column-permuted rotation M, out[i] = (o_r H / 16)[perm(i)]
+    // (perm keeps bits 0..3, so four consecutive dims stay together)
+    const int src = rot_perm ? rot_perm_dest(4 * tid) : 4 * tid;
     OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + 4 * tid;
-    store4(dst, vec[4 * tid] * 0.0625f, vec[4 * tid + 1] * 0.0625f, vec[4 * tid + 2] * 0.0625f,
-           vec[4 * tid + 3] * 0.0625f);
+    store4(dst, vec[src] * 0.0625f, vec[src + 1] * 0.0625f, vec[src + 2] * 0.0625f, vec[src + 3] * 0.0625f);
   }
 }
 
@@ -749,7 +768,7 @@ static cudaError_t launch_uq_combine_t(const CombineLaunch& a, OutT* out, cudaSt
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, uq_combine_kernel<OutT>, a.part_o, a.part_m, a.part_l, out, a.num_kv_heads,
-                            a.qg, a.num_partitions, a.out_stride_seq, a.out_stride_head);
+                            a.qg, a.num_partitions, a.out_stride_seq, a.out_stride_head, a.rot_perm);
 }
 
 cudaError_t launch_uq_combine(const CombineLaunch& a, cudaStream_t stream) {

@@ -89,7 +89,7 @@ class UqDev:
 
     def desc(self, out_dtype=torch.float32, q_haircut=False):
         return qpa.uq_desc(self.q, self.kv, self.bt, self.c.query_group, self.c.softmax_scale, out_dtype,
-                           self.c.scale_format, q_haircut)
+                           self.c.scale_format, q_haircut, self.c.rot_perm)
 
     def run(self, P, out_dtype=torch.float32, workspace=None, q_haircut=False):
         desc = self.desc(out_dtype, q_haircut)

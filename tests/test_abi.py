@@ -126,9 +126,9 @@ def _uq_desc(**kw):
 def test_uq_flags_validation(lib):
     import quantized_paged_attention_gb300 as qpa
     assert qpa.UqDesc.flags.offset == 36 and ctypes.sizeof(qpa.UqDesc) == 64
-    for f in (0, 1, 2, 3):
+    for f in range(8):
         assert lib.uq_decode_hd256_workspace_size(ctypes.byref(_uq_desc(flags=f)), 3) > 0
-    for f in (4, 8, -1):
+    for f in (8, 16, -1):
         assert lib.uq_decode_hd256_workspace_size(ctypes.byref(_uq_desc(flags=f)), 3) == 0
         st = lib.uq_decode_hd256(FAKE, FAKE, FAKE, FAKE, FAKE, 3, FAKE, ctypes.byref(_uq_desc(flags=f)), FAKE,
                                  1 << 20, None)

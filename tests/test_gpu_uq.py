@@ -20,7 +20,7 @@ def _lib():
 def _check(c, got, units=None, what="", q_haircut=False):
     ref = oracle.uq_decode_hd256(c.q_bits, c.kv_cache, c.centroids, c.block_table, c.seq_lens,
                                  c.query_group, c.softmax_scale, units=units, scale_format=c.scale_format,
-                                 q_haircut=q_haircut)
+                                 q_haircut=q_haircut, rot_perm=c.rot_perm)
     return check_attention(got, ref, lambda s, h: uq_v_absmax(c, s, h), c, units, what)
 
 
@@ -165,3 +165,28 @@ def test_page_formats_full_config_sampled():
     got = out.cpu().double().numpy()
     assert np.all(np.isfinite(got))
     _check(c, got, units=_sampled_units(c, 3, 9), what="uq-full ue8m0 haircut", q_haircut=True)
+
+
+# ---- the page's column-permuted rotation
+@pytest.mark.parametrize("fmt,haircut", [("e4m3", False), ("ue8m0", True)])
+@pytest.mark.parametrize("P", [1, 4])
+def test_rotation_permutation(fmt, haircut, P):
+    c = synth.make_uq_case(290 + P + (5 if haircut else 0), LENS, 2, 8, 64, 288, scale_format=fmt, rot_perm=True)
+    out, _, _ = UqDev(c).run(P, q_haircut=haircut)
+    got = out.cpu().double().numpy()
+    _check(c, got, what=f"perm {fmt} haircut={haircut} P={P}", q_haircut=haircut)
+
+
+def test_rotation_permutation_matters_and_bf16_output():
+    c = synth.make_uq_case(299, [7, 40], 2, 6, 32, 288, rot_perm=True,
+                           centroids=synth.sorted_random_centroids(8))
+    d = UqDev(c)
+    out, _, _ = d.run(2)
+    got = out.cpu().double().numpy()
+    _check(c, got, what="perm lut qg=6 bs=32")
+    plain = oracle.uq_decode_hd256(c.q_bits, c.kv_cache, c.centroids, c.block_table, c.seq_lens, 6,
+                                   c.softmax_scale)
+    tol = max(uq_v_absmax(c, s, h) for s in range(2) for h in range(2)) * 2e-3
+    assert np.max(np.abs(got - plain)) > 3 * tol
+    o16, _, _ = d.run(2, out_dtype=torch.bfloat16)
+    assert torch.max(torch.abs(o16.float() - out)).item() <= torch.max(torch.abs(out)).item() * 2 ** -8 + 1e-6
