@@ -29,4 +29,4 @@ from .attention import (attend, combine_partials, partition_partials, pa_decode_
                         tile_groups_of_partition)
 from .uq import (decode_uq_slots, perm_dest, perm_source, rotate_q_fp32, rotation_matrix,  # noqa: F401
                  uq_decode_hd256, wht_matrix)
-from .scorer import nvfp4_index_score, nvfp4_token_dots  # noqa: F401
+from .scorer import nvfp4_index_score, nvfp4_index_score_per_token, nvfp4_token_dots  # noqa: F401

@@ -15,6 +15,9 @@ byte i) and bytes 8192..9215 the e4m3 scales (8 per token, one per 16 dims).
                      ([IDX] ``frag_max``: the max of a column's scores over
                      the page); blocks at or past ceil(L / 128) get -inf.
 
+Per-token output (``nvfp4_index_score_per_token``): the same dots before the
+block max, one column per token, -inf where the token is not visible.
+
 Readings: no scale, weight or activation is applied to the dot (none is
 shown); the per-block sentinels ``init``/``local`` are taken as 0, which
 makes the page's skip predicate false everywhere; columns the page never
@@ -23,7 +26,8 @@ writes (b >= ceil(L/128)) are written as -inf.
 Pins (tests/test_oracle_scorer.py): a scalar brute force over single tokens
 and nibbles on tiny inputs; query_len 1 with a fully visible block gives the
 max of the dots; a fully masked block gives -inf; every score is >= each
-visible dot of its block and equal to one of them.
+visible dot of its block and equal to one of them. Per-token output: the
+same scalar brute force token by token; its block max equals the block score.
 """
 import numpy as np
 
@@ -76,4 +80,26 @@ def nvfp4_index_score(q_codes, pages, block_table, seq_lens, query_len: int,
                 if hi > lo:
                     res[:, qoff, b] = dots[:, qoff, lo:hi].max(axis=1)
         out[:, rows] = res
+    return out
+
+
+def nvfp4_index_score_per_token(q_codes, pages, block_table, seq_lens, query_len: int,
+                                num_cols: int, reqs=None) -> np.ndarray:
+    """Per-token scores [H, R*QL, num_cols] (float64): column t holds
+    dot[h, row, t] where token t is visible to the row (t < L and
+    t <= L - QL + qoff), else -inf. The block score above is the max of these
+    columns over a block. ``reqs`` as for nvfp4_index_score."""
+    R = seq_lens.shape[0]
+    H = q_codes.shape[1]
+    out = np.full((H, R * query_len, num_cols), np.nan)
+    if reqs is None:
+        reqs = range(R)
+    for r in reqs:
+        L = int(seq_lens[r])
+        dots = nvfp4_token_dots(q_codes, pages, block_table, seq_lens, query_len, r)
+        res = np.full((H, query_len, num_cols), -np.inf)
+        for qoff in range(query_len):
+            n = max(0, min(L - query_len + qoff + 1, L, num_cols))   # visible tokens 0 .. n-1
+            res[:, qoff, :n] = dots[:, qoff, :n]
+        out[:, r * query_len:(r + 1) * query_len] = res
     return out

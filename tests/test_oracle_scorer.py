@@ -27,9 +27,12 @@ def _scalar_e4m3(b):
     return s * (8 + m) * 2.0 ** (e - 10)
 
 
-def _brute(c):
-    """Token-by-token, nibble-by-nibble scalar scoring."""
+def _brute(c, per_token_cols=None):
+    """Token-by-token, nibble-by-nibble scalar scoring; with per_token_cols,
+    the per-token dots in that many columns instead of the block max."""
     R, QL, H, S = c.num_reqs, c.query_len, c.num_heads, c.num_cols
+    if per_token_cols is not None:
+        S = per_token_cols
     out = [[[-math.inf] * S for _ in range(R * QL)] for _ in range(H)]
     for r in range(R):
         L = int(c.seq_lens[r])
@@ -47,6 +50,10 @@ def _brute(c):
                 row = r * QL + qoff
                 for h in range(H):
                     dot = sum(_scalar_e4m3(int(c.q_codes[row, h, d])) * k[d] for d in range(128))
+                    if per_token_cols is not None:
+                        if t < S:
+                            out[h][row][t] = dot
+                        continue
                     b = t // 128
                     if b < S and dot > out[h][row][b]:
                         out[h][row][b] = dot
@@ -123,3 +130,26 @@ def test_tail_poison_ignored():
     c = synth.make_idx_case(7, [200], query_len=4, num_heads=2, num_cols=2)
     s = _run(c)
     assert not np.any(np.isnan(s))
+
+
+# ---- per-token output
+@pytest.mark.parametrize("lens,cols", [([130], 200), ([3, 257], 300), ([5], 2)])
+def test_per_token_brute_force_tiny(lens, cols):
+    c = synth.make_idx_case(41, lens, query_len=4, num_heads=2, num_cols=4)
+    ref = _brute(c, per_token_cols=cols)
+    got = oracle.nvfp4_index_score_per_token(c.q_codes, c.pages, c.block_table, c.seq_lens, 4, cols)
+    assert np.array_equal(np.isinf(ref), np.isinf(got))
+    fin = np.isfinite(ref)
+    assert np.max(np.abs(got[fin] - ref[fin]) / np.maximum(np.abs(ref[fin]), 1.0)) < 1e-12
+
+
+def test_per_token_block_max_is_block_score():
+    c = synth.make_idx_case(43, [1, 127, 128, 129, 700, 1000], query_len=3, num_heads=2, num_cols=8)
+    blk = oracle.nvfp4_index_score(c.q_codes, c.pages, c.block_table, c.seq_lens, 3, 8)
+    tok = oracle.nvfp4_index_score_per_token(c.q_codes, c.pages, c.block_table, c.seq_lens, 3, 8 * 128)
+    assert np.array_equal(tok.reshape(2, -1, 8, 128).max(axis=3), blk)
+    # visible columns per row: min(L - QL + qoff + 1, L), never negative
+    for r, L in enumerate(c.seq_lens.tolist()):
+        for qoff in range(3):
+            n = int(np.isfinite(tok[0, 3 * r + qoff]).sum())
+            assert n == max(0, min(L - 3 + qoff + 1, L, 1024))
