@@ -337,16 +337,17 @@ def time_uq(c, P, steps, warmup, dev, q_haircut=False):
     return r
 
 
-def time_idx(c, steps, warmup, dev):
+def time_idx(c, steps, warmup, dev, per_token_cols=None):
     import torch
     import quantized_paged_attention_gb300 as qpa
     q = torch.from_numpy(c.q_codes).to(dev)
     pages = torch.from_numpy(c.pages).to(dev)
     bt = torch.from_numpy(c.block_table).to(dev)
     sl = torch.from_numpy(c.seq_lens).to(dev)
-    scores = torch.empty((c.num_heads, q.shape[0], c.num_cols), dtype=torch.float32, device=dev)
-    desc = qpa.idx_desc(q, pages, bt, c.query_len, c.num_cols, scores)
-    r = _time_loop(lambda: qpa.nvfp4_index_score(q, pages, bt, sl, c.query_len, c.num_cols, scores=scores,
+    cols = c.num_cols if per_token_cols is None else per_token_cols
+    scores = torch.empty((c.num_heads, q.shape[0], cols), dtype=torch.float32, device=dev)
+    desc = qpa.idx_desc(q, pages, bt, c.query_len, cols, scores, per_token=per_token_cols is not None)
+    r = _time_loop(lambda: qpa.nvfp4_index_score(q, pages, bt, sl, c.query_len, cols, scores=scores,
                                                  desc=desc), None, steps, warmup)
     if qpa.kernel_error() != 0:
         raise RuntimeError("device error word raised during the benchmark")
@@ -559,6 +560,17 @@ def main():
             "kv_bytes": ci.kv_bytes,
             "gbs": round(ci.kv_bytes / (i_ms * 1e-3) / 1e9, 1),
             "frac_of_peak": round(ci.kv_bytes / (i_ms * 1e-3) / 1e9 / peak, 4)}
+        t_ms, _ = time_idx(ci, esteps, a.warmup, dev, per_token_cols=32768)
+        t_ms = _max_over_ranks(t_ms)
+        out_bytes = ci.num_heads * ci.num_reqs * ci.query_len * 32768 * 4
+        extra["nvfp4_index_score_64req_per_token"] = {
+            "workload": "NVFP4 paged index scorer, 64 requests, lengths U[4096,32768], query_len 4, 2 heads, "
+                        "one score column per token (32768 columns)",
+            "us_per_step": round(t_ms * 1e3, 2), "l2": "flushed (256 MB write, then read) before every timed step",
+            "kv_bytes": ci.kv_bytes, "score_bytes_written": out_bytes,
+            "gbs_kv": round(ci.kv_bytes / (t_ms * 1e-3) / 1e9, 1),
+            "gbs_read_plus_written": round((ci.kv_bytes + out_bytes) / (t_ms * 1e-3) / 1e9, 1),
+            "frac_of_peak": round((ci.kv_bytes + out_bytes) / (t_ms * 1e-3) / 1e9 / peak, 4)}
         del ci
 
     cpu = None

@@ -274,6 +274,12 @@ int uq_decode_hd256_combine(int num_partitions, void* out, const qpa_uq_desc* d,
  * [0, num_cols) of every row is written: columns at or past ceil(L/128) get
  * -inf. No scale, weight or activation is applied to the dot.
  *
+ * flags (other bits: QPA_ERR_SHAPE):
+ *   QPA_IDX_PER_TOKEN  one column per token instead of per block, i.e. the
+ *       dots before the page max ([IDX] frag_max reduces them):
+ *           scores[h][r*query_len + qoff][t] = dot[t] if t <= L - query_len + qoff
+ *       (t < L follows), else -inf, for every t in [0, num_cols).
+ *
  * Layouts:
  *   q          uint8 (e4m3fn) [num_reqs*query_len][num_heads][128] with byte
  *              strides q_stride_tok / q_stride_head (multiples of 16)
@@ -282,13 +288,16 @@ int uq_decode_hd256_combine(int num_partitions, void* out, const qpa_uq_desc* d,
  *              the codes (64 per token, dim 2i in the low nibble of byte i),
  *              bytes 8192..9215 the e4m3 scales (8 per token, one per 16 dims)
  *   block_table int32 [num_reqs][max_blocks_per_seq]; only entries below
- *              min(ceil(L/128), num_cols) are read
+ *              min(ceil(L/128), num_cols) are read (per token:
+ *              min(ceil(L/128), ceil(num_cols/128)))
  *   seq_lens   int32 [num_reqs]
  *   scores     float32 [num_heads][num_reqs*query_len][num_cols] with element
  *              strides s_stride_head / s_stride_row (the last dim contiguous)
  * Supported: head_dim 128, query_len * num_heads <= 16.
  * Alignment: q and kv_pages 16-byte aligned, scores 4-byte aligned.
  * ====================================================================== */
+#define QPA_IDX_PER_TOKEN 1
+
 typedef struct qpa_idx_desc {
   int32_t num_reqs;
   int32_t query_len;
@@ -296,8 +305,8 @@ typedef struct qpa_idx_desc {
   int32_t head_dim;         /* 128 */
   int32_t num_blocks;
   int32_t max_blocks_per_seq;
-  int32_t num_cols;         /* S: score columns per row */
-  int32_t reserved;
+  int32_t num_cols;         /* S: score columns per row (blocks, or tokens with QPA_IDX_PER_TOKEN) */
+  int32_t flags;            /* 0 or QPA_IDX_PER_TOKEN */
   int64_t page_stride;      /* bytes; 0 = 9216 */
   int64_t q_stride_tok;     /* bytes; 0 = num_heads*128 */
   int64_t q_stride_head;    /* bytes; 0 = 128 */

@@ -22,6 +22,7 @@ QPA_OUT_BF16 = 1
 QPA_UQ_UE8M0_SCALES = 1
 QPA_UQ_Q_HAIRCUT = 2
 QPA_UQ_ROT_PERM = 4
+QPA_IDX_PER_TOKEN = 1
 _lib = None
 
 
@@ -60,7 +61,7 @@ class IdxDesc(ctypes.Structure):
     _fields_ = [("num_reqs", ctypes.c_int32), ("query_len", ctypes.c_int32),
                 ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
-                ("num_cols", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("num_cols", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("page_stride", ctypes.c_int64), ("q_stride_tok", ctypes.c_int64),
                 ("q_stride_head", ctypes.c_int64), ("s_stride_head", ctypes.c_int64),
                 ("s_stride_row", ctypes.c_int64)]
@@ -349,7 +350,8 @@ def uq_decode_hd256_combine(num_partitions, out, desc, workspace, stream=None):
 
 
 # --------------------------------------------------------------------- nvfp4 index scorer
-def idx_desc(q_codes, pages, block_table, query_len, num_cols, scores=None):
+def idx_desc(q_codes, pages, block_table, query_len, num_cols, scores=None, per_token=False):
+    """num_cols counts blocks, or tokens with per_token (one column per token)."""
     RQ, H, D = q_codes.shape
     assert D == 128 and RQ % query_len == 0
     d = IdxDesc()
@@ -359,20 +361,22 @@ def idx_desc(q_codes, pages, block_table, query_len, num_cols, scores=None):
     d.q_stride_tok, d.q_stride_head = q_codes.stride(0), q_codes.stride(1)
     if scores is not None:
         d.s_stride_head, d.s_stride_row = scores.stride(0), scores.stride(1)
+    d.flags = QPA_IDX_PER_TOKEN if per_token else 0
     return d
 
 
 def nvfp4_index_score(q_codes, pages, block_table, seq_lens, query_len: int, num_cols: int, scores=None,
-                      stream=None, desc=None):
+                      stream=None, desc=None, per_token=False):
     """Paged NVFP4 index scores. q_codes uint8 (e4m3) [R*QL, H, 128]; pages
-    uint8 [NB, 9216]; returns float32 scores [H, R*QL, num_cols]."""
+    uint8 [NB, 9216]; returns float32 scores [H, R*QL, num_cols] (columns are
+    blocks, or tokens with per_token)."""
     lib = load_library()
     _need_cuda(q_codes, pages, block_table, seq_lens, scores)
     if scores is None:
         scores = torch.empty((q_codes.shape[1], q_codes.shape[0], num_cols), dtype=torch.float32,
                              device=q_codes.device)
     if desc is None:
-        desc = idx_desc(q_codes, pages, block_table, query_len, num_cols, scores)
+        desc = idx_desc(q_codes, pages, block_table, query_len, num_cols, scores, per_token)
     st = lib.nvfp4_index_score(_ptr(q_codes), _ptr(pages), _ptr(block_table), _ptr(seq_lens), _ptr(scores),
                                ctypes.byref(desc), _stream(stream))
     _check("nvfp4_index_score", st)

@@ -8,7 +8,9 @@
 //    scales after PAGE_CODES);
 //  * row qoff of request r sees tokens t <= L - QL + qoff (score_cgs limits);
 //  * the score of a block is the max of its column over the page (frag_max);
-//    blocks past the end of the request are written as -inf.
+//    blocks past the end of the request are written as -inf. A flag keeps
+//    the dots before that max instead: one column per token, -inf where the
+//    token is not visible.
 //
 // GB300 design:
 //  * persistent CTAs of 4 warps; the (request, block) pages are split into
@@ -52,11 +54,12 @@ struct IdxParams {
   long long q_stride_tok, q_stride_head;  // bytes
   long long s_stride_head, s_stride_row;  // elements
   int num_reqs, query_len, num_heads, max_blocks, num_cols, num_blocks;
+  int per_token;    // one column per token instead of the block max
 };
 
 enum : int { IEV_NONE = 0, IEV_ITEM = 1, IEV_HALF = 2 };
 
-template <int NT>
+template <int NT, bool PER_TOKEN>
 __global__ void __launch_bounds__(idx::THREADS, idx::CTAS_PER_SM)
 idx_score_kernel(const IdxParams p) {
   using namespace idx;
@@ -67,17 +70,27 @@ idx_score_kernel(const IdxParams p) {
   const int rows = QL * H;
   const uint64_t pol = policy_evict_first();
   const uint32_t ring = smem_u32(smem) + warp * DEPTH * SLOT_BYTES;
-  auto nblocks = [&](int L) { return min((max(L, 0) + BLK - 1) / BLK, S); };
+  const int col_blocks = PER_TOKEN ? (S + BLK - 1) / BLK : S;   // blocks that own a column
+  auto nblocks = [&](int L) { return min((max(L, 0) + BLK - 1) / BLK, col_blocks); };
+  const long long GW = (long long)gridDim.x * NW;
+  const long long gw = (long long)blockIdx.x * NW + warp;
 
   // ---- columns past each request's last block (and every column when L <= 0)
-  // are -inf; CTA c fills the requests c, c + gridDim.x, ...
-  for (int r = blockIdx.x; r < R; r += gridDim.x) {
-    const int nb = nblocks(__ldg(p.seq_lens + r));
-    const int cells = (S - nb) * rows;
-    for (int i = threadIdx.x; i < cells; i += THREADS) {
-      const int b = nb + i % (S - nb), n = i / (S - nb);
-      const int qoff = n / H, h = n % H;
-      p.scores[h * p.s_stride_head + (long long)(r * QL + qoff) * p.s_stride_row + b] = -INFINITY;
+  // are -inf: units (request, row, 1024-column chunk) spread over all warps,
+  // a warp's lanes on consecutive columns
+  {
+    constexpr int CH = 1024;
+    const int chunks = (S + CH - 1) / CH;
+    const long long fill_units = (long long)R * rows * chunks;
+    for (long long u = gw; u < fill_units; u += GW) {
+      const int ch = (int)(u % chunks);
+      const long long rn = u / chunks;
+      const int n = (int)(rn % rows), r = (int)(rn / rows);
+      const int nb = nblocks(__ldg(p.seq_lens + r));
+      const int col0 = max(min(PER_TOKEN ? nb * BLK : nb, S), ch * CH);
+      const int col1 = min(S, (ch + 1) * CH);
+      float* row = p.scores + (n % H) * p.s_stride_head + (long long)(r * QL + n / H) * p.s_stride_row;
+      for (int col = col0 + lane; col < col1; col += 32) row[col] = -INFINITY;
     }
   }
 
@@ -90,8 +103,6 @@ idx_score_kernel(const IdxParams p) {
     for (int sh = 16; sh; sh >>= 1) nb += __shfl_xor_sync(0xffffffffu, nb, sh);
     U += nb;
   }
-  const long long GW = (long long)gridDim.x * NW;
-  const long long gw = (long long)blockIdx.x * NW + warp;
   const long long u0 = U * gw / GW, u1 = U * (gw + 1) / GW;
   // locate u0: request r_cur with prefix(r_cur) <= u0 < prefix(r_cur + 1)
   int r_cur = 0, b_cur = 0, L_cur = 0;
@@ -267,11 +278,20 @@ idx_score_kernel(const IdxParams p) {
           const int lim = last0 + n / H;
           const float va = ta <= lim ? acc[nt][hh] : -INFINITY;
           const float vb = tb <= lim ? acc[nt][2 + hh] : -INFINITY;
-          mx[nt][hh] = fmaxf(mx[nt][hh], fmaxf(va, vb));
+          if constexpr (PER_TOKEN) {
+            // 8 lanes of equal c write 8 consecutive tokens of one row
+            if (n < rows) {
+              float* row = p.scores + (n % H) * p.s_stride_head + (long long)(er * QL + n / H) * p.s_stride_row;
+              if (ta < S) row[ta] = va;
+              if (tb < S) row[tb] = vb;
+            }
+          } else {
+            mx[nt][hh] = fmaxf(mx[nt][hh], fmaxf(va, vb));
+          }
         }
       }
     }
-    if (half == 1) {
+    if (!PER_TOKEN && half == 1) {
       // block done: reduce over the 8 token lanes and store
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -311,14 +331,18 @@ cudaError_t launch_idx_score(const IdxLaunch& a, cudaStream_t stream) {
   p.max_blocks = a.max_blocks;
   p.num_cols = a.num_cols;
   p.num_blocks = a.num_blocks;
+  p.per_token = a.per_token;
   if (a.num_reqs <= 0 || a.num_cols <= 0) return cudaSuccess;
   const int grid = idx::CTAS_PER_SM * a.num_sms;
-  if (a.query_len * a.num_heads <= 8) {
-    cudaFuncSetAttribute(idx_score_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, idx::SMEM);
-    idx_score_kernel<1><<<grid, idx::THREADS, idx::SMEM, stream>>>(p);
+  auto launch = [&](auto kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, idx::SMEM);
+    kernel<<<grid, idx::THREADS, idx::SMEM, stream>>>(p);
+  };
+  const bool two = a.query_len * a.num_heads > 8;
+  if (a.per_token) {
+    if (two) launch(idx_score_kernel<2, true>); else launch(idx_score_kernel<1, true>);
   } else {
-    cudaFuncSetAttribute(idx_score_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, idx::SMEM);
-    idx_score_kernel<2><<<grid, idx::THREADS, idx::SMEM, stream>>>(p);
+    if (two) launch(idx_score_kernel<2, false>); else launch(idx_score_kernel<1, false>);
   }
   return cudaGetLastError();
 }

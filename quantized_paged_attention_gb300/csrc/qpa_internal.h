@@ -86,6 +86,7 @@ struct IdxLaunch {
   long long page_stride, q_stride_tok, q_stride_head;   // bytes
   long long s_stride_head, s_stride_row;                // elements
   int num_reqs, query_len, num_heads, max_blocks, num_cols, num_blocks;
+  int per_token;    // one column per token (QPA_IDX_PER_TOKEN)
   int num_sms;
 };
 

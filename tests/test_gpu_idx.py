@@ -68,3 +68,44 @@ def test_full_config_sampled():
     ref = _ref(c, reqs=reqs)
     rows = [r * 4 + q for r in reqs for q in range(4)]
     check_scores(got, ref, rows=rows, what="idx-full")
+
+
+# ---- per-token output
+def _ref_tok(c, cols, reqs=None):
+    return oracle.nvfp4_index_score_per_token(c.q_codes, c.pages, c.block_table, c.seq_lens, c.query_len, cols,
+                                              reqs=reqs)
+
+
+@pytest.mark.parametrize("ql,h", [(4, 2), (1, 1), (3, 4)])
+@pytest.mark.parametrize("cols", [1536, 1000, 77])
+def test_per_token_small_ragged(ql, h, cols):
+    """Token columns past the table (1536 > 12 blocks), ending inside a block
+    (1000) and short of most requests (77)."""
+    lens = [0, 1, 3, 4, 5, 127, 128, 129, 255, 256, 257, 1000]
+    c = synth.make_idx_case(330 + ql * 10 + h, lens, query_len=ql, num_heads=h, num_cols=12)
+    got = IdxDev(c).run(per_token_cols=cols).cpu().double().numpy()
+    check_scores(got, _ref_tok(c, cols), what=f"per-token ql={ql} h={h} cols={cols}")
+
+
+def test_per_token_strided_and_block_max():
+    c = synth.make_idx_case(340, [500, 40, 1300], query_len=4, num_heads=2, num_cols=11)
+    d = IdxDev(c)
+    big = torch.full((2, 12, 1500), 7.0, device=d.q.device)
+    view = big[:, :, :1408]
+    d.run(scores=view, per_token_cols=1408)
+    got = big.cpu().double().numpy()
+    check_scores(got[:, :, :1408], _ref_tok(c, 1408), what="per-token strided")
+    assert np.all(got[:, :, 1408:] == 7.0)
+    blk = d.run().cpu().double().numpy()                 # the block max of the same dots
+    assert np.array_equal(got[:, :, :1408].reshape(2, 12, 11, 128).max(axis=3), blk)
+
+
+def test_per_token_full_config_sampled():
+    """64 requests, lengths U[4096, 32768], query_len 4, 2 heads, 32768 token
+    columns; 4 requests (incl. the shortest and longest) against the oracle."""
+    c = synth.idx_full()
+    got = IdxDev(c).run(per_token_cols=32768).cpu().double().numpy()
+    assert not np.any(np.isnan(got))
+    reqs = sorted({3, 40, int(np.argmin(c.seq_lens)), int(np.argmax(c.seq_lens))})
+    rows = [r * 4 + q for r in reqs for q in range(4)]
+    check_scores(got, _ref_tok(c, 32768, reqs=reqs), rows=rows, what="idx-full per-token")
