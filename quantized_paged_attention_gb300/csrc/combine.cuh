@@ -1,10 +1,11 @@
 // Flash-combine of split-KV partials for one query row (the [PA] page's
 // cross-partition reduce): M = max_p m_p, w_p = l_p exp(m_p - M),
-// o = sum_p w_p O_p / sum_p w_p. An empty partition (m_p = -inf) has weight
-// exactly 0; the exponent argument is clamped so no NaN can arise.
+// o = sum_p w_p O_p / sum_p w_p. An empty partition (m_p = -inf or l_p = 0)
+// has weight exactly 0 and its O is never read, so it need not be written;
+// the exponent argument is clamped so no NaN can arise.
 //
-// One CTA per row. The first chunk of O loads and all (m, l) loads are
-// issued before any dependent work.
+// One CTA per row: all (m, l) loads first, then the O loads of the
+// partitions with a nonzero weight, all issued before any dependent work.
 #pragma once
 #include "common.cuh"
 
@@ -44,12 +45,6 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
   // rbase = ((seq * Hk + kvh) * P) * qg + r: partition pp of the row is at rbase + pp * qg
   const float* ob = part_o + rbase * D + 4 * v4;
   const long long pstride = (long long)qg * D;
-  float4 o[KMAX];
-#pragma unroll
-  for (int k = 0; k < KMAX; ++k) {
-    const int pp = sub + k * nsub;
-    o[k] = pp < P ? __ldg(reinterpret_cast<const float4*>(ob + pp * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   for (int pp = tid; pp < P; pp += blockDim.x) {
     ms[pp] = part_m[rbase + (long long)pp * qg];
     ls[pp] = part_l[rbase + (long long)pp * qg];
@@ -70,27 +65,18 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
   for (int sh = 16; sh; sh >>= 1) den += __shfl_xor_sync(0xffffffffu, den, sh);
   const float inv = den > 0.f ? 1.f / den : 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int k = 0; k < KMAX; ++k) {
-    const int pp = sub + k * nsub;
-    if (pp < P) {
-      const float w = weight(pp);
-      acc.x += w * o[k].x; acc.y += w * o[k].y; acc.z += w * o[k].z; acc.w += w * o[k].w;
-    }
-  }
-  for (int base = KMAX * nsub; base < P; base += KMAX * nsub) {
+  for (int base = 0; base < P; base += KMAX * nsub) {
+    float w[KMAX];
+    float4 o[KMAX];
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) {
       const int pp = base + sub + k * nsub;
-      o[k] = pp < P ? __ldg(reinterpret_cast<const float4*>(ob + pp * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[k] = pp < P ? weight(pp) : 0.f;
+      o[k] = w[k] != 0.f ? __ldg(reinterpret_cast<const float4*>(ob + pp * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) {
-      const int pp = base + sub + k * nsub;
-      if (pp < P) {
-        const float w = weight(pp);
-        acc.x += w * o[k].x; acc.y += w * o[k].y; acc.z += w * o[k].z; acc.w += w * o[k].w;
-      }
+      acc.x += w[k] * o[k].x; acc.y += w[k] * o[k].y; acc.z += w[k] * o[k].z; acc.w += w[k] * o[k].w;
     }
   }
   part[tid] = acc;

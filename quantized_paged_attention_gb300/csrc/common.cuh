@@ -9,7 +9,7 @@ namespace qpa {
 
 // Error word raised by a kernel that gave up waiting or met an invalid block
 // id (the library's only device-side state). 0 = no error.
-enum : int { KERR_NONE = 0, KERR_TIMEOUT_FULL = 1, KERR_TIMEOUT_EMPTY = 2, KERR_BAD_BLOCK = 3 };
+enum : int { KERR_NONE = 0, KERR_TIMEOUT_FULL = 1, KERR_TIMEOUT_EMPTY = 2, KERR_BAD_BLOCK = 3, KERR_SCHEDULE = 4 };
 extern __device__ int g_kernel_error;
 
 // Any wait gives up after this many nanoseconds and reports an error rather

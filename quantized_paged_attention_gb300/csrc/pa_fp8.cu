@@ -61,7 +61,7 @@ struct Smem {
   static constexpr int redOff = cOff + 2 * R * 4;          // [2][4][R] tile maxima per warp
   static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][4 NWG][R] row sums per warp
   static constexpr int msmOff = lredOff + 2 * 4 * NWG * R * 4;   // [2][NWG][R] row maxima per group
-  static constexpr int infoOff = msmOff + 2 * NWG * R * 4; // [2] {item, L, tiles, partition}
+  static constexpr int infoOff = msmOff + 2 * NWG * R * 4; // [2] {item row, L, tiles, first tile group}
   static constexpr int barOff = (infoOff + 2 * 16 + 7) & ~7;
   static constexpr int NBAR = 2 * NS + 2 * 10 + 4 + 1;
   static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag, QK total
@@ -85,17 +85,6 @@ struct Fp8Params {
   int num_seqs, num_kv_heads, qg, block_size, log2_bs, num_blocks, max_blocks, num_partitions;
   float softmax_scale;
 };
-
-// Tiles of an item: partition `part` owns tile groups part, part+P, ...; each
-// tile group is two 128-token tiles, the second absent when it starts at or
-// past the length.
-__device__ __forceinline__ int item_tiles(int part, int P, int L) {
-  if (part * fp8::TG >= L) return 0;
-  const int ntg_seq = (L + fp8::TG - 1) / fp8::TG;
-  const int ntg = (ntg_seq - 1 - part) / P + 1;
-  const int last = part + (ntg - 1) * P;
-  return 2 * ntg - ((last * fp8::TG + fp8::TILE < L) ? 0 : 1);
-}
 
 template <int NT>
 __global__ void __launch_bounds__(fp8::Smem<NT>::THREADS, 1)
@@ -171,16 +160,10 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 
   const int P = p.num_partitions;
   const int Hk = p.num_kv_heads;
-  const int num_items = p.num_seqs * Hk * P;
   const int G = gridDim.x;
   const int bs = p.block_size;
   const int lbs = p.log2_bs;
   const int bpt = TG / bs;                  // table entries per tile group
-  auto load_len = [&](int item) -> int {
-    if (item >= num_items) return 0;
-    const int seq = item / (P * Hk);
-    return max(0, min(__ldg(p.seq_lens + seq), p.max_blocks * bs));
-  };
 
   if (warp < WARP_PROD0) {
     // ======================================================== softmax warps
@@ -235,7 +218,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&qempty[qb]);
-      const int item = inf.x, L = inf.y, nt = inf.z, part = inf.w;
+      const int item = inf.x, L = inf.y, nt = inf.z, tg0 = inf.w;   // tiles of tile groups tg0, tg0 + 1, ...
       if (nt == 0) break;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -244,7 +227,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       }
       for (int i = 0; i < nt; ++i, ++j) {
         if (NWG == 2 && (j & 1) != wg) continue;
-        const int start = (part + (i >> 1) * P) * TG + (i & 1) * TILE;
+        const int start = (tg0 + (i >> 1)) * TG + (i & 1) * TILE;
         const int b = j & 1;                 // S buffer
         const int ob = 2 * b + ((j >> 1) & 1);   // P' and O buffer (alternate per group)
         // ---- softmax of tile j
@@ -450,12 +433,11 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     int j = 0, qcnt = 0;
     bool ok = true;
 
-    auto load_q = [&](int item, uint4 (&qv)[NT]) {
+    auto seq_len = [&](int sq) -> int { return max(0, min(__ldg(p.seq_lens + sq), p.max_blocks * bs)); };
+    auto load_q = [&](int seq, int kvh, uint4 (&qv)[NT]) {
 #pragma unroll
       for (int h = 0; h < NT; ++h) qv[h] = make_uint4(0, 0, 0, 0);
-      if (item >= num_items) return;
-      const int t2 = item / P;
-      const int kvh = t2 % Hk, seq = t2 / Hk;
+      if (seq < 0) return;
 #pragma unroll
       for (int h = 0; h < NT; ++h) {
         const int row = qrow + 8 * h;
@@ -464,57 +446,139 @@ pa_fp8_partition_kernel(const Fp8Params p) {
                                                        (long long)(kvh * p.qg + row) * p.q_stride_head) + h16);
       }
     };
-    auto load_entries = [&](int item, int tg) -> int32_t {
-      if (item >= num_items) return 0;
-      const int seq = item / (P * Hk);
+    auto load_entries = [&](int seq, int tg) -> int32_t {
+      if (seq < 0) return 0;
       const int e = tg * bpt + lane;
       return (lane < bpt && e < p.max_blocks) ? __ldg(p.block_table + (long long)seq * p.max_blocks + e) : 0;
     };
 
-    // ---- this CTA's items: round-robin over the items in (sequence, partition,
-    // kv head) order, so that the CTAs working at the same time read all heads
-    // of the same pages. Empty partitions (starting past the length) get zero
-    // partials right away.
-    auto seq_len = [&](int sq) -> int { return max(0, min(__ldg(p.seq_lens + sq), p.max_blocks * bs)); };
-    auto item_of = [&](int k) -> int {      // k-th item in (sequence, partition, kv head) order
-      const int sq = k / (P * Hk), rem = k - sq * (P * Hk);
-      const int part = rem / Hk, kvh = rem - part * Hk;
-      return (sq * Hk + kvh) * P + part;
-    };
-    uint4 qv[NT];
-    int32_t ent0 = 0;
-    int L = 0;
-    if ((int)blockIdx.x < num_items) {
-      const int it0 = item_of(blockIdx.x);
-      L = seq_len(it0 / (P * Hk));
-      load_q(it0, qv);
-      ent0 = load_entries(it0, it0 % P);
+    // ---- schedule. One KV head's work is its sequences' tile groups in
+    // sequence order, W = sum_s ceil(L_s / TG) of them. The CTAs form groups of
+    // Hk, one CTA per head, and the NGe groups split W into equal contiguous
+    // ranges: the Hk CTAs of a group stream the same pages at the same time,
+    // and every CTA gets the same number of tile groups (+-1) in a handful of
+    // items. An item is the part of one (sequence, head) inside a range; its
+    // softmax state goes to slot c of the (sequence, head), c = its range
+    // minus the range of the sequence's first tile group. NGe is bounded so
+    // that no sequence meets more than P ranges; with P = 1 sequences stay
+    // whole and belong to the range of their first tile group. Slots without
+    // an item get (m, l) = (-inf, 0) and no O.
+    const int B = p.num_seqs;
+    long long W = 0;
+    int Tmax = 0;
+    for (int s0 = 0; s0 < B; s0 += 32) {
+      const int T = s0 + lane < B ? (seq_len(s0 + lane) + TG - 1) / TG : 0;
+      W += (long long)__reduce_add_sync(0xffffffffu, (unsigned)T);
+      Tmax = max(Tmax, __reduce_max_sync(0xffffffffu, T));
     }
-    for (int k = blockIdx.x; k < num_items && ok; k += G) {
-      const int item = item_of(k);
-      const int part = item % P;
-      const int kvh = (item / P) % Hk;
-      const int nt = item_tiles(part, P, L);
-      // next item's length, query rows and first table entries
-      int Lnext = 0;
-      uint4 qn[NT];
+    int NG, g, h_first, h_step;
+    if (G >= Hk) {
+      NG = G / Hk; g = blockIdx.x / Hk; h_first = blockIdx.x % Hk; h_step = Hk;
+    } else {
+      NG = 1; g = 0; h_first = blockIdx.x; h_step = G;
+    }
+    long long NGe = NG;
+    if (P >= 2 && W > 0) {
+      // ranges of at least ceil(Tmax / max(1, P - 2)) tile groups: a sequence of
+      // T <= Tmax tile groups then meets at most P of them
+      const int den = max(1, P - 2);
+      const long long rreq = (Tmax + den - 1) / den;
+      NGe = max(1LL, min((long long)NG, W / rreq));
+    }
+    const bool active = W > 0 && g < NGe;
+    const long long rs = active ? W * g / NGe : 0, re = active ? W * (g + 1) / NGe : 0;
+    auto range_of = [&](long long x) -> long long { return ((x + 1) * NGe + W - 1) / W - 1; };
+
+    // first sequence of the range: P >= 2, the one holding tile group rs;
+    // P = 1, the first one starting at or after rs
+    int s_first = B;
+    long long off_first = 0;
+    if (active) {
+      long long base = 0;
+      for (int s0 = 0; s0 < B; s0 += 32) {
+        const int sq = s0 + lane;
+        const int T = sq < B ? (seq_len(sq) + TG - 1) / TG : 0;
+        int incl = T;
 #pragma unroll
-      for (int h = 0; h < NT; ++h) qn[h] = make_uint4(0, 0, 0, 0);
-      int32_t ent0n = 0;
-      if (k + G < num_items) {
-        const int itn = item_of(k + G);
-        Lnext = seq_len(itn / (P * Hk));
-        load_q(itn, qn);
-        ent0n = load_entries(itn, itn % P);
-      }
-      if (nt == 0) {
-        const long long row0 = (long long)item * p.qg;
-        for (int r = 0; r < p.qg; ++r) p.part_o[(row0 + r) * D + pt] = 0.f;
-        if (pt < p.qg) {
-          p.part_m[row0 + pt] = -INFINITY;
-          p.part_l[row0 + pt] = 0.f;
+        for (int sh = 1; sh < 32; sh <<= 1) {
+          const int t2 = __shfl_up_sync(0xffffffffu, incl, sh);
+          if (lane >= sh) incl += t2;
         }
+        const long long lo = base + incl - T, hi = base + incl;
+        const unsigned hit = __ballot_sync(0xffffffffu, sq < B && T > 0 && (P >= 2 ? hi > rs : lo >= rs));
+        if (hit) {
+          const int src = __ffs(hit) - 1;
+          s_first = s0 + src;
+          off_first = __shfl_sync(0xffffffffu, lo, src);
+          break;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+
+    // (sequence, head) pairs with no tokens: every slot empty
+    for (int pr = blockIdx.x; pr < B * Hk; pr += G) {
+      if (seq_len(pr / Hk) == 0) {
+        const long long rb = (long long)pr * P * p.qg;
+        for (int i = pt; i < P * p.qg; i += 128) {
+          p.part_m[rb + i] = -INFINITY;
+          p.part_l[rb + i] = 0.f;
+        }
+      }
+    }
+
+    // the range's items in order: sequences with tokens whose offset lies
+    // below re, then the same walk for the CTA's next head (only when G < Hk)
+    struct Cur { int s, h, L; long long off; };
+    auto walk = [&](int sq, long long off, int h) -> Cur {
+      while (true) {
+        while (sq < B && off < re) {
+          const int L = seq_len(sq);
+          if (L > 0) return Cur{sq, h, L, off};
+          ++sq;                                   // no tile groups: the offset stays
+        }
+        h += h_step;
+        if (h >= Hk || s_first >= B) return Cur{-1, h, 0, 0};
+        sq = s_first;
+        off = off_first;
+      }
+    };
+    auto first_tg = [&](const Cur& c) -> int { return P >= 2 ? (int)(max(rs, c.off) - c.off) : 0; };
+
+    Cur cur = active && s_first < B ? walk(s_first, off_first, h_first) : Cur{-1, 0, 0, 0};
+    uint4 qv[NT];
+    load_q(cur.s, cur.h, qv);
+    int32_t ent0 = load_entries(cur.s, cur.s >= 0 ? first_tg(cur) : 0);
+    while (cur.s >= 0 && ok) {
+      const int T = (cur.L + TG - 1) / TG;
+      int tg_b = 0, tg_e = T, slot = 0, nc = 1;
+      if (P >= 2) {
+        tg_b = first_tg(cur);
+        tg_e = (int)(min(re, cur.off + T) - cur.off);
+        const long long r0 = range_of(cur.off);
+        slot = (int)(g - r0);
+        nc = (int)(range_of(cur.off + T - 1) - r0 + 1);
+      }
+      const int L = cur.L;
+      const int kvh = cur.h;
+      const int nt = 2 * (tg_e - tg_b) - (((tg_e - 1) * TG + TILE < L) ? 0 : 1);
+      const int item = (cur.s * Hk + kvh) * P + slot;
+      // next item's query rows and first table entries
+      const Cur nxt = walk(cur.s + 1, cur.off + T, cur.h);
+      uint4 qn[NT];
+      load_q(nxt.s, nxt.h, qn);
+      const int32_t ent0n = load_entries(nxt.s, nxt.s >= 0 ? first_tg(nxt) : 0);
+      if (slot < 0 || slot >= nc || nc > P || tg_b >= tg_e) {
+        // cannot happen with the bound on NGe; never publish a bad slot
+        if (lane == 0) atomicExch(&g_kernel_error, KERR_SCHEDULE);
       } else {
+        if (slot == 0 && nc < P) {
+          const long long rb = ((long long)(cur.s * Hk + kvh) * P + nc) * p.qg;
+          for (int i = pt; i < (P - nc) * p.qg; i += 128) {
+            p.part_m[rb + i] = -INFINITY;
+            p.part_l[rb + i] = 0.f;
+          }
+        }
         // ---- query operand: 4 e4m3 terms of q 2^a (a per row: max |q| 2^a in [128, 256))
         const int qb = qcnt & 1;
         if (qcnt >= 2 && !warp_wait(&qempty[qb], ((qcnt >> 1) - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) {
@@ -565,7 +629,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           }
           if (h16 == 0) stsf(cbuf_s + 4 * (qb * R + row), row < p.qg ? base_scale * down : 0.f);
         }
-        if (pt == 0) sts_i4(info_s + 16 * qb, make_int4(item, L, nt, part));
+        if (pt == 0) sts_i4(info_s + 16 * qb, make_int4(item, L, nt, tg_b));
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(&qfull[qb]);
@@ -575,10 +639,10 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         const size_t kvh_off = size_t(kvh) * head_bytes;
         int32_t ent = ent0, nent = 0;
         for (int i = 0; i < nt; ++i) {
-          const int tg = part + (i >> 1) * P;
+          const int tg = tg_b + (i >> 1);
           if ((i & 1) == 0) {
             if (i > 0) ent = nent;
-            nent = (i + 2 < nt) ? load_entries(item, tg + P) : 0;
+            nent = (i + 2 < nt) ? load_entries(cur.s, tg + 1) : 0;
           }
           const int s = j % NS;
           const int rnd = j / NS;
@@ -613,7 +677,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           ++j;
         }
       }
-      L = Lnext;
+      cur = nxt;
 #pragma unroll
       for (int h = 0; h < NT; ++h) qv[h] = qn[h];
       ent0 = ent0n;

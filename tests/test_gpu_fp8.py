@@ -35,25 +35,56 @@ def test_tiny_config():
     _check(c, out.cpu().double().numpy(), what="tiny")
 
 
-def test_tiny_partials_match_oracle_partitions():
+def _check_slots_cover(c, O, m, l, s, h, P, what):
+    """The slots of (sequence s, head h) hold the softmax states of
+    consecutive runs of 256-token tile groups that cover the sequence, in slot
+    order; every other slot is empty (m = -inf, l = 0)."""
+    QG = c.query_group
+    L = int(c.seq_lens[s])
+    q = oracle.decode_bf16(c.q_bits)[s, h * QG:(h + 1) * QG]
+    k, v = dense_kv_fp8(c.kv_cache, c.block_table, s, h, L, c.k_scale, c.v_scale)
+    T = -(-L // 256)
+    live = [pp for pp in range(P) if l[s, h, pp].max() > 0]
+    for pp in range(P):
+        if pp not in live:
+            assert np.all(np.isneginf(m[s, h, pp])) and np.all(l[s, h, pp] == 0), f"{what}: slot {pp} not empty"
+    vmax = float(np.abs(v).max()) if L else 0.0
+    b = 0
+    for idx, pp in enumerate(live):
+        ends = [T] if idx == len(live) - 1 else range(b + 1, T)
+        hit = None
+        for e in ends:
+            t1 = min(e * 256, L)
+            rm, rl, rO = partition_partials(q, k[b * 256:t1], v[b * 256:t1], c.softmax_scale, 1)
+            if np.max(np.abs(m[s, h, pp] - rm[0])) < 1e-3 and np.max(np.abs(l[s, h, pp] / rl[0] - 1)) < 2e-3:
+                hit = e
+                break
+        assert hit is not None, f"{what}: slot {pp} is no run of tile groups starting at {b}"
+        assert np.max(np.abs(O[s, h, pp] - rO[0])) <= 2e-3 * vmax, f"{what}: slot {pp} O"
+        b = hit
+    assert b == T, f"{what}: runs end at tile group {b} of {T}"
+
+
+def test_tiny_partials_cover_the_sequence():
     c = synth.fp8_tiny()
     P = 2
     out, ws, desc = Fp8Dev(c).run(P)
     O, m, l = [t.cpu().double().numpy() for t in qpa.fp8_workspace_views(ws, desc, P)]
-    q = oracle.decode_bf16(c.q_bits)
     for s in range(c.num_seqs):
-        L = int(c.seq_lens[s])
-        k, v = dense_kv_fp8(c.kv_cache, c.block_table, s, 0, L, c.k_scale, c.v_scale)
-        rm, rl, rO = partition_partials(q[s, :8], k, v, c.softmax_scale, P)
-        vmax = float(np.abs(v).max())
-        for p in range(P):
-            if np.isinf(rm[p]).all():
-                assert np.all(np.isneginf(m[s, 0, p])) and np.all(l[s, 0, p] == 0)
-                assert np.all(O[s, 0, p] == 0)
-                continue
-            assert np.max(np.abs(m[s, 0, p] - rm[p])) < 1e-3
-            assert np.max(np.abs(l[s, 0, p] / rl[p] - 1)) < 2e-3
-            assert np.max(np.abs(O[s, 0, p] - rO[p])) <= 2e-3 * vmax
+        _check_slots_cover(c, O, m, l, s, 0, P, "tiny")
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 7, 32])
+def test_partials_cover_ragged(P):
+    """Runs of tile groups per slot, on sequences of 0..9 tile groups, with
+    one to 32 slots."""
+    c = synth.make_fp8_case(70 + P, [0, 1, 255, 256, 257, 700, 1500, 2304, 40, 900], 2, 8)
+    out, ws, desc = Fp8Dev(c).run(P)
+    O, m, l = [t.cpu().double().numpy() for t in qpa.fp8_workspace_views(ws, desc, P)]
+    for s in range(c.num_seqs):
+        for h in range(2):
+            _check_slots_cover(c, O, m, l, s, h, P, f"P={P} seq {s} head {h}")
+    _check(c, out.cpu().double().numpy(), what=f"cover P={P}")
 
 
 @pytest.mark.parametrize("P", [1, 2, 3, 7, 32, 100, 300])
