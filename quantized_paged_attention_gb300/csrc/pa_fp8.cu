@@ -3,12 +3,21 @@
 //
 // What it computes follows the ROCm/FlyDSL PR #825 page ("perf(pa tile):
 // readable tile-programming PA decode kernel": per-tensor fp8 K/V, query
-// length 1, GQA, cross-CTA partition split and a parallel flash-combine
-// reduce) and the partition map of the ultraquant_decode_hd256 page (STEP F:
-// partition p owns the 256-token tile groups p, p+P, p+2P, ...).
+// length 1, GQA, cross-CTA split of a sequence and a parallel flash-combine
+// reduce), with 256-token tile groups as the split granule (the
+// ultraquant_decode_hd256 page, STEP F).
 //
 // GB300 design (not the pages' AMD design): one persistent CTA per SM with
 // three warp roles around the 5th-generation tensor core.
+//  * Work split: the CTAs form groups of Hk, one per KV head; the groups cut
+//    each head's tile groups (in sequence order) into equal contiguous
+//    ranges, so the CTAs of a group read the same pages together and every
+//    CTA gets the same number of tile groups in a few items. The part of a
+//    sequence inside one range is an item; its softmax state is one of the
+//    num_partitions slots of the (sequence, head) (slot = range index minus
+//    that of the sequence's first tile group), unused slots are marked empty,
+//    and the combine merges the slots. The page's own map (partition p owns
+//    tile groups p, p+P, ...) gives many short items on ragged batches.
 //  * 4 copy warps stream the item's 128-token tiles (K 16 KB + V 16 KB) into a
 //    ring of shared-memory slots with per-lane 16-byte cp.async (a page chunk
 //    of block_size 16 is only 2 KB, far too small per copy for one TMA issuing
