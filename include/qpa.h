@@ -62,17 +62,20 @@ int qpa_version(void);
 int qpa_kernel_error(void* stream);
 
 /* ========================================================================
- * fp8 paged-attention decode ([PA]; partition map from [UQ] step F)
+ * fp8 paged-attention decode ([PA]; 256-token tile groups from [UQ] step F)
  *
  * For every sequence s (length L = seq_lens[s]), KV head h and query row g
  * (query head h*query_group + g):
  *     out = sum_t softmax_t(softmax_scale * q . k_t) v_t,   t = 0 .. L-1,
  *     k_t = e4m3fn(K byte) * (*k_scale),  v_t = e4m3fn(V byte) * (*v_scale).
- * The work is split over num_partitions partitions per (s, h): partition p
- * owns the 256-token tile groups p, p+P, p+2P, ... and writes (m_p, l_p,
- * O_p) to the workspace; the combine kernel merges them. Any P >= 1 gives the
- * same result (up to rounding); a partition with no tokens contributes
- * nothing. L = 0 gives 0. There is no cap on tile groups per partition.
+ * The sequence is split into runs of consecutive 256-token tile groups, at
+ * most num_partitions (P) per (s, h); run c writes its softmax state
+ * (m_c, l_c, O_c) to slot c of the workspace, the slots after the last run
+ * are marked empty (m = -inf, l = 0, O not written), and the combine kernel
+ * merges the slots. The runs follow an even split of all sequences' tile
+ * groups over the GPU's SMs, so a short sequence usually takes one slot and
+ * a long one a few. Any P >= 1 gives the same result (up to rounding).
+ * L = 0 gives 0.
  *
  * Layouts (row-major, element counts in brackets):
  *   q           bf16  [num_seqs][num_kv_heads*query_group][128] with the
@@ -94,10 +97,11 @@ int qpa_kernel_error(void* stream);
  *               holds, at 256-byte-aligned offsets, float32
  *               O [num_seqs][num_kv_heads][P][query_group][128],
  *               m [num_seqs][num_kv_heads][P][query_group] (max scaled logit,
- *               natural-log units, -inf for an empty partition) and
+ *               natural-log units, -inf for an empty slot) and
  *               l [num_seqs][num_kv_heads][P][query_group]
- *               (sum of exp(logit - m)); O is normalised by l and already
- *               multiplied by v_scale.
+ *               (sum of exp(logit - m), 0 for an empty slot); O is
+ *               normalised by l and already multiplied by v_scale. The
+ *               combine reads O only where l > 0 and m > -inf.
  * Supported: head_dim 128, query_group 1..16, block_size 16/32/64/128/256.
  * Alignment: q, kv_cache and out 16-byte aligned.
  * ====================================================================== */
@@ -162,7 +166,9 @@ int pa_decode_fp8_combine(int num_partitions, void* out, const qpa_fp8_desc* d,
  *   workspace pa_decode_fp8_ext_workspace_size() bytes: float32
  *             O [num_seqs][num_kv_heads][P][query_len*query_group][128] and m,
  *             l [num_seqs][num_kv_heads][P][query_len*query_group], row
- *             qoff*query_group + g (as pa_decode_fp8; O includes the V scale).
+ *             qoff*query_group + g; O includes the V scale. Partition p owns
+ *             the 256-token tile groups p, p+P, ... ([UQ] step F); an empty
+ *             one writes m = -inf, l = 0, O = 0.
  * Supported: head_dim 128, block_size 16..256, query_len 1..4 with
  * query_len * query_group <= 16. Errors as pa_decode_fp8; an unsupported
  * query_len or row count is QPA_ERR_SHAPE.
@@ -196,9 +202,11 @@ int pa_decode_fp8_ext(const void* q, const uint8_t* kv_cache, const int32_t* blo
  *   bytes 136..263  V codes (same nibble order)
  *   bytes 264..271  V scales (e4m3fn), one per 32 dims
  * Q is rotated inside the partition kernel and the output is rotated back in
- * the combine kernel. Partitions, empty partitions and L = 0 behave as for
- * pa_decode_fp8; the workspace holds the same (O, m, l) partials with
- * head_dim 256, in the rotated domain (no v_scale: the scales are per group).
+ * the combine kernel. Partition p owns the 256-token tile groups p, p+P,
+ * p+2P, ... ([UQ] step F); a partition with no tokens writes m = -inf, l = 0,
+ * O = 0; L = 0 gives 0. The workspace holds (O, m, l) partials laid out as
+ * for pa_decode_fp8 with head_dim 256, in the rotated domain (no v_scale: the
+ * scales are per group).
  *
  * Layouts:
  *   q          bf16 [num_seqs][num_kv_heads*query_group][256] (not rotated),
@@ -341,7 +349,7 @@ int nvfp4_index_score(const uint8_t* q, const uint8_t* kv_pages, const int32_t* 
  *
  * All calls share the one array and it keeps the last call's contents.
  * Nothing in it needs to start at zero: the partition kernel writes every
- * partial before the combine kernel reads it. Calls that overlap on the GPU
+ * partial the combine kernel reads. Calls that overlap on the GPU
  * (different streams, or different host threads on one device) race on the
  * array and must be serialised by the caller.
  * ---------------------------------------------------------------------- */
