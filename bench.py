@@ -519,6 +519,16 @@ def main():
             "kv_bytes": cr.kv_bytes, "gbs": round(cr.kv_bytes / (r_ms * 1e-3) / 1e9, 1),
             "frac_of_peak": round(cr.kv_bytes / (r_ms * 1e-3) / 1e9 / peak, 4)}
         del cr
+        c64 = synth.make_fp8_case(1006 + rank, [16384] * 16, 8, 8, head_dim=64, poison=False)
+        h_ms, h_part, _, _, _, _ = time_fp8(c64, 32, max(20, a.steps // 4), a.warmup, dev)
+        h_ms = _max_over_ranks(h_ms)
+        extra["fp8_b16_16k_hd64"] = {
+            "workload": "fp8 paged decode, 16 seqs x 16384 tokens, 8 KV heads, group 8, head_dim 64, block 16, P=32",
+            "us_per_step": round(h_ms * 1e3, 2), "partition_us": round(h_part * 1e3, 2),
+            "kv_bytes": c64.kv_bytes, "gbs": round(c64.kv_bytes / (h_ms * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(c64.kv_bytes / (h_ms * 1e-3) / 1e9 / peak, 4),
+            "l2": "no flush: the 268 MB KV stream per step is larger than L2"}
+        del c64
         esteps = max(20, a.steps // 4)
         for name, cent, pagefmt in (("uq_hd256_b4_75k_e2m1", None, False),
                                     ("uq_hd256_b4_75k_randtable", "rand", False),

@@ -34,7 +34,7 @@ struct Fp8Layout {
 
 bool fp8_shape_ok(const qpa_fp8_desc* d) {
   if (d->num_seqs < 0 || d->num_kv_heads < 1 || d->query_group < 1 || d->query_group > 16) return false;
-  if (d->head_dim != 128) return false;
+  if (d->head_dim != 128 && d->head_dim != 64) return false;
   const int bs = d->block_size;
   if (!(bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256)) return false;
   if (d->num_blocks < 1 || d->max_blocks_per_seq < 1) return false;
@@ -73,7 +73,7 @@ int fp8_check(const void* q, const uint8_t* kv, const int32_t* bt, const int32_t
 int fp8x_query_len(const qpa_fp8_ext_desc* d) { return d->query_len > 1 ? d->query_len : 1; }
 
 bool fp8x_shape_ok(const qpa_fp8_ext_desc* d) {
-  if (!fp8_shape_ok(&d->base)) return false;
+  if (!fp8_shape_ok(&d->base) || d->base.head_dim != 128) return false;
   if (d->query_len < 0 || d->query_len > 4) return false;
   if (fp8x_query_len(d) * d->base.query_group > 16) return false;
   if (d->kv_scale_per_token != 0 && d->kv_scale_per_token != 1) return false;
@@ -210,6 +210,7 @@ int pa_decode_fp8_partition(const void* q, const uint8_t* kv_cache, const int32_
   a.max_blocks = d->max_blocks_per_seq;
   a.num_partitions = num_partitions;
   a.softmax_scale = d->softmax_scale != 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
+  a.head_dim = d->head_dim;
   a.num_sms = num_sms_current();
   if (a.num_sms <= 0) return QPA_ERR_CUDA;
   return launch_fp8_partition(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;

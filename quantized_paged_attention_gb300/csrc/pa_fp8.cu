@@ -95,7 +95,11 @@ struct Fp8Params {
   float softmax_scale;
 };
 
-template <int NT>
+// HD: the cache's head_dim (64 or 128). Shared-memory rows stay 128 bytes
+// (the 128-byte-swizzle layout); with HD = 64 their upper half is zeroed once
+// and never written, so the QK steps over it are skipped and the PV rows of
+// dims 64..127 come out zero.
+template <int NT, int HD>
 __global__ void __launch_bounds__(fp8::Smem<NT>::THREADS, 1)
 pa_fp8_partition_kernel(const Fp8Params p) {
   using namespace fp8;
@@ -159,6 +163,13 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     *abort_flag = 0;
     *qk_total = -1;
     fence_mbar_init();
+  }
+  if constexpr (HD < D) {
+    // zero the tile ring and the query operands: the dims HD..127 of every row
+    // stay zero for the whole launch
+    for (int i = threadIdx.x; i < (NS * TILE_BYTES + 2 * S::qBytes) / 16; i += blockDim.x)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(ring + 16 * i), "r"(0u) : "memory");
+    fence_proxy_async();
   }
   if (warp == WARP_MMA) tmem_alloc(tmem_slot, S::TMEM_COLS);
   tc_fence_before();
@@ -407,7 +418,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             ot = o[r] * a0 + other[r] * a1;
           }
           // (lt >= 1: the row maximum's own term is exactly 1)
-          if (r < p.qg) p.part_o[(row0 + r) * D + t] = ot * (vscale * rcp_approx(lt));
+          if (r < p.qg && t < HD) p.part_o[(row0 + r) * HD + t] = ot * (vscale * rcp_approx(lt));
           if (t == r) {
             lt_mine = lt;
             mt_mine = mt;
@@ -430,10 +441,13 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     // ======================================================== copy warps
     const int pw = warp - WARP_PROD0;
     const uint64_t pol = policy_evict_first();
-    const int l3 = lane >> 3, c8 = lane & 7;
-    const uint32_t doff_e = (uint32_t)((32 * pw + l3) * D + ((c8 ^ l3) << 4));
-    const uint32_t doff_o = (uint32_t)((32 * pw + l3) * D + ((c8 ^ (l3 + 4)) << 4));
-    const size_t head_bytes = size_t(bs) * D;
+    // copy lanes: CPR 16-byte chunks per token row, RPI rows per instruction;
+    // lane = (row lr, chunk cc), row 32 pw + lr + RPI ii, chunk cc ^ (row & 7)
+    constexpr int CPR = HD / 16, RPI = 32 / CPR, NII = 32 / RPI;
+    const int lr = lane / CPR, cc = lane % CPR;
+    const uint32_t doff_e = (uint32_t)((32 * pw + lr) * D + ((cc ^ (lr & 7)) << 4));
+    const uint32_t doff_o = (uint32_t)((32 * pw + lr) * D + ((cc ^ ((lr + 4) & 7)) << 4));
+    const size_t head_bytes = size_t(bs) * HD;
     const size_t v_off = size_t(Hk) * head_bytes;
     const size_t blk_bytes = 2 * v_off;
     const int pt = 32 * pw + lane;                  // query-operand thread: row pt >> 4, dims 8 (pt & 15) ..
@@ -450,7 +464,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 #pragma unroll
       for (int h = 0; h < NT; ++h) {
         const int row = qrow + 8 * h;
-        if (row < p.qg)
+        if (row < p.qg && h16 < HD / 8)
           qv[h] = __ldg(reinterpret_cast<const uint4*>(p.q + seq * p.q_stride_seq +
                                                        (long long)(kvh * p.qg + row) * p.q_stride_head) + h16);
       }
@@ -633,8 +647,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             }
             const int rr = term * R + row;
             const uint32_t addr = qsm + qb * S::qBytes + rr * D + (((h16 >> 1) ^ (rr & 7)) << 4) + 8 * (h16 & 1);
-            asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(e[0] | (e[1] << 16)),
-                         "r"(e[2] | (e[3] << 16)) : "memory");
+            if (h16 < HD / 8)
+              asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(e[0] | (e[1] << 16)),
+                           "r"(e[2] | (e[3] << 16)) : "memory");
           }
           if (h16 == 0) stsf(cbuf_s + 4 * (qb * R + row), row < p.qg ? base_scale * down : 0.f);
         }
@@ -670,14 +685,16 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             if (tok0 + 16 < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
             pb = 0;
           }
-          const uint8_t* ka = p.kv + size_t(pa) * blk_bytes + kvh_off + size_t(tok0 & (bs - 1)) * D + l3 * D + c8 * 16;
-          const uint8_t* kb = bs == 16 ? p.kv + size_t(pb) * blk_bytes + kvh_off + l3 * D + c8 * 16 : ka + 16 * D;
+          // tokens tok0 .. tok0 + 15 lie in block pa, tok0 + 16 .. in pb (the same
+          // block unless block_size is 16)
+          const uint8_t* ka = p.kv + size_t(pa) * blk_bytes + kvh_off + size_t(tok0 & (bs - 1)) * HD + lr * HD + cc * 16;
+          const uint8_t* kb = bs == 16 ? p.kv + size_t(pb) * blk_bytes + kvh_off + lr * HD + cc * 16 : ka + 16 * HD;
           const uint32_t slot = ring + s * TILE_BYTES;
 #pragma unroll
-          for (int ii = 0; ii < 8; ++ii) {
-            const bool valid = tok0 + l3 + 4 * ii < L;
-            const uint8_t* src = ii < 4 ? ka + 512 * ii : kb + 512 * (ii - 4);
-            const uint32_t dst = slot + ((ii & 1) ? doff_o : doff_e) + 512 * ii;
+          for (int ii = 0; ii < NII; ++ii) {
+            const bool valid = tok0 + lr + RPI * ii < L;
+            const uint8_t* src = ii < NII / 2 ? ka + RPI * HD * ii : kb + RPI * HD * (ii - NII / 2);
+            const uint32_t dst = slot + (((RPI * ii) & 4) ? doff_o : doff_e) + RPI * D * ii;
             cp_async16_zfill(dst, src, valid, pol);
             cp_async16_zfill(dst + V_OFF, src + v_off, valid, pol);
           }
@@ -726,7 +743,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           tc_fence_after();
           const uint32_t ka = ring + s * TILE_BYTES;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+          for (int k = 0; k < HD / 32; ++k)
             mma_e4m3(tmem + b * NQ, umma_desc(ka + 32 * k, 16, 1024, kSwizzle128B),
                      umma_desc(qa + 32 * k, 16, 1024, kSwizzle128B), IDESC_QK, k);
           umma_commit(&sfull[b]);
@@ -804,21 +821,21 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 
 // Flash-combine of the partitions ([PA] reduce kernel): one CTA per query
 // row (seq, kv_head, r), see combine_row.
-template <typename OutT>
+template <typename OutT, int HD>
 __global__ void __launch_bounds__(kCombineMaxThreads)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
                const float* __restrict__ part_l, OutT* __restrict__ out, int num_kv_heads, int qg,
                int num_partitions, long long out_stride_seq, long long out_stride_head) {
   extern __shared__ __align__(16) float sw[];
-  __shared__ __align__(16) float vec[fp8::D];
+  __shared__ __align__(16) float vec[HD];
   pdl_wait_primary();
   const int row = blockIdx.x;                 // ((seq * Hk) + kvh) * qg + r
   const int r = row % qg;
   const int sk = row / qg;                    // seq * Hk + kvh
   const int seq = sk / num_kv_heads, kvh = sk % num_kv_heads;
-  combine_row<fp8::D, kCombineKmax128>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg,
-                                       num_partitions, sw, vec);
-  if (threadIdx.x < fp8::D / 4) {
+  combine_row<HD, kCombineKmax128>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg,
+                                   num_partitions, sw, vec);
+  if (threadIdx.x < HD / 4) {
     const int t = threadIdx.x;
     OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + 4 * t;
     store4(dst, vec[4 * t], vec[4 * t + 1], vec[4 * t + 2], vec[4 * t + 3]);
@@ -852,25 +869,27 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
   const long long items = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   if (items <= 0) return cudaSuccess;
   const int grid = (int)std::min<long long>(items, (long long)a.num_sms);
-  if (a.qg <= 8) {
-    const int smem = fp8::Smem<1>::total;
-    cudaFuncSetAttribute(pa_fp8_partition_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    pa_fp8_partition_kernel<1><<<grid, fp8::Smem<1>::THREADS, smem, stream>>>(p);
+  auto launch = [&](auto kernel, int threads, int smem) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kernel<<<grid, threads, smem, stream>>>(p);
+  };
+  if (a.head_dim == 64) {
+    if (a.qg <= 8) launch(pa_fp8_partition_kernel<1, 64>, fp8::Smem<1>::THREADS, fp8::Smem<1>::total);
+    else launch(pa_fp8_partition_kernel<2, 64>, fp8::Smem<2>::THREADS, fp8::Smem<2>::total);
   } else {
-    const int smem = fp8::Smem<2>::total;
-    cudaFuncSetAttribute(pa_fp8_partition_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    pa_fp8_partition_kernel<2><<<grid, fp8::Smem<2>::THREADS, smem, stream>>>(p);
+    if (a.qg <= 8) launch(pa_fp8_partition_kernel<1, 128>, fp8::Smem<1>::THREADS, fp8::Smem<1>::total);
+    else launch(pa_fp8_partition_kernel<2, 128>, fp8::Smem<2>::THREADS, fp8::Smem<2>::total);
   }
   return cudaGetLastError();
 }
 
-template <typename OutT>
+template <typename OutT, int HD>
 static cudaError_t launch_combine_t(const CombineLaunch& a, OutT* out, cudaStream_t stream) {
   const int grid = a.num_seqs * a.num_kv_heads * a.qg;
-  const int threads = combine_threads(fp8::D, kCombineKmax128, a.num_partitions);
+  const int threads = combine_threads(HD, kCombineKmax128, a.num_partitions);
   const size_t smem = combine_smem_bytes(a.num_partitions, threads);
   if (smem > 40 * 1024)
-    cudaFuncSetAttribute(combine_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(combine_kernel<OutT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(threads);
@@ -881,14 +900,19 @@ static cudaError_t launch_combine_t(const CombineLaunch& a, OutT* out, cudaStrea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<OutT>, a.part_o, a.part_m, a.part_l, out, a.num_kv_heads,
+  return cudaLaunchKernelEx(&cfg, combine_kernel<OutT, HD>, a.part_o, a.part_m, a.part_l, out, a.num_kv_heads,
                             a.qg, a.num_partitions, a.out_stride_seq, a.out_stride_head);
 }
 
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t stream) {
   if (a.num_seqs * a.num_kv_heads * a.qg <= 0) return cudaSuccess;
-  cudaError_t e = a.out_bf16 ? launch_combine_t(a, static_cast<__nv_bfloat16*>(a.out), stream)
-                             : launch_combine_t(a, static_cast<float*>(a.out), stream);
+  cudaError_t e;
+  if (a.d == 64)
+    e = a.out_bf16 ? launch_combine_t<__nv_bfloat16, 64>(a, static_cast<__nv_bfloat16*>(a.out), stream)
+                   : launch_combine_t<float, 64>(a, static_cast<float*>(a.out), stream);
+  else
+    e = a.out_bf16 ? launch_combine_t<__nv_bfloat16, 128>(a, static_cast<__nv_bfloat16*>(a.out), stream)
+                   : launch_combine_t<float, 128>(a, static_cast<float*>(a.out), stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

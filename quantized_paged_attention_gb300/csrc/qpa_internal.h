@@ -21,6 +21,7 @@ struct Fp8Launch {
   long long q_stride_seq, q_stride_head;
   int num_seqs, num_kv_heads, qg, block_size, num_blocks, max_blocks, num_partitions;
   float softmax_scale;
+  int head_dim;     // 64 or 128
   int num_sms;
 };
 

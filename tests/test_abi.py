@@ -61,7 +61,7 @@ def _call(lib, d, P=2, ws_bytes=1 << 20, q=FAKE, ws=FAKE):
 
 def test_host_validation(lib):
     assert _call(lib, _desc(), P=0) == -5
-    assert _call(lib, _desc(head_dim=64)) == -2
+    assert _call(lib, _desc(head_dim=96)) == -2
     assert _call(lib, _desc(block_size=24)) == -2
     assert _call(lib, _desc(query_group=17)) == -2
     assert _call(lib, _desc(), q=ctypes.c_void_p(0)) == -1
@@ -76,7 +76,9 @@ def test_workspace_size(lib):
     n = lib.pa_decode_fp8_workspace_size(ctypes.byref(d), 2)
     rows = 2 * 1 * 2 * 8
     assert n >= rows * 130 * 4 and n % 256 == 0
-    assert lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc(head_dim=64)), 2) == 0
+    assert lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc(head_dim=96)), 2) == 0
+    n64 = lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc(head_dim=64)), 2)
+    assert n64 >= rows * 66 * 4 and n64 < n
 
 
 def _ext_desc(query_len=2, per_token=1, **kw):
@@ -111,6 +113,8 @@ def test_ext_workspace_size(lib):
     # query_len 0 means one query token
     one = lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=0)), 2)
     assert one == lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc()), 2)
+    # head_dim 64 is served by pa_decode_fp8 only
+    assert lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=1, head_dim=64)), 2) == 0
 
 
 def _uq_desc(**kw):

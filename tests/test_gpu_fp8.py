@@ -188,3 +188,32 @@ def test_full_ragged_config_sampled():
     for s in (int(np.argmin(c.seq_lens)), int(np.argmax(c.seq_lens))):
         units.append((s, 7))
     _check(c, got, units=units, what="ragged-full")
+
+
+# ---- head_dim 64 ([PA]: head_dim 64 or 128)
+@pytest.mark.parametrize("P", [1, 3, 32])
+@pytest.mark.parametrize("qg", [8, 16, 5])
+def test_head_dim_64(P, qg):
+    c = synth.make_fp8_case(900 + P + qg, [0, 1, 127, 128, 129, 255, 256, 257, 1000, 3000], 2, qg, head_dim=64)
+    out, _, _ = Fp8Dev(c).run(P)
+    _check(c, out.cpu().double().numpy(), what=f"hd64 P={P} qg={qg}")
+
+
+@pytest.mark.parametrize("bs", [32, 64, 256])
+def test_head_dim_64_block_sizes_and_bf16(bs):
+    c = synth.make_fp8_case(930 + bs, [1, bs - 1, bs + 1, 2000], 2, 8, head_dim=64, block_size=bs)
+    d = Fp8Dev(c)
+    out, _, _ = d.run(4)
+    _check(c, out.cpu().double().numpy(), what=f"hd64 bs={bs}")
+    o16, _, _ = d.run(4, out_dtype=torch.bfloat16)
+    assert torch.max(torch.abs(o16.float() - out)).item() <= torch.max(torch.abs(out)).item() * 2 ** -8 + 1e-6
+
+
+def test_head_dim_64_long_sampled():
+    """16 seqs x 16384 tokens, 8 KV heads, group 8, head_dim 64, P = 32 (the
+    benchmark's head_dim 64 line); three sampled (seq, head) units."""
+    c = synth.make_fp8_case(960, [16384] * 16, 8, 8, head_dim=64, poison=False)
+    out, _, _ = Fp8Dev(c).run(32)
+    got = out.cpu().double().numpy()
+    assert np.all(np.isfinite(got))
+    _check(c, got, units=[(0, 0), (9, 3), (15, 7)], what="hd64 long")

@@ -250,3 +250,20 @@ def test_ext_per_token_brute_force():
                         blk, sl = int(c.block_table[s, t // bs]), t % bs
                         num += w[t] * float(vc[blk, 0, sl, d]) * float(c.v_scale[blk, 0, sl])
                     assert abs(out[s, qoff, g, d] - num / den) < 1e-12
+
+
+def test_head_dim_64_is_the_zero_padded_128_case():
+    """The decode at head_dim 64 equals the head_dim 128 decode of the same
+    tokens with the extra 64 dims of q and K zero and V's extra dims dropped,
+    at the same softmax scale."""
+    c = synth.make_fp8_case(77, [5, 130], 2, 4, head_dim=64)
+    out64 = oracle.pa_decode_fp8(c.q_bits, c.kv_cache, c.block_table, c.seq_lens, c.k_scale, c.v_scale, 4,
+                                 c.softmax_scale)
+    q = np.zeros(c.q_bits.shape[:2] + (128,), dtype=np.uint16)
+    q[..., :64] = c.q_bits
+    kv = np.zeros(c.kv_cache.shape[:4] + (128,), dtype=np.uint8)
+    kv[..., :64] = c.kv_cache
+    out128 = oracle.pa_decode_fp8(q, kv, c.block_table, c.seq_lens, c.k_scale, c.v_scale, 4, c.softmax_scale)
+    assert c.softmax_scale == 1 / 8
+    assert np.max(np.abs(out128[..., :64] - out64)) < 1e-13
+    assert np.all(out128[..., 64:] == 0)
