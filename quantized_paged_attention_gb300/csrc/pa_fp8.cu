@@ -51,7 +51,7 @@ constexpr int TILE = 128;       // tokens per MMA tile
 constexpr int TILE_BYTES = 2 * TILE * D;   // K tile then V tile
 constexpr int V_OFF = TILE * D;
 
-template <int NT>
+template <int NT, bool EXT = false>
 struct Smem {
   static constexpr int NWG = NT == 1 ? 2 : 1;      // softmax warp groups
   static constexpr int WARP_PROD0 = 4 * NWG;       // 4 copy warps
@@ -71,7 +71,8 @@ struct Smem {
   static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][4 NWG][R] row sums per warp
   static constexpr int msmOff = lredOff + 2 * 4 * NWG * R * 4;   // [2][NWG][R] row maxima per group
   static constexpr int infoOff = msmOff + 2 * NWG * R * 4; // [2] {item row, L, tiles, first tile group}
-  static constexpr int barOff = (infoOff + 2 * 16 + 7) & ~7;
+  static constexpr int scOff = infoOff + 2 * 16;           // EXT: [NS][K, V][128] f32 per-token scales
+  static constexpr int barOff = (scOff + (EXT ? NS * 2 * TILE * 4 : 0) + 7) & ~7;
   static constexpr int NBAR = 2 * NS + 2 * 10 + 4 + 1;
   static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag, QK total
   static constexpr int total = miscOff + 16 + 1024;        // + alignment slack
@@ -93,17 +94,26 @@ struct Fp8Params {
   long long q_stride_seq, q_stride_head;   // elements
   int num_seqs, num_kv_heads, qg, block_size, log2_bs, num_blocks, max_blocks, num_partitions;
   float softmax_scale;
+  // multi-token variant: query_len new tokens per sequence (row qoff * qg + g,
+  // causal inside the query block), K/V scales per tensor or per token
+  // ([num_blocks][Hk][block_size] in k_scale / v_scale)
+  long long q_stride_tok;
+  int query_len, per_token;
 };
 
 // HD: the cache's head_dim (64 or 128). Shared-memory rows stay 128 bytes
 // (the 128-byte-swizzle layout); with HD = 64 their upper half is zeroed once
 // and never written, so the QK steps over it are skipped and the PV rows of
 // dims 64..127 come out zero.
-template <int NT, int HD>
+// EXT: the multi-token / per-token variant (query_len, per_token of the
+// parameters); rows = query_len * qg per item, a causal limit per row, and
+// with per-token scales the copy warps bring each tile's K and V scales into
+// shared memory next to the tile.
+template <int NT, int HD, bool EXT>
 __global__ void __launch_bounds__(fp8::Smem<NT>::THREADS, 1)
 pa_fp8_partition_kernel(const Fp8Params p) {
   using namespace fp8;
-  using S = Smem<NT>;
+  using S = Smem<NT, EXT>;
   constexpr int R = S::R, NQ = S::NQ, NWG = S::NWG;
   constexpr int WARP_PROD0 = S::WARP_PROD0, WARP_MMA = S::WARP_MMA;
   constexpr uint32_t IDESC_QK = idesc_e4m3(128, NQ, false, false);
@@ -134,6 +144,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   const uint32_t lred_s = sbase + S::lredOff;
   const uint32_t msm_s = sbase + S::msmOff;
   const uint32_t info_s = sbase + S::infoOff;
+  const uint32_t sc_s = sbase + S::scOff;
   const uint32_t stg_s = sbase + S::stgOff;
   const uint32_t ring = sbase + S::ringOff;
   const uint32_t qsm = sbase + S::qOff;
@@ -181,6 +192,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   const int P = p.num_partitions;
   const int Hk = p.num_kv_heads;
   const int G = gridDim.x;
+  const int QL = EXT ? p.query_len : 1;
+  const int rows = EXT ? QL * p.qg : p.qg;   // partial rows per item
+  const bool per_token = EXT && p.per_token != 0;
   const int bs = p.block_size;
   const int lbs = p.log2_bs;
   const int bpt = TG / bs;                  // table entries per tile group
@@ -193,7 +207,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     const int wq = warp & 3;                           // lane quarter of tensor memory
     const int t = threadIdx.x & 127;                   // tensor-memory lane
     const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
-    const float vscale = __ldg(p.v_scale);
+    const float vscale = per_token ? 1.f : __ldg(p.v_scale);
     const uint32_t ptok = psm + (t >> 3) * (8 * NQ) + (t & 7) * 16;   // this token's P' row
     float m[R], l[R], o[R], c[R];
 #pragma unroll
@@ -262,10 +276,27 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         if (lane == 0) mbar_arrive(&sfree[b]);
         const bool valid = start + t < L;
         float x[R];
+        float vs_t = 1.f;                    // this token's V scale (EXT, per token)
+        if constexpr (EXT) {
+          float ks_t = 1.f;
+          if (per_token) {
+            // the tile's scales landed with its copies (the slot's full barrier)
+            if (!warp_wait(&full[j % NS], (j / NS) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
+            ks_t = ldsf(sc_s + 4 * ((j % NS) * 2 * TILE + t));
+            vs_t = valid ? ldsf(sc_s + 4 * ((j % NS) * 2 * TILE + TILE + t)) : 0.f;
+          }
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float sv = fmaf(fmaf(fmaf(v[3 * R + r], 0.0625f, v[2 * R + r]), 0.0625f, v[R + r]), 0.0625f, v[r]);
-          x[r] = valid ? sv * c[r] : -INFINITY;
+          for (int r = 0; r < R; ++r) {
+            // row r = qoff * qg + g sees the tokens below L - QL + 1 + qoff
+            const float sv = fmaf(fmaf(fmaf(v[3 * R + r], 0.0625f, v[2 * R + r]), 0.0625f, v[R + r]), 0.0625f, v[r]);
+            x[r] = (start + t < L - QL + 1 + r / p.qg) ? sv * c[r] * ks_t : -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float sv = fmaf(fmaf(fmaf(v[3 * R + r], 0.0625f, v[2 * R + r]), 0.0625f, v[R + r]), 0.0625f, v[r]);
+            x[r] = valid ? sv * c[r] : -INFINITY;
+          }
         }
         {
           // row maxima over the warp's 32 tokens (hardware warp reduction)
@@ -295,7 +326,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             for (int u = 0; u < 4; ++u) {
               const int r = 4 * q4 + u;
               const float mn = fmaxf(m[r], tm[u]);
-              alpha[r] = ex2(m[r] - mn);
+              // (EXT: a row may have seen no token yet, -inf - -inf)
+              alpha[r] = (EXT && mn == -INFINITY) ? 1.f : ex2(m[r] - mn);
               m[r] = mn;
             }
           }
@@ -304,10 +336,20 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         uint32_t tw[3][R / 4];
 #pragma unroll
         for (int k = 0; k < R / 2; ++k) {
-          const uint32_t p16 = f32x2_to_f16x2(ex2(x[2 * k] - m[2 * k]), ex2(x[2 * k + 1] - m[2 * k + 1]));
+          float pa0, pa1;
+          if constexpr (EXT) {
+            pa0 = x[2 * k] == -INFINITY ? 0.f : ex2(x[2 * k] - m[2 * k]);
+            pa1 = x[2 * k + 1] == -INFINITY ? 0.f : ex2(x[2 * k + 1] - m[2 * k + 1]);
+          } else {
+            pa0 = ex2(x[2 * k] - m[2 * k]);
+            pa1 = ex2(x[2 * k + 1] - m[2 * k + 1]);
+          }
+          const uint32_t p16 = f32x2_to_f16x2(pa0, pa1);
           l[2 * k] = fmaf(l[2 * k], alpha[2 * k], f16_lo_to_f32(p16));
           l[2 * k + 1] = fmaf(l[2 * k + 1], alpha[2 * k + 1], f16_hi_to_f32(p16));
-          uint32_t h = hmul2(p16, 0x5C005C00u);                      // x 256
+          // the PV operand: p, times the token's V scale with per-token scales
+          const uint32_t pv16 = per_token ? f32x2_to_f16x2(pa0 * vs_t, pa1 * vs_t) : p16;
+          uint32_t h = hmul2(pv16, 0x5C005C00u);                     // x 256
           const uint32_t e0 = f16x2_to_e4m3x2(h);
           h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e0)), 0x4C004C00u);   // residual x 16
           const uint32_t e1 = f16x2_to_e4m3x2(h);
@@ -383,7 +425,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         if (!warp_wait(&merge[qb], kph, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
         const uint32_t lr = lred_s + qb * 4 * NWG * R * 4;
         const uint32_t mr = msm_s + qb * NWG * R * 4;
-        const long long row0 = (long long)item * p.qg;
+        const long long row0 = (long long)item * rows;
         float lsum[NWG][R], mg[NWG][R];
 #pragma unroll
         for (int g = 0; g < NWG; ++g)
@@ -413,18 +455,21 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             const float m_me = wg == 0 ? mg[0][r] : mg[NWG - 1][r], m_ot = wg == 0 ? mg[NWG - 1][r] : mg[0][r];
             const float l_me = wg == 0 ? lsum[0][r] : lsum[NWG - 1][r], l_ot = wg == 0 ? lsum[NWG - 1][r] : lsum[0][r];
             mt = fmaxf(m_me, m_ot);
-            const float a0 = ex2(m_me - mt), a1 = ex2(m_ot - mt);
+            const float a0 = (EXT && m_me == -INFINITY) ? 0.f : ex2(m_me - mt);
+            const float a1 = (EXT && m_ot == -INFINITY) ? 0.f : ex2(m_ot - mt);
             lt = l_me * a0 + l_ot * a1;
             ot = o[r] * a0 + other[r] * a1;
           }
-          // (lt >= 1: the row maximum's own term is exactly 1)
-          if (r < p.qg && t < HD) p.part_o[(row0 + r) * HD + t] = ot * (vscale * rcp_approx(lt));
+          // (lt >= 1: the row maximum's own term is exactly 1; EXT: lt = 0 for a
+          // row that saw no token)
+          if (r < rows && t < HD)
+            p.part_o[(row0 + r) * HD + t] = (EXT && lt == 0.f) ? 0.f : ot * (vscale * rcp_approx(lt));
           if (t == r) {
             lt_mine = lt;
             mt_mine = mt;
           }
         }
-        if (t < p.qg) {
+        if (t < rows) {
           p.part_m[row0 + t] = mt_mine * kLn2;
           p.part_l[row0 + t] = lt_mine;
         }
@@ -452,7 +497,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     const size_t blk_bytes = 2 * v_off;
     const int pt = 32 * pw + lane;                  // query-operand thread: row pt >> 4, dims 8 (pt & 15) ..
     const int qrow = pt >> 4, h16 = pt & 15;
-    const float base_scale = __ldg(p.k_scale) * p.softmax_scale * kLog2e;
+    const float base_scale = (per_token ? 1.f : __ldg(p.k_scale)) * p.softmax_scale * kLog2e;
     int j = 0, qcnt = 0;
     bool ok = true;
 
@@ -463,10 +508,11 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       if (seq < 0) return;
 #pragma unroll
       for (int h = 0; h < NT; ++h) {
-        const int row = qrow + 8 * h;
-        if (row < p.qg && h16 < HD / 8)
-          qv[h] = __ldg(reinterpret_cast<const uint4*>(p.q + seq * p.q_stride_seq +
-                                                       (long long)(kvh * p.qg + row) * p.q_stride_head) + h16);
+        const int row = qrow + 8 * h;       // EXT: row qoff * qg + g
+        const int qoff = EXT ? row / p.qg : 0, g = EXT ? row - qoff * p.qg : row;
+        if (row < rows && h16 < HD / 8)
+          qv[h] = __ldg(reinterpret_cast<const uint4*>(p.q + seq * p.q_stride_seq + (EXT ? qoff * p.q_stride_tok : 0) +
+                                                       (long long)(kvh * p.qg + g) * p.q_stride_head) + h16);
       }
     };
     auto load_entries = [&](int seq, int tg) -> int32_t {
@@ -542,8 +588,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     // (sequence, head) pairs with no tokens: every slot empty
     for (int pr = blockIdx.x; pr < B * Hk; pr += G) {
       if (seq_len(pr / Hk) == 0) {
-        const long long rb = (long long)pr * P * p.qg;
-        for (int i = pt; i < P * p.qg; i += 128) {
+        const long long rb = (long long)pr * P * rows;
+        for (int i = pt; i < P * rows; i += 128) {
           p.part_m[rb + i] = -INFINITY;
           p.part_l[rb + i] = 0.f;
         }
@@ -596,8 +642,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         if (lane == 0) atomicExch(&g_kernel_error, KERR_SCHEDULE);
       } else {
         if (slot == 0 && nc < P) {
-          const long long rb = ((long long)(cur.s * Hk + kvh) * P + nc) * p.qg;
-          for (int i = pt; i < (P - nc) * p.qg; i += 128) {
+          const long long rb = ((long long)(cur.s * Hk + kvh) * P + nc) * rows;
+          for (int i = pt; i < (P - nc) * rows; i += 128) {
             p.part_m[rb + i] = -INFINITY;
             p.part_l[rb + i] = 0.f;
           }
@@ -651,7 +697,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
               asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(e[0] | (e[1] << 16)),
                            "r"(e[2] | (e[3] << 16)) : "memory");
           }
-          if (h16 == 0) stsf(cbuf_s + 4 * (qb * R + row), row < p.qg ? base_scale * down : 0.f);
+          if (h16 == 0) stsf(cbuf_s + 4 * (qb * R + row), row < rows ? base_scale * down : 0.f);
         }
         if (pt == 0) sts_i4(info_s + 16 * qb, make_int4(item, L, nt, tg_b));
         fence_proxy_async();
@@ -697,6 +743,16 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             const uint32_t dst = slot + (((RPI * ii) & 4) ? doff_o : doff_e) + RPI * D * ii;
             cp_async16_zfill(dst, src, valid, pol);
             cp_async16_zfill(dst + V_OFF, src + v_off, valid, pol);
+          }
+          if (per_token && lane < 16) {
+            // this warp's 32 tokens' K (lanes 0..7) or V (8..15) scales, 4 tokens
+            // per lane; the scale arrays are indexed like the cache's (block, head, slot)
+            const int ch = lane & 7;
+            const int blk = (bs == 16 && ch >= 4) ? pb : pa;
+            const float* sarr = lane < 8 ? p.k_scale : p.v_scale;
+            const float* src = sarr + (size_t(blk) * Hk + kvh) * bs + ((tok0 + 4 * ch) & (bs - 1));
+            const uint32_t dst = sc_s + 4 * (s * 2 * TILE + (lane < 8 ? 0 : TILE) + 32 * pw + 4 * ch);
+            cp_async16_zfill(dst, src, tok0 + 4 * ch < L, pol);
           }
           // the slot's barrier counts this lane once all its copies so far have landed
           cp_async_arrive_noinc(&full[s]);
@@ -866,6 +922,9 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
   p.max_blocks = a.max_blocks;
   p.num_partitions = a.num_partitions;
   p.softmax_scale = a.softmax_scale;
+  p.q_stride_tok = 0;
+  p.query_len = 1;
+  p.per_token = 0;
   const long long items = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   if (items <= 0) return cudaSuccess;
   const int grid = (int)std::min<long long>(items, (long long)a.num_sms);
@@ -874,12 +933,54 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
     kernel<<<grid, threads, smem, stream>>>(p);
   };
   if (a.head_dim == 64) {
-    if (a.qg <= 8) launch(pa_fp8_partition_kernel<1, 64>, fp8::Smem<1>::THREADS, fp8::Smem<1>::total);
-    else launch(pa_fp8_partition_kernel<2, 64>, fp8::Smem<2>::THREADS, fp8::Smem<2>::total);
+    if (a.qg <= 8) launch(pa_fp8_partition_kernel<1, 64, false>, fp8::Smem<1>::THREADS, fp8::Smem<1>::total);
+    else launch(pa_fp8_partition_kernel<2, 64, false>, fp8::Smem<2>::THREADS, fp8::Smem<2>::total);
   } else {
-    if (a.qg <= 8) launch(pa_fp8_partition_kernel<1, 128>, fp8::Smem<1>::THREADS, fp8::Smem<1>::total);
-    else launch(pa_fp8_partition_kernel<2, 128>, fp8::Smem<2>::THREADS, fp8::Smem<2>::total);
+    if (a.qg <= 8) launch(pa_fp8_partition_kernel<1, 128, false>, fp8::Smem<1>::THREADS, fp8::Smem<1>::total);
+    else launch(pa_fp8_partition_kernel<2, 128, false>, fp8::Smem<2>::THREADS, fp8::Smem<2>::total);
   }
+  return cudaGetLastError();
+}
+
+// The multi-token / per-token decode on the same kernel (rows = query_len *
+// qg <= 16; head_dim 128).
+cudaError_t launch_fp8x_partition(const Fp8ExtLaunch& a, cudaStream_t stream) {
+  Fp8Params p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.kv = a.kv;
+  p.block_table = a.block_table;
+  p.seq_lens = a.seq_lens;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  p.part_o = a.part_o;
+  p.part_m = a.part_m;
+  p.part_l = a.part_l;
+  p.q_stride_seq = a.q_stride_seq;
+  p.q_stride_head = a.q_stride_head;
+  p.num_seqs = a.num_seqs;
+  p.num_kv_heads = a.num_kv_heads;
+  p.qg = a.qg;
+  p.block_size = a.block_size;
+  p.log2_bs = 0;
+  while ((1 << p.log2_bs) < a.block_size) ++p.log2_bs;
+  p.num_blocks = a.num_blocks;
+  p.max_blocks = a.max_blocks;
+  p.num_partitions = a.num_partitions;
+  p.softmax_scale = a.softmax_scale;
+  p.q_stride_tok = a.q_stride_tok;
+  p.query_len = a.query_len;
+  p.per_token = a.per_token;
+  const long long items = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
+  if (items <= 0) return cudaSuccess;
+  const int grid = (int)std::min<long long>(items, (long long)a.num_sms);
+  auto launch = [&](auto kernel, int threads, int smem) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kernel<<<grid, threads, smem, stream>>>(p);
+  };
+  if (a.query_len * a.qg <= 8)
+    launch(pa_fp8_partition_kernel<1, 128, true>, fp8::Smem<1, true>::THREADS, fp8::Smem<1, true>::total);
+  else
+    launch(pa_fp8_partition_kernel<2, 128, true>, fp8::Smem<2, true>::THREADS, fp8::Smem<2, true>::total);
   return cudaGetLastError();
 }
 

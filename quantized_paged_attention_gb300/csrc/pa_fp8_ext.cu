@@ -519,7 +519,7 @@ combine_ext_kernel(const float* __restrict__ part_o, const float* __restrict__ p
 }
 
 // ------------------------------------------------------------------ host side
-cudaError_t launch_fp8x_partition(const Fp8ExtLaunch& a, cudaStream_t stream) {
+cudaError_t launch_fp8x_partition_mma(const Fp8ExtLaunch& a, cudaStream_t stream) {
   Fp8ExtParams p;
   p.q = static_cast<const uint16_t*>(a.q);
   p.kv = a.kv;
