@@ -53,7 +53,7 @@ constexpr int V_OFF = TILE * D;
 
 template <int NT, bool EXT = false>
 struct Smem {
-  static constexpr int NWG = NT == 1 ? 2 : 1;      // softmax warp groups
+  static constexpr int NWG = 2;                    // softmax warp groups
   static constexpr int WARP_PROD0 = 4 * NWG;       // 4 copy warps
   static constexpr int WARP_MMA = WARP_PROD0 + 4;  // QK issuing warp, then the PV issuing warp
   static constexpr int THREADS = (WARP_MMA + 2) * 32;
@@ -65,15 +65,15 @@ struct Smem {
   static constexpr int ringOff = 0;
   static constexpr int qOff = NS * TILE_BYTES;
   static constexpr int pOff = qOff + 2 * qBytes;
-  static constexpr int stgOff = pOff + 4 * pBytes;         // [2][R][128] f32 second group's O
-  static constexpr int cOff = stgOff + (NWG == 2 ? 2 * R * D * 4 : 0);   // [2][R] logit multiplier per row
+  static constexpr int stgOff = pOff + 4 * pBytes;         // [2][R][128] f32 second group's O (8 rows)
+  static constexpr int cOff = stgOff + (NT == 1 ? 2 * R * D * 4 : 0);   // [2][R] logit multiplier per row
   static constexpr int redOff = cOff + 2 * R * 4;          // [2][4][R] tile maxima per warp
   static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][4 NWG][R] row sums per warp
   static constexpr int msmOff = lredOff + 2 * 4 * NWG * R * 4;   // [2][NWG][R] row maxima per group
   static constexpr int infoOff = msmOff + 2 * NWG * R * 4; // [2] {item row, L, tiles, first tile group}
   static constexpr int scOff = infoOff + 2 * 16;           // EXT: [NS][K, V][128] f32 per-token scales
   static constexpr int barOff = (scOff + (EXT ? NS * 2 * TILE * 4 : 0) + 7) & ~7;
-  static constexpr int NBAR = 2 * NS + 2 * 10 + 4 + 1;
+  static constexpr int NBAR = 2 * NS + 27;
   static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag, QK total
   static constexpr int total = miscOff + 16 + 1024;        // + alignment slack
   static_assert(total <= 227 * 1024, "shared memory");
@@ -132,9 +132,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   uint64_t* sfree = sfull + 2;        // [2] S tile read (4 softmax warps)
   uint64_t* pfull = sfree + 2;        // [4] P' buffer written (4 softmax warps)
   uint64_t* ofull = pfull + 4;        // [4] O buffer ready (PV commit)
-  uint64_t* xbar = ofull + 4;         // [2] tile maxima exchanged (4 softmax warps)
-  uint64_t* merge = xbar + 2;         // [2] item states published (softmax warps)
-  uint64_t* mfree = merge + 2;        // [2] item states read (first group's 4 warps)
+  uint64_t* xbar = ofull + 4;         // [2 S buffers][2 row blocks] tile maxima exchanged (a group's 4 warps)
+  uint64_t* merge = xbar + 4;         // [2][2] item states published (softmax warps)
+  uint64_t* mfree = merge + 4;        // [2] item states read (the merging group's 4 warps)
   uint64_t* done = mfree + 2;         // [1] all MMAs finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::miscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::miscOff + 4);
@@ -157,17 +157,22 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       mbar_init(&full[i], 128);
       mbar_init(&empty[i], 1);
     }
+    // 8 rows: the two groups take alternate tiles (one group reads an S
+    // buffer, writes a P' buffer); 16 rows: each group owns 8 rows of every tile
+    constexpr int SPLIT_READERS = NT == 2 ? 8 : 4;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 4);
       mbar_init(&qempty[i], 1 + 4 * NWG);
       mbar_init(&sfull[i], 1);
-      mbar_init(&sfree[i], 4);
-      mbar_init(&pfull[i], 4);
-      mbar_init(&pfull[2 + i], 4);
+      mbar_init(&sfree[i], SPLIT_READERS);
+      mbar_init(&pfull[i], SPLIT_READERS);
+      mbar_init(&pfull[2 + i], SPLIT_READERS);
       mbar_init(&ofull[i], 1);
       mbar_init(&ofull[2 + i], 1);
       mbar_init(&xbar[i], 4);
-      mbar_init(&merge[i], 4 * NWG);
+      mbar_init(&xbar[2 + i], 4);
+      mbar_init(&merge[i], NT == 2 ? 4 : 4 * NWG);
+      mbar_init(&merge[2 + i], NT == 2 ? 4 : 4 * NWG);
       mbar_init(&mfree[i], 4);
     }
     mbar_init(done, 2);
@@ -201,36 +206,43 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 
   if (warp < WARP_PROD0) {
     // ======================================================== softmax warps
-    // NWG groups of 4 warps; with two groups, group g takes the tiles j with
-    // j & 1 == g (buffer b = g) and the groups merge their states per item.
+    // Two groups of 4 warps. With 8 query rows group g takes the tiles j with
+    // j & 1 == g (buffer b = g) and the groups merge their states per item;
+    // with 16 rows (row split) group g owns rows 8g .. 8g + 7 of every tile,
+    // reads its 32 columns of S and O and writes its 32 columns of P', and
+    // finishes its own rows. Either way a thread carries RG = 8 rows.
+    constexpr bool RS = NT == 2;
+    constexpr int RG = 8;
+    constexpr int NG = RS ? 2 : 1;                     // row blocks
     const int wg = warp >> 2;
     const int wq = warp & 3;                           // lane quarter of tensor memory
     const int t = threadIdx.x & 127;                   // tensor-memory lane
     const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
     const float vscale = per_token ? 1.f : __ldg(p.v_scale);
-    const uint32_t ptok = psm + (t >> 3) * (8 * NQ) + (t & 7) * 16;   // this token's P' row
-    float m[R], l[R], o[R], c[R];
+    const int rblk = RS ? wg : 0;                      // this group's row block
+    // this token's P' row, the group's 32 columns
+    const uint32_t ptok = psm + (t >> 3) * (8 * NQ) + (t & 7) * 16 + 256 * rblk;
+    float m[RG], l[RG], o[RG], c[RG];
 #pragma unroll
-    for (int r = 0; r < R; ++r) { o[r] = 0.f; m[r] = -INFINITY; l[r] = 0.f; c[r] = 0.f; }
+    for (int r = 0; r < RG; ++r) { o[r] = 0.f; m[r] = -INFINITY; l[r] = 0.f; c[r] = 0.f; }
     int j = 0, qcnt = 0;
     bool ok = true;
     int pend_j = -1;                     // this group's tile whose O is not folded in yet
-    float pend_alpha[R];
+    float pend_alpha[RG];
 #pragma unroll
-    for (int r = 0; r < R; ++r) pend_alpha[r] = 0.f;
+    for (int r = 0; r < RG; ++r) pend_alpha[r] = 0.f;
     // O of tile pend_j (rescale factor pend_alpha) into the accumulators
     auto fold = [&]() -> bool {
       const int ob = 2 * (pend_j & 1) + ((pend_j >> 1) & 1);
       if (!warp_wait(&ofull[ob], (pend_j >> 2) & 1, abort_flag, KERR_TIMEOUT_FULL)) return false;
       tc_fence_after();
-      float w[NQ];
-#pragma unroll
-      for (int h = 0; h < NT; ++h) tmem_ld32(tl + 2 * NQ + ob * NQ + 32 * h, *reinterpret_cast<float(*)[32]>(w + 32 * h));
+      float w[32];
+      tmem_ld32(tl + 2 * NQ + ob * NQ + 32 * rblk, w);
       tmem_wait_ld();
       tc_fence_before();
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float sv = fmaf(fmaf(w[2 * R + r], 0.0625f, w[R + r]), 0.0625f, w[r]);
+      for (int r = 0; r < RG; ++r) {
+        const float sv = fmaf(fmaf(w[2 * RG + r], 0.0625f, w[RG + r]), 0.0625f, w[r]);
         o[r] = fmaf(sv, 0.00390625f, o[r] * pend_alpha[r]);
       }
       return true;
@@ -243,8 +255,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       if (!warp_wait(&qfull[qb], (qcnt >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
       const int4 inf = lds_i4(info_s + 16 * qb);
 #pragma unroll
-      for (int q4 = 0; q4 < R / 4; ++q4) {
-        const float4 cv = lds_f4(cbuf_s + 4 * (qb * R + 4 * q4));
+      for (int q4 = 0; q4 < RG / 4; ++q4) {
+        const float4 cv = lds_f4(cbuf_s + 4 * (qb * R + RG * rblk + 4 * q4));
         c[4 * q4] = cv.x;
         c[4 * q4 + 1] = cv.y;
         c[4 * q4 + 2] = cv.z;
@@ -255,27 +267,26 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       const int item = inf.x, L = inf.y, nt = inf.z, tg0 = inf.w;   // tiles of tile groups tg0, tg0 + 1, ...
       if (nt == 0) break;
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
+      for (int r = 0; r < RG; ++r) {
         m[r] = -INFINITY;
         l[r] = 0.f;
       }
       for (int i = 0; i < nt; ++i, ++j) {
-        if (NWG == 2 && (j & 1) != wg) continue;
+        if (!RS && (j & 1) != wg) continue;
         const int start = (tg0 + (i >> 1)) * TG + (i & 1) * TILE;
         const int b = j & 1;                 // S buffer
         const int ob = 2 * b + ((j >> 1) & 1);   // P' and O buffer (alternate per group)
         // ---- softmax of tile j
         if (!warp_wait(&sfull[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
         tc_fence_after();
-        float v[NQ];
-#pragma unroll
-        for (int h = 0; h < NT; ++h) tmem_ld32(tl + b * NQ + 32 * h, *reinterpret_cast<float(*)[32]>(v + 32 * h));
+        float v[32];
+        tmem_ld32(tl + b * NQ + 32 * rblk, v);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfree[b]);
         const bool valid = start + t < L;
-        float x[R];
+        float x[RG];
         float vs_t = 1.f;                    // this token's V scale (EXT, per token)
         if constexpr (EXT) {
           float ks_t = 1.f;
@@ -286,40 +297,40 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             vs_t = valid ? ldsf(sc_s + 4 * ((j % NS) * 2 * TILE + TILE + t)) : 0.f;
           }
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            // row r = qoff * qg + g sees the tokens below L - QL + 1 + qoff
-            const float sv = fmaf(fmaf(fmaf(v[3 * R + r], 0.0625f, v[2 * R + r]), 0.0625f, v[R + r]), 0.0625f, v[r]);
-            x[r] = (start + t < L - QL + 1 + r / p.qg) ? sv * c[r] * ks_t : -INFINITY;
+          for (int r = 0; r < RG; ++r) {
+            // row qoff * qg + g sees the tokens below L - QL + 1 + qoff
+            const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
+            x[r] = (start + t < L - QL + 1 + (RG * rblk + r) / p.qg) ? sv * c[r] * ks_t : -INFINITY;
           }
         } else {
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const float sv = fmaf(fmaf(fmaf(v[3 * R + r], 0.0625f, v[2 * R + r]), 0.0625f, v[R + r]), 0.0625f, v[r]);
+          for (int r = 0; r < RG; ++r) {
+            const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
             x[r] = valid ? sv * c[r] : -INFINITY;
           }
         }
         {
           // row maxima over the warp's 32 tokens (hardware warp reduction)
-          float mx[R];
+          float mx[RG];
 #pragma unroll
-          for (int r = 0; r < R; ++r) mx[r] = warp_max(x[r]);
+          for (int r = 0; r < RG; ++r) mx[r] = warp_max(x[r]);
           if (lane == 0) {
 #pragma unroll
-            for (int q4 = 0; q4 < R / 4; ++q4)
-              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red_s + 4 * ((b * 4 + wq) * R + 4 * q4)),
+            for (int q4 = 0; q4 < RG / 4; ++q4)
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red_s + 4 * (((b * NG + rblk) * 4 + wq) * RG + 4 * q4)),
                            "f"(mx[4 * q4]), "f"(mx[4 * q4 + 1]), "f"(mx[4 * q4 + 2]), "f"(mx[4 * q4 + 3]) : "memory");
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xbar[b]);
-        if (!warp_wait(&xbar[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
-        float alpha[R];
+        if (lane == 0) mbar_arrive(&xbar[2 * b + rblk]);
+        if (!warp_wait(&xbar[2 * b + rblk], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
+        float alpha[RG];
         {
-          const uint32_t rb = red_s + b * 4 * R * 4;
+          const uint32_t rb = red_s + (b * NG + rblk) * 4 * RG * 4;
 #pragma unroll
-          for (int q4 = 0; q4 < R / 4; ++q4) {
-            const float4 a0 = lds_f4(rb + 16 * q4), a1 = lds_f4(rb + 16 * (R / 4 + q4));
-            const float4 a2 = lds_f4(rb + 16 * (2 * R / 4 + q4)), a3 = lds_f4(rb + 16 * (3 * R / 4 + q4));
+          for (int q4 = 0; q4 < RG / 4; ++q4) {
+            const float4 a0 = lds_f4(rb + 16 * q4), a1 = lds_f4(rb + 16 * (RG / 4 + q4));
+            const float4 a2 = lds_f4(rb + 16 * (2 * RG / 4 + q4)), a3 = lds_f4(rb + 16 * (3 * RG / 4 + q4));
             const float tm[4] = {fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x)), fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y)),
                                  fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z)), fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w))};
 #pragma unroll
@@ -333,9 +344,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           }
         }
         // probabilities (f16), the row sums, and P' = 3 e4m3 terms of 256 p
-        uint32_t tw[3][R / 4];
+        uint32_t tw[3][RG / 4];
 #pragma unroll
-        for (int k = 0; k < R / 2; ++k) {
+        for (int k = 0; k < RG / 2; ++k) {
           float pa0, pa1;
           if constexpr (EXT) {
             pa0 = x[2 * k] == -INFINITY ? 0.f : ex2(x[2 * k] - m[2 * k]);
@@ -366,20 +377,12 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           }
         }
         {
+          // columns slot * 8 + row of the group's 32: terms 0, 1 | term 2, zero slot
           const uint32_t pb = ptok + ob * S::pBytes;
-          if constexpr (NT == 1) {
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(tw[0][0]), "r"(tw[0][1]),
-                         "r"(tw[1][0]), "r"(tw[1][1]) : "memory");
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(tw[2][0]), "r"(tw[2][1]),
-                         "r"(0u), "r"(0u) : "memory");
-          } else {
-#pragma unroll
-            for (int q = 0; q < 3; ++q)
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128 * q), "r"(tw[q][0]),
-                           "r"(tw[q][1]), "r"(tw[q][2]), "r"(tw[q][3]) : "memory");
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 384), "r"(0u), "r"(0u), "r"(0u),
-                         "r"(0u) : "memory");
-          }
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(tw[0][0]), "r"(tw[0][1]),
+                       "r"(tw[1][0]), "r"(tw[1][1]) : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(tw[2][0]), "r"(tw[2][1]),
+                       "r"(0u), "r"(0u) : "memory");
         }
         fence_proxy_async();
         __syncwarp();
@@ -388,98 +391,101 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         if (pend_j >= 0 && !fold()) { ok = false; break; }
         pend_j = j;
 #pragma unroll
-        for (int r = 0; r < R; ++r) pend_alpha[r] = alpha[r];
+        for (int r = 0; r < RG; ++r) pend_alpha[r] = alpha[r];
       }
       if (ok && pend_j >= 0 && !fold()) ok = false;
       pend_j = -1;
       if (!ok) break;
 
-      // ---- item done: row sums over the group's 128 token lanes, merge of the
-      // groups' (m, l, O) to a common maximum, partials of the item. The group
-      // that does not own the item's last tile merges: it finished first, and
-      // with an even tile count per item the owner of the last tile would
-      // otherwise always be the same group, which then carries every merge.
+      // ---- item done: row sums over the group's 128 token lanes, then the
+      // item's partials. 8 rows: the groups' (m, l, O) merge to a common
+      // maximum; the group that does not own the item's last tile merges (it
+      // finished first, and with an even tile count per item the owner of the
+      // last tile would otherwise always be the same group, which then carries
+      // every merge). 16 rows: each group finishes its own 8 rows.
       const uint32_t kph = (qcnt >> 1) & 1;
-      const int merger = NWG == 2 ? (j & 1) : 0;
+      const int merger = RS ? wg : (j & 1);
+      uint64_t* mbar = &merge[RS ? 2 * qb + wg : qb];
       // (the buffers of item qcnt - 2 must have been read by its merger)
-      if (NWG == 2 && qcnt >= 2 &&
+      if (!RS && qcnt >= 2 &&
           !warp_wait(&mfree[qb], ((qcnt >> 1) - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) { ok = false; break; }
       {
-        float lr[R];
+        float lr[RG];
 #pragma unroll
-        for (int r = 0; r < R; ++r) lr[r] = l[r];
-        const float ls = transpose_reduce<R, false>(lr, lane);
-        if ((lane & (32 / R - 1)) == 0) stsf(lred_s + 4 * ((qb * 4 * NWG + warp) * R + lane / (32 / R)), ls);
+        for (int r = 0; r < RG; ++r) lr[r] = l[r];
+        const float ls = transpose_reduce<RG, false>(lr, lane);
+        if ((lane & (32 / RG - 1)) == 0) stsf(lred_s + 4 * ((qb * 4 * NWG + warp) * RG + lane / (32 / RG)), ls);
       }
       if (t == 0) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) stsf(msm_s + 4 * ((qb * NWG + wg) * R + r), m[r]);
+        for (int r = 0; r < RG; ++r) stsf(msm_s + 4 * ((qb * NWG + wg) * RG + r), m[r]);
       }
-      if (NWG == 2 && wg != merger) {
+      if (!RS && wg != merger) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) stsf(stg_s + 4 * ((qb * R + r) * D + t), o[r]);
+        for (int r = 0; r < RG; ++r) stsf(stg_s + 4 * ((qb * RG + r) * D + t), o[r]);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&merge[qb]);
+      if (lane == 0) mbar_arrive(mbar);
       if (wg == merger) {
-        if (!warp_wait(&merge[qb], kph, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
-        const uint32_t lr = lred_s + qb * 4 * NWG * R * 4;
-        const uint32_t mr = msm_s + qb * NWG * R * 4;
+        if (!warp_wait(mbar, kph, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
+        const uint32_t lr = lred_s + qb * 4 * NWG * RG * 4;
+        const uint32_t mr = msm_s + qb * NWG * RG * 4;
         const long long row0 = (long long)item * rows;
-        float lsum[NWG][R], mg[NWG][R];
+        // [0]: this group, [1]: the other (8 rows only)
+        float lsum[2][RG], mg[2][RG];
 #pragma unroll
-        for (int g = 0; g < NWG; ++g)
+        for (int gi = 0; gi < (RS ? 1 : 2); ++gi) {
+          const int g = gi == 0 ? wg : 1 - wg;
 #pragma unroll
-          for (int q4 = 0; q4 < R / 4; ++q4) {
-            const float4 a0 = lds_f4(lr + 16 * ((4 * g) * R / 4 + q4)), a1 = lds_f4(lr + 16 * ((4 * g + 1) * R / 4 + q4));
-            const float4 a2 = lds_f4(lr + 16 * ((4 * g + 2) * R / 4 + q4)), a3 = lds_f4(lr + 16 * ((4 * g + 3) * R / 4 + q4));
-            const float4 mm = lds_f4(mr + 16 * (g * R / 4 + q4));
-            lsum[g][4 * q4] = (a0.x + a1.x) + (a2.x + a3.x);
-            lsum[g][4 * q4 + 1] = (a0.y + a1.y) + (a2.y + a3.y);
-            lsum[g][4 * q4 + 2] = (a0.z + a1.z) + (a2.z + a3.z);
-            lsum[g][4 * q4 + 3] = (a0.w + a1.w) + (a2.w + a3.w);
-            mg[g][4 * q4] = mm.x;
-            mg[g][4 * q4 + 1] = mm.y;
-            mg[g][4 * q4 + 2] = mm.z;
-            mg[g][4 * q4 + 3] = mm.w;
+          for (int q4 = 0; q4 < RG / 4; ++q4) {
+            const float4 a0 = lds_f4(lr + 16 * ((4 * g) * RG / 4 + q4)), a1 = lds_f4(lr + 16 * ((4 * g + 1) * RG / 4 + q4));
+            const float4 a2 = lds_f4(lr + 16 * ((4 * g + 2) * RG / 4 + q4)), a3 = lds_f4(lr + 16 * ((4 * g + 3) * RG / 4 + q4));
+            const float4 mm = lds_f4(mr + 16 * (g * RG / 4 + q4));
+            lsum[gi][4 * q4] = (a0.x + a1.x) + (a2.x + a3.x);
+            lsum[gi][4 * q4 + 1] = (a0.y + a1.y) + (a2.y + a3.y);
+            lsum[gi][4 * q4 + 2] = (a0.z + a1.z) + (a2.z + a3.z);
+            lsum[gi][4 * q4 + 3] = (a0.w + a1.w) + (a2.w + a3.w);
+            mg[gi][4 * q4] = mm.x;
+            mg[gi][4 * q4 + 1] = mm.y;
+            mg[gi][4 * q4 + 2] = mm.z;
+            mg[gi][4 * q4 + 3] = mm.w;
           }
-        float other[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) other[r] = NWG == 2 ? ldsf(stg_s + 4 * ((qb * R + r) * D + t)) : 0.f;
+        }
         float lt_mine = 0.f, mt_mine = 0.f;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
+        for (int r = 0; r < RG; ++r) {
           float mt = mg[0][r], lt = lsum[0][r], ot = o[r];
-          if (NWG == 2) {
+          if constexpr (!RS) {
             // (each group's maximum is -inf only if it saw no token of the item)
-            const float m_me = wg == 0 ? mg[0][r] : mg[NWG - 1][r], m_ot = wg == 0 ? mg[NWG - 1][r] : mg[0][r];
-            const float l_me = wg == 0 ? lsum[0][r] : lsum[NWG - 1][r], l_ot = wg == 0 ? lsum[NWG - 1][r] : lsum[0][r];
+            const float other = ldsf(stg_s + 4 * ((qb * RG + r) * D + t));
+            const float m_me = mg[0][r], m_ot = mg[1][r];
             mt = fmaxf(m_me, m_ot);
             const float a0 = (EXT && m_me == -INFINITY) ? 0.f : ex2(m_me - mt);
             const float a1 = (EXT && m_ot == -INFINITY) ? 0.f : ex2(m_ot - mt);
-            lt = l_me * a0 + l_ot * a1;
-            ot = o[r] * a0 + other[r] * a1;
+            lt = lsum[0][r] * a0 + lsum[1][r] * a1;
+            ot = o[r] * a0 + other * a1;
           }
           // (lt >= 1: the row maximum's own term is exactly 1; EXT: lt = 0 for a
           // row that saw no token)
-          if (r < rows && t < HD)
-            p.part_o[(row0 + r) * HD + t] = (EXT && lt == 0.f) ? 0.f : ot * (vscale * rcp_approx(lt));
+          const int row = RG * rblk + r;
+          if (row < rows && t < HD)
+            p.part_o[(row0 + row) * HD + t] = (EXT && lt == 0.f) ? 0.f : ot * (vscale * rcp_approx(lt));
           if (t == r) {
             lt_mine = lt;
             mt_mine = mt;
           }
         }
-        if (t < rows) {
-          p.part_m[row0 + t] = mt_mine * kLn2;
-          p.part_l[row0 + t] = lt_mine;
+        if (t < RG && RG * rblk + t < rows) {
+          p.part_m[row0 + RG * rblk + t] = mt_mine * kLn2;
+          p.part_l[row0 + RG * rblk + t] = lt_mine;
         }
-        if (NWG == 2) {
+        if (!RS) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&mfree[qb]);
         }
       }
 #pragma unroll
-      for (int r = 0; r < R; ++r) o[r] = 0.f;
+      for (int r = 0; r < RG; ++r) o[r] = 0.f;
       ++qcnt;
     }
   } else if (warp < WARP_MMA) {
@@ -691,7 +697,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
                 x[2 * k + 1] = (x[2 * k + 1] - f16_hi_to_f32(back)) * 16.f;
               }
             }
-            const int rr = term * R + row;
+            const int rr = (row >> 3) * 32 + term * 8 + (row & 7);   // S / P' column layout
             const uint32_t addr = qsm + qb * S::qBytes + rr * D + (((h16 >> 1) ^ (rr & 7)) << 4) + 8 * (h16 & 1);
             if (h16 < HD / 8)
               asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(e[0] | (e[1] << 16)),
