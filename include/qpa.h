@@ -102,7 +102,8 @@ int qpa_kernel_error(void* stream);
  *               (sum of exp(logit - m), 0 for an empty slot); O is
  *               normalised by l and already multiplied by v_scale. The
  *               combine reads O only where l > 0 and m > -inf.
- * Supported: head_dim 128, query_group 1..16, block_size 16/32/64/128/256.
+ * Supported: head_dim 64 or 128 ([PA]), query_group 1..16, block_size
+ * 16/32/64/128/256. Layouts above with head_dim in place of 128.
  * Alignment: q, kv_cache and out 16-byte aligned.
  * ====================================================================== */
 typedef struct qpa_fp8_desc {
