@@ -405,13 +405,22 @@ def _barrier():
 
 
 def _max_over_ranks(x):
+    """The largest x over the ranks (each rank times its own replica; the job
+    takes as long as the slowest)."""
     if not _DIST["on"]:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _aggregate_gbs(bytes_per_rank, ms_max, world):
+    """Whole-job throughput: the bytes all ranks processed (every rank runs a
+    replica of the workload) over the slowest rank's time per step."""
+    return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
 
 
 def _profile_case(a):
@@ -498,14 +507,14 @@ def main():
     ms, part_ms, comb_ms, launches, clocks, total_ms = time_fp8(c, P, a.steps, a.warmup, dev, sampler)
     ms_max = _max_over_ranks(ms)
     kv = c.kv_bytes
-    value = kv * world / (ms_max * 1e-3) / 1e9
+    value = _aggregate_gbs(kv, ms_max, world)
     part_gbs = kv / (part_ms * 1e-3) / 1e9
 
     e2e = None
     if not a.no_e2e:
         e_ms, h2d, d2h = time_e2e(c, P, max(3, min(a.steps, 10)), dev)
         e_ms = _max_over_ranks(e_ms)
-        e2e = {"value": round(kv * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e2e = {"value": round(_aggregate_gbs(kv, e_ms, world), 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4)}
 
     extra = {}
