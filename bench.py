@@ -579,6 +579,19 @@ def main():
             "kv_bytes": ci.kv_bytes,
             "gbs": round(ci.kv_bytes / (i_ms * 1e-3) / 1e9, 1),
             "frac_of_peak": round(ci.kv_bytes / (i_ms * 1e-3) / 1e9 / peak, 4)}
+        cs = synth.idx_shared_prefix(seed=1007 + rank)
+        s_ms, _ = time_idx(cs, esteps, a.warmup, dev)
+        s_ms = _max_over_ranks(s_ms)
+        extra["nvfp4_index_score_64req_shared_prefix"] = {
+            "workload": "NVFP4 paged index scorer, 64 requests, lengths U[16384,32768], the first 16384 tokens "
+                        "(128 pages) shared by all requests, query_len 4, 2 heads, S=256",
+            "us_per_step": round(s_ms * 1e3, 2), "l2": "flushed (256 MB write, then read) before every timed step",
+            "kv_bytes": cs.kv_bytes, "unique_page_bytes": cs.unique_page_bytes,
+            "gbs": round(cs.kv_bytes / (s_ms * 1e-3) / 1e9, 1),
+            "gbs_unique": round(cs.unique_page_bytes / (s_ms * 1e-3) / 1e9, 1),
+            "kv_bytes_is": "pages per (request, block) as the scorer processes them; unique_page_bytes counts a "
+                           "shared page once"}
+        del cs
         t_ms, _ = time_idx(ci, esteps, a.warmup, dev, per_token_cols=32768)
         t_ms = _max_over_ranks(t_ms)
         out_bytes = ci.num_heads * ci.num_reqs * ci.query_len * 32768 * 4

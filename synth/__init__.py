@@ -478,17 +478,28 @@ class IdxCase:
         nblk = (self.seq_lens.astype(np.int64) + IDX_BLK - 1) // IDX_BLK
         return int(nblk.sum()) * IDX_PAGE
 
+    @property
+    def unique_page_bytes(self) -> int:
+        """Bytes of the distinct physical pages the requests map."""
+        nblk = (self.seq_lens.astype(np.int64) + IDX_BLK - 1) // IDX_BLK
+        ids = np.concatenate([self.block_table[s, :n] for s, n in enumerate(nblk)]) if len(nblk) else []
+        return int(np.unique(ids).size) * IDX_PAGE
+
 
 def make_idx_case(seed: int, seq_lens, query_len: int = 4, num_heads: int = 2,
                   num_blocks: int | None = None, num_cols: int | None = None,
-                  poison: bool = True, chunk_pages: int = 512) -> IdxCase:
+                  poison: bool = True, chunk_pages: int = 512, shared_prefix_blocks: int = 0) -> IdxCase:
+    """shared_prefix_blocks: the first that many blocks of every request map
+    to the same physical pages (a prefix shared by all requests); the other
+    blocks get pages of their own."""
     r = rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     R = seq_lens.shape[0]
     nblk = [int(math.ceil(int(L) / IDX_BLK)) for L in seq_lens]
     max_blocks = max(1, max(nblk))
+    SP = int(shared_prefix_blocks)
     if num_blocks is None:
-        num_blocks = max(1, sum(nblk))
+        num_blocks = max(1, SP + sum(max(0, n - SP) for n in nblk) if SP else sum(nblk))
     if num_cols is None:
         num_cols = max_blocks
     q_codes = round_to_e4m3_bytes(r.standard_normal((R * query_len, num_heads, IDX_D),
@@ -502,11 +513,21 @@ def make_idx_case(seed: int, seq_lens, query_len: int = 4, num_heads: int = 2,
         codes = pack_nibbles(round_to_e2m1_codes(k / scf))
         pages[o:o + n, :8192] = codes.reshape(n, 8192)
         pages[o:o + n, 8192:] = sc.reshape(n, 1024)
-    bt = _assign_blocks(r, nblk, num_blocks, max_blocks)
+    if SP:
+        perm = r.permutation(num_blocks).astype(np.int32)
+        bt = np.full((R, max_blocks), -1, dtype=np.int32)
+        off = SP
+        for s, n in enumerate(nblk):
+            k = min(n, SP)
+            bt[s, :k] = perm[:k]
+            bt[s, k:n] = perm[off:off + n - k]
+            off += n - k
+    else:
+        bt = _assign_blocks(r, nblk, num_blocks, max_blocks)
     if poison:
         for s in range(R):
             L = int(seq_lens[s])
-            if L % IDX_BLK and nblk[s]:
+            if L % IDX_BLK and nblk[s] > SP:          # never poison a shared page
                 blk = bt[s, nblk[s] - 1]
                 t0 = L % IDX_BLK
                 pages[blk, 8192 + 8 * t0:] = 0x7F   # NaN scales past the end
@@ -518,3 +539,11 @@ def idx_full(seed: int = 1004) -> IdxCase:
     r = rng(seed + 7)
     lens = r.integers(4096, 32768 + 1, size=64).astype(np.int32)
     return make_idx_case(seed, lens, 4, 2, num_cols=256, poison=False)
+
+
+def idx_shared_prefix(seed: int = 1007) -> IdxCase:
+    """64 requests, lengths U[16384, 32768], query_len 4, 2 index heads, the
+    first 16384 tokens (128 pages) shared by all requests."""
+    r = rng(seed + 7)
+    lens = r.integers(16384, 32768 + 1, size=64).astype(np.int32)
+    return make_idx_case(seed, lens, 4, 2, num_cols=256, poison=False, shared_prefix_blocks=128)

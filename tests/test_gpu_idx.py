@@ -109,3 +109,24 @@ def test_per_token_full_config_sampled():
     reqs = sorted({3, 40, int(np.argmin(c.seq_lens)), int(np.argmax(c.seq_lens))})
     rows = [r * 4 + q for r in reqs for q in range(4)]
     check_scores(got, _ref_tok(c, 32768, reqs=reqs), rows=rows, what="idx-full per-token")
+
+
+def test_shared_prefix_pages():
+    """Requests whose first blocks map the same physical pages (a shared
+    prefix): every request's scores against the oracle."""
+    c = synth.make_idx_case(350, [300, 700, 1000, 256, 129, 900], query_len=4, num_heads=2, num_cols=9,
+                            shared_prefix_blocks=2)
+    assert np.all(c.block_table[:, :2] == c.block_table[0, :2])
+    got = IdxDev(c).run().cpu().double().numpy()
+    check_scores(got, _ref(c), what="shared prefix")
+
+
+def test_shared_prefix_full_sampled():
+    """64 requests, lengths U[16384, 32768], 128 shared prefix pages (the
+    benchmark's shared-prefix line); 4 requests against the oracle."""
+    c = synth.idx_shared_prefix()
+    got = IdxDev(c).run().cpu().double().numpy()
+    assert not np.any(np.isnan(got))
+    reqs = [0, 17, int(np.argmin(c.seq_lens)), int(np.argmax(c.seq_lens))]
+    rows = [r * 4 + q for r in sorted(set(reqs)) for q in range(4)]
+    check_scores(got, _ref(c, reqs=sorted(set(reqs))), rows=rows, what="shared prefix full")
