@@ -167,9 +167,10 @@ int pa_decode_fp8_combine(int num_partitions, void* out, const qpa_fp8_desc* d,
  *   workspace pa_decode_fp8_ext_workspace_size() bytes: float32
  *             O [num_seqs][num_kv_heads][P][query_len*query_group][128] and m,
  *             l [num_seqs][num_kv_heads][P][query_len*query_group], row
- *             qoff*query_group + g; O includes the V scale. Partition p owns
- *             the 256-token tile groups p, p+P, ... ([UQ] step F); an empty
- *             one writes m = -inf, l = 0, O = 0.
+ *             qoff*query_group + g; O includes the V scale. Slots hold runs
+ *             of tile groups as for pa_decode_fp8 (empty slot: m = -inf,
+ *             l = 0, O not written); a row that sees no token of a run has
+ *             m = -inf, l = 0, O = 0 in that slot.
  * Supported: head_dim 128, block_size 16..256, query_len 1..4 with
  * query_len * query_group <= 16. Errors as pa_decode_fp8; an unsupported
  * query_len or row count is QPA_ERR_SHAPE.
