@@ -16,12 +16,12 @@ gives 0 ([UQ] STEP G divides by a sum clamped to 1 when it is 0).
 
 The partition rewrite (``partition_partials`` + ``combine_partials``) is the
 same result split over P partitions: partition p owns the 256-token tile
-groups p, p+P, p+2P, ... ([UQ] STEP F, "tile-groups are always strided"),
+groups p, p+P, p+2P, ... ([UQ] STEP F: the tile groups of a partition are strided by P),
 keeps (m_p, l_p, O_p) = (max logit, sum of exp(logit - m_p),
 sum exp(logit - m_p) v / l_p), an empty partition gives (-inf, 0, 0)
 ([PA] NaN-guard commit), and the combine takes M = max_p m_p,
-w_p = l_p e^(m_p - M), out = sum_p w_p O_p / sum_p w_p ([PA] "parallel
-flash-combine reduce kernel").
+w_p = l_p e^(m_p - M), out = sum_p w_p O_p / sum_p w_p ([PA], its
+cross-partition reduce kernel).
 
 Pins (tests/test_oracle_attention.py): a 2-token case built so the softmax
 weights are exactly 1/4 and 3/4; L = 1 gives v_0; constant V gives the
