@@ -1,5 +1,6 @@
-// fp8 (e4m3fn, per-tensor scale) paged-attention decode: split-KV partition
-// kernel and flash-combine kernel.
+// fp8 (e4m3fn) paged-attention decode: split-KV partition kernel (head_dim
+// 64 or 128, up to 16 query rows per KV head, a multi-token / per-token-scale
+// variant) and flash-combine kernel.
 //
 // What it computes follows the ROCm/FlyDSL PR #825 page ("perf(pa tile):
 // readable tile-programming PA decode kernel": per-tensor fp8 K/V, query
@@ -24,11 +25,14 @@
 //    thread), XOR-swizzled so that each slot is the 128-byte-swizzle canonical
 //    layout the tensor core reads; tokens past the sequence length are
 //    zero-filled. The copy warps also build the item's query operand.
-//  * 1 MMA warp issues tcgen05.mma kind::f8f6f4 straight on the e4m3 bytes:
-//    S^T = K Q'^T (M = 128 tokens, N = 32) and O^T = V^T P'^T (M = 128 dims,
-//    N = 32), accumulators in tensor memory (two S and two O buffers).
-//  * 4 softmax warps: thread t owns tensor-memory lane t, i.e. token t of an
-//    S tile and dim t of an O tile. They turn S into probabilities (online
+//  * a QK warp and a PV warp issue tcgen05.mma kind::f8f6f4 straight on the
+//    e4m3 bytes: S^T = K Q'^T (M = 128 tokens, N = 32 or 64) and
+//    O^T = V^T P'^T (M = 128 dims, N = 32 or 64), accumulators in tensor
+//    memory (two S and four O buffers).
+//  * two groups of 4 softmax warps: thread t owns tensor-memory lane t, i.e.
+//    token t of an S tile and dim t of an O tile. With up to 8 query rows the
+//    groups take alternate tiles and merge per item; with 16 rows each group
+//    owns 8 rows of every tile. They turn S into probabilities (online
 //    softmax across the item's tiles), write P' for the next MMA, and fold
 //    each O tile into per-dim register accumulators with the softmax rescale.
 // Exactness: the query (bf16) and the probabilities (f16) enter the fp8 MMA
@@ -67,9 +71,9 @@ struct Smem {
   static constexpr int pOff = qOff + 2 * qBytes;
   static constexpr int stgOff = pOff + 4 * pBytes;         // [2][R][128] f32 second group's O (8 rows)
   static constexpr int cOff = stgOff + (NT == 1 ? 2 * R * D * 4 : 0);   // [2][R] logit multiplier per row
-  static constexpr int redOff = cOff + 2 * R * 4;          // [2][4][R] tile maxima per warp
-  static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][4 NWG][R] row sums per warp
-  static constexpr int msmOff = lredOff + 2 * 4 * NWG * R * 4;   // [2][NWG][R] row maxima per group
+  static constexpr int redOff = cOff + 2 * R * 4;          // [2 S buffers][row blocks][4 warps][8] tile maxima
+  static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][8 warps][8] row sums per warp
+  static constexpr int msmOff = lredOff + 2 * 4 * NWG * R * 4;   // [2][2 groups][8] row maxima per group
   static constexpr int infoOff = msmOff + 2 * NWG * R * 4; // [2] {item row, L, tiles, first tile group}
   static constexpr int scOff = infoOff + 2 * 16;           // EXT: [NS][K, V][128] f32 per-token scales
   static constexpr int barOff = (scOff + (EXT ? NS * 2 * TILE * 4 : 0) + 7) & ~7;
@@ -83,14 +87,14 @@ struct Smem {
 
 struct Fp8Params {
   const uint16_t* q;          // bf16 bits
-  const uint8_t* kv;          // [NB][2][Hk][bs][128]
+  const uint8_t* kv;          // [NB][2][Hk][bs][head_dim]
   const int32_t* block_table;
   const int32_t* seq_lens;
   const float* k_scale;
   const float* v_scale;
-  float* part_o;              // [B][Hk][P][QG][D]
-  float* part_m;              // [B][Hk][P][QG]
-  float* part_l;              // [B][Hk][P][QG]
+  float* part_o;              // [B][Hk][P][rows][head_dim], rows = query_len * QG
+  float* part_m;              // [B][Hk][P][rows]
+  float* part_l;              // [B][Hk][P][rows]
   long long q_stride_seq, q_stride_head;   // elements
   int num_seqs, num_kv_heads, qg, block_size, log2_bs, num_blocks, max_blocks, num_partitions;
   float softmax_scale;
