@@ -81,15 +81,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-// 2-D tile load global -> shared, completion counted on an mbarrier.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int x, int y,
-                                            uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y),
-        "r"(smem_u32(bar)), "l"(policy) : "memory");
-}
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple
 // of 16), completion counted on an mbarrier.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -131,25 +122,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// The 8 copies of one 16-row x 128-byte K chunk and its V chunk (4 KB) into a
-// shared slot with the 128-byte XOR swizzle (chunk j of row r at j ^ (r & 7)).
-// Copy i (0..3) of K covers rows 4i..4i+3; lane l copies bytes 16 l of it.
-// d0 / d1 are the slot address plus this lane's swizzled offset for even /
-// odd i; src_k / src_v point at the chunk plus 16 l.
-__device__ __forceinline__ void cp_async_chunk_pair(uint32_t d0, uint32_t d1, const void* src_k,
-                                                    const void* src_v, uint64_t pol) {
-  asm volatile(
-      "cp.async.cg.shared.global.L2::cache_hint [%0], [%2], 16, %4;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%1+512], [%2+512], 16, %4;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0+1024], [%2+1024], 16, %4;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%1+1536], [%2+1536], 16, %4;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0+2048], [%3], 16, %4;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%1+2560], [%3+512], 16, %4;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%0+3072], [%3+1024], 16, %4;\n\t"
-      "cp.async.cg.shared.global.L2::cache_hint [%1+3584], [%3+1536], 16, %4;\n\t"
-      ::"r"(d0), "r"(d1), "l"(src_k), "l"(src_v), "l"(pol) : "memory");
-}
 
 // Half a scorer page: 4096 B of codes (lane l copies bytes 16 l + 512 i) and
 // 512 B of scales (lane l copies bytes 16 l).
@@ -300,15 +272,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 
 // ---------------------------------------------------------------- MMA
-// D += A(16x32 e4m3, row) * B(32x8 e4m3, col), f32 accumulate.
-__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 // D += A(16x16 f16, row) * B(16x8 f16, col), f32 accumulate.
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                               uint32_t a3, uint32_t b0, uint32_t b1) {
