@@ -56,7 +56,8 @@ int qpa_version(void);
 /* Synchronises `stream` (a cudaStream_t, NULL = legacy default stream), then
  * returns and clears the device error word of the current device: 0 when no
  * kernel reported a problem, otherwise a positive code (1, 2: a wait gave up
- * after its time limit; 3: an invalid block id was met). Returns QPA_ERR_CUDA
+ * after its time limit; 3: an invalid block id was met; 4: the fp8 work split
+ * produced an out-of-range slot, which its own bounds rule out). Returns QPA_ERR_CUDA
  * if the synchronisation fails. Diagnostic only; the decode entry points
  * never call it. */
 int qpa_kernel_error(void* stream);
