@@ -174,6 +174,63 @@ class OraclePool:
 
 
 # ------------------------------------------------------------------ GPU timing
+class L2Flush:
+    """Writes and then reads a 256 MB buffer (twice the 129 MB L2), so that the
+    next timed step starts with nothing of its inputs in L2; the read leaves
+    clean lines behind, so the timed kernels pay no write-back of the flush."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.words = self.buf.view(torch.int32)
+
+    def __call__(self):
+        self.buf.zero_()
+        self.words.sum()
+
+
+def time_replays(step, replays, warmup, flush):
+    """One step (a Python callable that only enqueues kernels) captured in a
+    CUDA graph and replayed `replays` times; each replay sits between its own
+    pair of CUDA events on the current stream, with the L2 flush before it,
+    outside the events. Returns (list of ms per replay, timing mode). If the
+    capture fails, the step's launches are timed directly the same way."""
+    import torch
+    for _ in range(warmup):
+        if flush:
+            flush()
+        step()
+    torch.cuda.synchronize()
+    run, mode = step, "direct launches"
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        g.replay()
+        torch.cuda.synchronize()
+        run, mode = g.replay, "cuda graph"
+    except Exception:
+        torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
+    _barrier()
+    torch.cuda.synchronize()
+    for i in range(replays):
+        if flush:
+            flush()
+        ev[i][0].record()
+        run()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    _barrier()
+    return [a.elapsed_time(b) for a, b in ev], mode
+
+
 def _device_inputs(c, dev):
     import numpy as np
     import torch
@@ -186,16 +243,8 @@ def _device_inputs(c, dev):
         vs=torch.tensor([c.v_scale], dtype=torch.float32, device=dev))
 
 
-def time_fp8(c, P, steps, warmup, dev, sampler=None):
-    """Times `steps` decode steps (partition then combine) back to back on the
-    current stream with CUDA events only at the two ends of the timed region,
-    so that the combine kernel's programmatic dependent launch overlaps the
-    partition kernel's tail as it does in use (an event recorded between the
-    two kernels would serialise them). A second pass of `steps` partition-only
-    launches, each between its own pair of CUDA events on the same stream,
-    gives the partition kernel's duration for the roofline. Returns (ms per
-    step, mean partition-kernel ms, step ms minus partition ms, kernel
-    launches in the timed step loop, clocks, total ms of the step loop)."""
+def fp8_steps(c, P, dev):
+    """(step, partition-only) callables of pa_decode_fp8 on a resident case."""
     import torch
     import quantized_paged_attention_gb300 as qpa
     x = _device_inputs(c, dev)
@@ -203,41 +252,30 @@ def time_fp8(c, P, steps, warmup, dev, sampler=None):
     ws = qpa.alloc_workspace(qpa.pa_decode_fp8_workspace_size(desc, P), dev)
     out = torch.empty(x["q"].shape, dtype=torch.float32, device=dev)
     args = (x["q"], x["kv"], x["bt"], x["sl"], x["ks"], x["vs"], P, desc, ws)
-    for _ in range(warmup):
+
+    def part():
         qpa.pa_decode_fp8_partition(*args)
+
+    def step():
+        part()
         qpa.pa_decode_fp8_combine(P, out, desc, ws)
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    _barrier()
-    torch.cuda.synchronize()
-    if sampler:
-        sampler.start()
-        time.sleep(0.05)
-    start.record()
-    for i in range(steps):
-        qpa.pa_decode_fp8_partition(*args)
-        qpa.pa_decode_fp8_combine(P, out, desc, ws)
-    end.record()
-    torch.cuda.synchronize()
-    clocks = sampler.stop() if sampler else None
-    _barrier()
-    total = start.elapsed_time(end)
-    # the partition kernel alone, each launch between its own events
+    return step, part
+
+
+def time_partition_events(part, steps):
+    """The partition kernel alone, `steps` launches each between its own CUDA
+    events on the launching stream (inputs larger than L2). Mean ms."""
+    import torch
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for i in range(steps):
         ev[i][0].record()
-        qpa.pa_decode_fp8_partition(*args)
+        part()
         ev[i][1].record()
     torch.cuda.synchronize()
-    part = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if qpa.kernel_error() != 0:
-        raise RuntimeError("device error word raised during the benchmark")
-    return total / steps, part, total / steps - part, 2 * steps, clocks, total
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
-def time_fp8_ext(c, P, steps, warmup, dev):
-    """Times `steps` calls of pa_decode_fp8_ext (partition + combine) back to
-    back between two CUDA events (the cache, 537 MB, is larger than L2)."""
+def fp8_ext_step(c, P, dev):
     import numpy as np
     import torch
     import quantized_paged_attention_gb300 as qpa
@@ -257,67 +295,11 @@ def time_fp8_ext(c, P, steps, warmup, dev):
 
     def step():
         qpa.pa_decode_fp8_ext(q, kv, bt, sl, ks, vs, P, c.query_group, out=out, workspace=ws, desc=desc)
-
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    _barrier()
-    a.record()
-    for _ in range(steps):
-        step()
-    b.record()
-    torch.cuda.synchronize()
-    _barrier()
-    if qpa.kernel_error() != 0:
-        raise RuntimeError("device error word raised during the benchmark")
-    return a.elapsed_time(b) / steps
+    return step
 
 
-def _time_loop(step_a, step_b, steps, warmup):
-    """Times `steps` steps (step_a = partition or whole kernel, step_b =
-    combine or None) with L2 flushed before every step: a 256 MB buffer, larger
-    than the 129 MB L2, is written and then read back between steps outside the
-    timed spans (these workloads are small enough to stay partly cached
-    otherwise). The read leaves L2 holding clean lines, so the timed kernel does
-    not pay for writing back the flush's dirty lines. A step is timed between
-    two CUDA events with nothing between its kernels; with a step_b, a second
-    pass times step_a alone the same way. Returns (mean ms per step, mean ms
-    of step_a)."""
-    import torch
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=torch.cuda.current_device())
-    flush_words = flush.view(torch.int32)
-
-    def flush_l2():
-        flush.zero_()
-        flush_words.sum()
-
-    for _ in range(warmup):
-        flush_l2()
-        step_a()
-        if step_b:
-            step_b()
-    torch.cuda.synchronize()
-
-    def timed(fns):
-        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(steps)]
-        _barrier()
-        torch.cuda.synchronize()
-        for i in range(steps):
-            flush_l2()
-            ev[i][0].record()
-            for fn in fns:
-                fn()
-            ev[i][1].record()
-        torch.cuda.synchronize()
-        _barrier()
-        return statistics.mean(a.elapsed_time(b) for a, b in ev)
-
-    step = timed([step_a, step_b] if step_b else [step_a])
-    return step, (timed([step_a]) if step_b else step)
-
-
-def time_uq(c, P, steps, warmup, dev, q_haircut=False):
+def uq_steps(c, P, dev, q_haircut=False):
+    """(step, partition-only) callables of uq_decode_hd256."""
     import numpy as np
     import torch
     import quantized_paged_attention_gb300 as qpa
@@ -330,14 +312,17 @@ def time_uq(c, P, steps, warmup, dev, q_haircut=False):
                        q_haircut=q_haircut, rot_perm=c.rot_perm)
     ws = qpa.alloc_workspace(qpa.uq_decode_hd256_workspace_size(desc, P), dev)
     out = torch.empty((q.shape[0], q.shape[1], 256), dtype=torch.float32, device=dev)
-    r = _time_loop(lambda: qpa.uq_decode_hd256_partition(q, kv, cent, bt, sl, P, desc, ws),
-                   lambda: qpa.uq_decode_hd256_combine(P, out, desc, ws), steps, warmup)
-    if qpa.kernel_error() != 0:
-        raise RuntimeError("device error word raised during the benchmark")
-    return r
+
+    def part():
+        qpa.uq_decode_hd256_partition(q, kv, cent, bt, sl, P, desc, ws)
+
+    def step():
+        part()
+        qpa.uq_decode_hd256_combine(P, out, desc, ws)
+    return step, part
 
 
-def time_idx(c, steps, warmup, dev, per_token_cols=None):
+def idx_step(c, dev, per_token_cols=None):
     import torch
     import quantized_paged_attention_gb300 as qpa
     q = torch.from_numpy(c.q_codes).to(dev)
@@ -347,11 +332,16 @@ def time_idx(c, steps, warmup, dev, per_token_cols=None):
     cols = c.num_cols if per_token_cols is None else per_token_cols
     scores = torch.empty((c.num_heads, q.shape[0], cols), dtype=torch.float32, device=dev)
     desc = qpa.idx_desc(q, pages, bt, c.query_len, cols, scores, per_token=per_token_cols is not None)
-    r = _time_loop(lambda: qpa.nvfp4_index_score(q, pages, bt, sl, c.query_len, cols, scores=scores,
-                                                 desc=desc), None, steps, warmup)
+
+    def step():
+        qpa.nvfp4_index_score(q, pages, bt, sl, c.query_len, cols, scores=scores, desc=desc)
+    return step
+
+
+def _check_error_word():
+    import quantized_paged_attention_gb300 as qpa
     if qpa.kernel_error() != 0:
         raise RuntimeError("device error word raised during the benchmark")
-    return r
 
 
 def time_e2e(c, P, steps, dev):
@@ -423,29 +413,62 @@ def _aggregate_gbs(bytes_per_rank, ms_max, world):
     return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
 
 
+UQ_P = 147          # partitions of the full hd256 workload
+
+
 def _profile_case(a):
     """Small cases (larger than L2) of each kernel for profiling runs."""
     import numpy as np
     import torch
     import synth
     dev = torch.device("cuda", 0)
+    flush = L2Flush(dev)
     if a.profile_case == "fp8":
         c = synth.make_fp8_case(1001, [16384] * 8, 8, 8, 128, 16, poison=False)
-        ms, part, *_ = time_fp8(c, 32, a.steps, a.warmup, dev)
-        nbytes = c.kv_bytes
+        step, part = fp8_steps(c, 32, dev)
     elif a.profile_case in ("uq", "uq_rand"):
         cent = synth.sorted_random_centroids(5) if a.profile_case == "uq_rand" else None
         c = synth.uq_full(centroids=cent)
-        ms, part = time_uq(c, 147, a.steps, a.warmup, dev)
-        nbytes = c.kv_bytes
+        step, part = uq_steps(c, UQ_P, dev)
     else:
         r = synth.rng(1104)
         c = synth.make_idx_case(1004, r.integers(4096, 32769, size=128).astype(np.int32), 4, 2,
                                 num_cols=256, poison=False)
-        ms, part = time_idx(c, a.steps, a.warmup, dev)
-        nbytes = c.kv_bytes
-    print(f"profile case {a.profile_case}: {ms * 1e3:.1f} us/step, first kernel {part * 1e3:.1f} us, "
-          f"{nbytes / 1e6:.1f} MB, {nbytes / (part * 1e-3) / 1e9:.0f} GB/s")
+        step = part = idx_step(c, dev)
+    for _ in range(a.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(a.steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        part()
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    _check_error_word()
+    med = statistics.median(ms)
+    print(f"profile case {a.profile_case}: first kernel {med * 1e3:.1f} us (median of {len(ms)}), "
+          f"{c.kv_bytes / 1e6:.1f} MB, {c.kv_bytes / (med * 1e-3) / 1e9:.0f} GB/s")
+
+
+def _cfg_entry(times_ms, nbytes, peak, **kw):
+    """Compact per-config record: min and median us over the replays, and for
+    a byte count the GB/s and fraction of the HBM peak at the median."""
+    med, lo = statistics.median(times_ms), min(times_ms)
+    e = {"us_min": round(lo * 1e3, 2), "us_med": round(med * 1e3, 2)}
+    if nbytes:
+        gbs = nbytes / (med * 1e-3) / 1e9
+        e.update(gbs=round(gbs, 1), frac=round(gbs / peak, 3))
+    e.update(kw)
+    return e
+
+
+CONFIG = {"workload": WORKLOAD, "kv_bytes_per_step": 16 * 16384 * 8 * 256,
+          "l2": "flushed (256 MB written, then read) before every timed step",
+          "parallelism": "replicas"}
 
 
 def main():
@@ -480,7 +503,7 @@ def main():
                 "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
                 "ms_per_step": round(tot_t / a.steps * 1e3, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": WORKLOAD, "reference": "float64 CPU oracle (oracle/), host cores"},
+                "config": CONFIG,
                 "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": pool.cores,
                                  "kind": "oracle", "sample": sample},
                 "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -500,15 +523,27 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peak, peak_kind = _peaks()
+    flush = L2Flush(dev)
+    replays = max(50, a.steps)
 
+    # ---- the headline: fp8 GQA, 16 x 16384, 8 KV heads, group 8, P = 32
     c = synth.fp8_gqa(seed=1001 + rank)
     P = 32
+    step, part = fp8_steps(c, P, dev)
     sampler = ClockSampler(local) if rank == 0 else None
-    ms, part_ms, comb_ms, launches, clocks, total_ms = time_fp8(c, P, a.steps, a.warmup, dev, sampler)
+    if sampler:
+        sampler.start()
+        time.sleep(0.05)
+    times, mode = time_replays(step, a.steps, a.warmup, flush)
+    clocks = sampler.stop() if sampler else None
+    part_ms = time_partition_events(part, a.steps)
+    _check_error_word()
+    ms = statistics.median(times)
     ms_max = _max_over_ranks(ms)
     kv = c.kv_bytes
     value = _aggregate_gbs(kv, ms_max, world)
     part_gbs = kv / (part_ms * 1e-3) / 1e9
+    configs = {"c2_fp8_b16x16k_qg8": _cfg_entry(times, kv, peak)}
 
     e2e = None
     if not a.no_e2e:
@@ -516,93 +551,49 @@ def main():
         e_ms = _max_over_ranks(e_ms)
         e2e = {"value": round(_aggregate_gbs(kv, e_ms, world), 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4)}
+    del step, part
 
     extra = {}
     if not a.no_extra:
+        def run(step_fn, nbytes, **kw):
+            t, _ = time_replays(step_fn, replays, a.warmup, flush)
+            _check_error_word()
+            return _cfg_entry(t, nbytes, peak, **kw)
+
+        ct = synth.fp8_tiny()
+        configs["c1_fp8_tiny"] = run(fp8_steps(ct, 2, dev)[0], 0, note="launch-bound, 60.7 KB of KV")
         cr = synth.fp8_ragged(seed=1002 + rank)
-        r_ms, r_part, _, _, _, _ = time_fp8(cr, 32, max(20, a.steps // 4), a.warmup, dev)
-        r_ms = _max_over_ranks(r_ms)
-        extra["fp8_ragged_b128"] = {
-            "workload": "fp8 paged decode, 128 seqs, lengths U[1024,16384], 8 KV heads, group 8, block 16, P=32",
-            "us_per_step": round(r_ms * 1e3, 2), "partition_us": round(r_part * 1e3, 2),
-            "kv_bytes": cr.kv_bytes, "gbs": round(cr.kv_bytes / (r_ms * 1e-3) / 1e9, 1),
-            "frac_of_peak": round(cr.kv_bytes / (r_ms * 1e-3) / 1e9 / peak, 4)}
+        configs["c3_fp8_ragged_b128"] = run(fp8_steps(cr, 32, dev)[0], cr.kv_bytes)
         del cr
-        c64 = synth.make_fp8_case(1006 + rank, [16384] * 16, 8, 8, head_dim=64, poison=False)
-        h_ms, h_part, _, _, _, _ = time_fp8(c64, 32, max(20, a.steps // 4), a.warmup, dev)
-        h_ms = _max_over_ranks(h_ms)
-        extra["fp8_b16_16k_hd64"] = {
-            "workload": "fp8 paged decode, 16 seqs x 16384 tokens, 8 KV heads, group 8, head_dim 64, block 16, P=32",
-            "us_per_step": round(h_ms * 1e3, 2), "partition_us": round(h_part * 1e3, 2),
-            "kv_bytes": c64.kv_bytes, "gbs": round(c64.kv_bytes / (h_ms * 1e-3) / 1e9, 1),
-            "frac_of_peak": round(c64.kv_bytes / (h_ms * 1e-3) / 1e9 / peak, 4),
-            "l2": "no flush: the 268 MB KV stream per step is larger than L2"}
-        del c64
-        esteps = max(20, a.steps // 4)
-        for name, cent, pagefmt in (("uq_hd256_b4_75k_e2m1", None, False),
-                                    ("uq_hd256_b4_75k_randtable", "rand", False),
-                                    ("uq_hd256_b4_75k_page_formats", None, True)):
-            cu = synth.uq_full(seed=1003 + rank, centroids=None if cent is None else synth.sorted_random_centroids(5),
-                               scale_format="ue8m0" if pagefmt else "e4m3", rot_perm=pagefmt)
-            u_ms, u_part = time_uq(cu, 147, esteps, a.warmup, dev, q_haircut=pagefmt)
-            u_ms = _max_over_ranks(u_ms)
-            extra[name] = {
-                "workload": "4-bit head_dim 256 decode, 4 seqs x 75000 tokens, 2 KV heads, group 8, block 64, "
-                            "288-byte slots, P=147, centroid table " + ("e2m1 values" if cent is None else
-                                                                         "seeded sorted random")
-                            + (", UE8M0 group scales, e4m3 query haircut, column-permuted rotation" if pagefmt
-                               else ", e4m3 group scales"),
-                "us_per_step": round(u_ms * 1e3, 2), "partition_us": round(u_part * 1e3, 2),
-                "l2": "flushed (256 MB write, then read) before every timed step", "kv_bytes": cu.kv_bytes, "gbs": round(cu.kv_bytes / (u_ms * 1e-3) / 1e9, 1),
-                "frac_of_peak": round(cu.kv_bytes / (u_ms * 1e-3) / 1e9 / peak, 4)}
+        for qg in (8, 6):
+            cu = synth.uq_full(seed=1003 + rank, query_group=qg)
+            configs[f"c4_hd256_b4x75k_qg{qg}"] = run(uq_steps(cu, UQ_P, dev)[0], cu.kv_bytes)
             del cu
-        for name, ql, qg, pt in (("fp8_ext_b16_16k_ql4_qg4_per_token", 4, 4, True),
-                                 ("fp8_ext_b16_16k_ql2_qg8", 2, 8, False)):
-            ce = synth.fp8_ext_long(seed=1005 + rank, query_group=qg, query_len=ql, per_token=pt)
-            x_ms = _max_over_ranks(time_fp8_ext(ce, 32, esteps, a.warmup, dev))
-            extra[name] = {
-                "workload": f"fp8 decode of {ql} query tokens per sequence (causal inside the query block), "
-                            f"16 seqs x 16384 tokens, 8 KV heads, group {qg}, block 16, P=32, "
-                            + ("per-token K/V scales" if pt else "per-tensor K/V scales"),
-                "us_per_step": round(x_ms * 1e3, 2), "kv_bytes": ce.kv_bytes,
-                "gbs": round(ce.kv_bytes / (x_ms * 1e-3) / 1e9, 1),
-                "frac_of_peak": round(ce.kv_bytes / (x_ms * 1e-3) / 1e9 / peak, 4),
-                "l2": "no flush: the cache is larger than L2"}
-            del ce
         ci = synth.idx_full(seed=1004 + rank)
-        i_ms, _ = time_idx(ci, esteps, a.warmup, dev)
-        i_ms = _max_over_ranks(i_ms)
-        extra["nvfp4_index_score_64req"] = {
-            "workload": "NVFP4 paged index scorer, 64 requests, lengths U[4096,32768], query_len 4, 2 heads, "
-                        "128-token pages of 72 B/token, S=256",
-            "us_per_step": round(i_ms * 1e3, 2), "l2": "flushed (256 MB write, then read) before every timed step",
-            "kv_bytes": ci.kv_bytes,
-            "gbs": round(ci.kv_bytes / (i_ms * 1e-3) / 1e9, 1),
-            "frac_of_peak": round(ci.kv_bytes / (i_ms * 1e-3) / 1e9 / peak, 4)}
+        configs["c5_nvfp4_score_64req"] = run(idx_step(ci, dev), ci.kv_bytes)
+
+        # the other workloads of the library's entry points
+        cu = synth.uq_full(seed=1003 + rank, centroids=synth.sorted_random_centroids(5))
+        extra["hd256_randtable"] = run(uq_steps(cu, UQ_P, dev)[0], cu.kv_bytes)
+        del cu
+        cu = synth.uq_full(seed=1003 + rank, scale_format="ue8m0", rot_perm=True)
+        extra["hd256_page_formats"] = run(uq_steps(cu, UQ_P, dev, q_haircut=True)[0], cu.kv_bytes)
+        del cu
+        c64 = synth.make_fp8_case(1006 + rank, [16384] * 16, 8, 8, head_dim=64, poison=False)
+        extra["fp8_hd64_b16x16k"] = run(fp8_steps(c64, 32, dev)[0], c64.kv_bytes)
+        del c64
+        for name, ql, qg, pt in (("fp8x_ql4_qg4_pertok", 4, 4, True), ("fp8x_ql2_qg8", 2, 8, False)):
+            ce = synth.fp8_ext_long(seed=1005 + rank, query_group=qg, query_len=ql, per_token=pt)
+            extra[name] = run(fp8_ext_step(ce, 32, dev), ce.kv_bytes)
+            del ce
         cs = synth.idx_shared_prefix(seed=1007 + rank)
-        s_ms, _ = time_idx(cs, esteps, a.warmup, dev)
-        s_ms = _max_over_ranks(s_ms)
-        extra["nvfp4_index_score_64req_shared_prefix"] = {
-            "workload": "NVFP4 paged index scorer, 64 requests, lengths U[16384,32768], the first 16384 tokens "
-                        "(128 pages) shared by all requests, query_len 4, 2 heads, S=256",
-            "us_per_step": round(s_ms * 1e3, 2), "l2": "flushed (256 MB write, then read) before every timed step",
-            "kv_bytes": cs.kv_bytes, "unique_page_bytes": cs.unique_page_bytes,
-            "gbs": round(cs.kv_bytes / (s_ms * 1e-3) / 1e9, 1),
-            "gbs_unique": round(cs.unique_page_bytes / (s_ms * 1e-3) / 1e9, 1),
-            "kv_bytes_is": "pages per (request, block) as the scorer processes them; unique_page_bytes counts a "
-                           "shared page once"}
+        extra["score_shared_prefix"] = run(idx_step(cs, dev), cs.kv_bytes,
+                                           unique_gbs_is="see unique_page_bytes",
+                                           unique_page_bytes=cs.unique_page_bytes)
         del cs
-        t_ms, _ = time_idx(ci, esteps, a.warmup, dev, per_token_cols=32768)
-        t_ms = _max_over_ranks(t_ms)
         out_bytes = ci.num_heads * ci.num_reqs * ci.query_len * 32768 * 4
-        extra["nvfp4_index_score_64req_per_token"] = {
-            "workload": "NVFP4 paged index scorer, 64 requests, lengths U[4096,32768], query_len 4, 2 heads, "
-                        "one score column per token (32768 columns)",
-            "us_per_step": round(t_ms * 1e3, 2), "l2": "flushed (256 MB write, then read) before every timed step",
-            "kv_bytes": ci.kv_bytes, "score_bytes_written": out_bytes,
-            "gbs_kv": round(ci.kv_bytes / (t_ms * 1e-3) / 1e9, 1),
-            "gbs_read_plus_written": round((ci.kv_bytes + out_bytes) / (t_ms * 1e-3) / 1e9, 1),
-            "frac_of_peak": round((ci.kv_bytes + out_bytes) / (t_ms * 1e-3) / 1e9 / peak, 4)}
+        extra["score_per_token_32k"] = run(idx_step(ci, dev, per_token_cols=32768), ci.kv_bytes + out_bytes,
+                                           bytes_are="pages read + scores written")
         del ci
 
     cpu = None
@@ -622,23 +613,24 @@ def main():
 
     if rank != 0:
         return
+    cfg = dict(CONFIG, parallelism=f"replicas x{world}", timing=f"{mode}, {a.steps} replays, median")
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": round(ms_max, 5), "us_per_step": round(ms_max * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": "synthetic (seeded N(0,1) K/V quantised to e4m3, bf16 Q)",
-        "config": {"workload": WORKLOAD, "kv_bytes_per_step": kv,
-                   "l2": "no flush: the 537 MB KV stream per step is larger than the 129 MB L2",
-                   "parallelism": f"replicas x{world}"},
+        "config": cfg,
         "roofline": {"bound": "hbm", "achieved": round(part_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(part_gbs / peak, 4), "traffic": _profiled_traffic(),
                      "kernel": "pa_fp8_partition_kernel", "peak_kind": peak_kind,
-                     "timing": "partition-only pass of the same step count after the step loop, CUDA events "
-                               "around each launch on the launching stream",
+                     "timing": "partition-only launches after the step replays, CUDA events around each launch "
+                               "on the launching stream",
                      "step_frac": round(value / world / peak, 4)},
-        "partition_us": round(part_ms * 1e3, 2), "combine_us": round(comb_ms * 1e3, 2),
-        "combine_us_is": "step time minus the partition kernel's own time (the combine overlaps the partition tail)",
-        "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "extra": extra,
+        "partition_us": round(part_ms * 1e3, 2),
+        "gpu_launches": 2 * a.steps, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "extra": extra,
+        # last, so that a tail of the output keeps it: every configuration of
+        # the decode study, CUDA-graph replays with L2 flushed before each
+        "configs": dict(configs, replays=replays),
     }
     print(json.dumps(line))
     if _DIST["on"]:

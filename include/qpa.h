@@ -346,9 +346,11 @@ int nvfp4_index_score(const uint8_t* q, const uint8_t* kv_pages, const int32_t* 
  * 256-byte padding; a call that needs more than the array returns
  * QPA_ERR_WORKSPACE without launching anything.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current) and caches it. Make that first call
- * before capturing any stream on that device.
+ * The array's device address belongs to a CUDA context. The first call in a
+ * (device, context) looks it up, with that device current, and caches it;
+ * a call in another context (or after cudaDeviceReset made a new primary
+ * context) looks it up again. Make that first call before capturing any
+ * stream on that device.
  *
  * All calls share the one array and it keeps the last call's contents.
  * Nothing in it needs to start at zero: the partition kernel writes every

@@ -13,22 +13,57 @@
 static __device__ __align__(256) unsigned char qpa_fp8_static_scratch[QPA_FP8_STATIC_SCRATCH_BYTES];
 
 namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and cached.
+// cuCtxGetCurrent through the runtime's driver entry-point query (no
+// link-time dependency on the driver library); null if unavailable.
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  return fn;
+}
+
+// One looked-up address per (device, context): the symbol's device address is
+// only valid in the context it was looked up in.
+struct Entry {
+  int dev;
+  CUcontext ctx;
+  void* ptr;
+};
+constexpr int kMaxEntries = 64;
+std::mutex g_mu;
+Entry g_entries[kMaxEntries];
+int g_num_entries = 0;
+
+// Device address of the scratch array in the current device's current
+// context. The first call in a (device, context) looks it up, with that device
+// current, and caches it.
 void* scratch_on_current_device() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return nullptr;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, qpa_fp8_static_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    g_scratch_ptr[dev] = p;
-  }
-  return g_scratch_ptr[dev];
+  if (ctx)
+    for (int i = 0; i < g_num_entries; ++i)
+      if (g_entries[i].dev == dev && g_entries[i].ctx == ctx) return g_entries[i].ptr;
+  // not looked up in this context yet (or no context is current, which the
+  // lookup itself makes the device's primary one)
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, qpa_fp8_static_scratch) != cudaSuccess || p == nullptr) return nullptr;
+  if (!ctx && (get(&ctx) != CUDA_SUCCESS || !ctx)) return nullptr;
+  Entry e{dev, ctx, p};
+  if (g_num_entries < kMaxEntries) g_entries[g_num_entries++] = e;
+  else g_entries[dev % kMaxEntries] = e;      // table full: reuse a slot (looked up again when evicted)
+  return p;
 }
 }  // namespace
 

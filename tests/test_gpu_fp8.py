@@ -7,6 +7,7 @@ import oracle
 import quantized_paged_attention_gb300 as qpa
 import synth
 from _gpu import Fp8Dev, check_attention, fp8_v_absmax
+from _oracle_pool import check_units, fp8_reference
 from oracle.attention import dense_kv_fp8, partition_partials
 
 pytestmark = pytest.mark.gpu
@@ -159,35 +160,20 @@ def test_invalid_block_id_raises_error_word():
     assert qpa.kernel_error() == 0                      # reading clears it
 
 
-def _sampled_units(c, n, seed):
-    rng = np.random.default_rng(seed)
-    all_units = [(s, h) for s in range(c.num_seqs) for h in range(c.num_kv_heads)]
-    idx = rng.choice(len(all_units), size=min(n, len(all_units)), replace=False)
-    return [all_units[i] for i in sorted(idx)]
-
-
-def test_full_gqa_config_sampled():
+def test_full_gqa_config_all_units():
     """16 seqs x 16384, 8 KV heads, group 8, P=32 (512-token partitions), as
-    the benchmark runs it; 8 sampled (seq, head) units against the oracle and
-    every output finite."""
+    the benchmark runs it; every one of the 128 (seq, head) units against the
+    oracle, element by element."""
     c = synth.fp8_gqa()
     out, _, _ = Fp8Dev(c).run(32)
-    got = out.cpu().double().numpy()
-    assert np.all(np.isfinite(got))
-    _check(c, got, units=_sampled_units(c, 8, 1), what="gqa-full")
+    check_units(out.cpu().double().numpy(), fp8_reference(c), c, what="gqa-full")
 
 
-def test_full_ragged_config_sampled():
-    """128 seqs, lengths U[1024, 16384], P=32; sampled units plus the
-    shortest and the longest sequence."""
+def test_full_ragged_config_all_units():
+    """128 seqs, lengths U[1024, 16384], P=32; all 1024 (seq, head) units."""
     c = synth.fp8_ragged()
     out, _, _ = Fp8Dev(c).run(32)
-    got = out.cpu().double().numpy()
-    assert np.all(np.isfinite(got))
-    units = _sampled_units(c, 6, 2)
-    for s in (int(np.argmin(c.seq_lens)), int(np.argmax(c.seq_lens))):
-        units.append((s, 7))
-    _check(c, got, units=units, what="ragged-full")
+    check_units(out.cpu().double().numpy(), fp8_reference(c), c, what="ragged-full")
 
 
 # ---- head_dim 64 ([PA]: head_dim 64 or 128)
@@ -209,11 +195,9 @@ def test_head_dim_64_block_sizes_and_bf16(bs):
     assert torch.max(torch.abs(o16.float() - out)).item() <= torch.max(torch.abs(out)).item() * 2 ** -8 + 1e-6
 
 
-def test_head_dim_64_long_sampled():
+def test_head_dim_64_long_all_units():
     """16 seqs x 16384 tokens, 8 KV heads, group 8, head_dim 64, P = 32 (the
-    benchmark's head_dim 64 line); three sampled (seq, head) units."""
+    benchmark's head_dim 64 line); all 128 (seq, head) units."""
     c = synth.make_fp8_case(960, [16384] * 16, 8, 8, head_dim=64, poison=False)
     out, _, _ = Fp8Dev(c).run(32)
-    got = out.cpu().double().numpy()
-    assert np.all(np.isfinite(got))
-    _check(c, got, units=[(0, 0), (9, 3), (15, 7)], what="hd64 long")
+    check_units(out.cpu().double().numpy(), fp8_reference(c), c, what="hd64 long")

@@ -6,6 +6,7 @@ import torch
 import oracle
 import synth
 from _gpu import IdxDev, check_scores
+from _oracle_pool import idx_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -55,19 +56,21 @@ def test_repeat_is_deterministic():
     assert torch.equal(a, b)
 
 
-def test_full_config_sampled():
+def _check_all_requests(c, got, per_token_cols=None, what=""):
+    """Every request's score rows against the oracle (one pool task per
+    request)."""
+    ref = idx_reference(c, per_token_cols=per_token_cols)
+    ql = c.query_len
+    full = np.stack([ref[r] for r in range(c.num_reqs)], axis=1)      # [H, R, QL, cols]
+    full = full.reshape(full.shape[0], c.num_reqs * ql, full.shape[-1])
+    check_scores(got, full, what=what)
+
+
+def test_full_config_all_requests():
     """64 requests, lengths U[4096, 32768], query_len 4, 2 heads, S=256 (as
-    the benchmark runs it); 6 requests (incl. the shortest and longest)
-    against the oracle."""
+    the benchmark runs it); all 64 requests against the oracle."""
     c = synth.idx_full()
-    got = IdxDev(c).run().cpu().double().numpy()
-    assert not np.any(np.isnan(got))
-    rng = np.random.default_rng(5)
-    reqs = sorted(set(rng.choice(c.num_reqs, 4, replace=False).tolist()
-                      + [int(np.argmin(c.seq_lens)), int(np.argmax(c.seq_lens))]))
-    ref = _ref(c, reqs=reqs)
-    rows = [r * 4 + q for r in reqs for q in range(4)]
-    check_scores(got, ref, rows=rows, what="idx-full")
+    _check_all_requests(c, IdxDev(c).run().cpu().double().numpy(), what="idx-full")
 
 
 # ---- per-token output
@@ -100,15 +103,12 @@ def test_per_token_strided_and_block_max():
     assert np.array_equal(got[:, :, :1408].reshape(2, 12, 11, 128).max(axis=3), blk)
 
 
-def test_per_token_full_config_sampled():
+def test_per_token_full_config_all_requests():
     """64 requests, lengths U[4096, 32768], query_len 4, 2 heads, 32768 token
-    columns; 4 requests (incl. the shortest and longest) against the oracle."""
+    columns; all 64 requests against the oracle."""
     c = synth.idx_full()
     got = IdxDev(c).run(per_token_cols=32768).cpu().double().numpy()
-    assert not np.any(np.isnan(got))
-    reqs = sorted({3, 40, int(np.argmin(c.seq_lens)), int(np.argmax(c.seq_lens))})
-    rows = [r * 4 + q for r in reqs for q in range(4)]
-    check_scores(got, _ref_tok(c, 32768, reqs=reqs), rows=rows, what="idx-full per-token")
+    _check_all_requests(c, got, per_token_cols=32768, what="idx-full per-token")
 
 
 def test_shared_prefix_pages():
@@ -121,12 +121,8 @@ def test_shared_prefix_pages():
     check_scores(got, _ref(c), what="shared prefix")
 
 
-def test_shared_prefix_full_sampled():
+def test_shared_prefix_full_all_requests():
     """64 requests, lengths U[16384, 32768], 128 shared prefix pages (the
-    benchmark's shared-prefix line); 4 requests against the oracle."""
+    benchmark's shared-prefix line); all 64 requests against the oracle."""
     c = synth.idx_shared_prefix()
-    got = IdxDev(c).run().cpu().double().numpy()
-    assert not np.any(np.isnan(got))
-    reqs = [0, 17, int(np.argmin(c.seq_lens)), int(np.argmax(c.seq_lens))]
-    rows = [r * 4 + q for r in sorted(set(reqs)) for q in range(4)]
-    check_scores(got, _ref(c, reqs=sorted(set(reqs))), rows=rows, what="shared prefix full")
+    _check_all_requests(c, IdxDev(c).run().cpu().double().numpy(), what="shared prefix full")

@@ -7,6 +7,10 @@ import torch
 import oracle
 import synth
 from _gpu import UqDev, check_attention, uq_v_absmax
+from _oracle_pool import check_units, uq_reference
+
+# the partition count the benchmark runs the full hd256 workload with
+UQ_BENCH_P = 147
 
 pytestmark = pytest.mark.gpu
 
@@ -108,22 +112,13 @@ def test_warps_per_item(lens, P, want_w, rand):
     _check(c, out.cpu().double().numpy(), what=f"W={w} P={P}")
 
 
-def _sampled_units(c, n, seed):
-    rng = np.random.default_rng(seed)
-    all_units = [(s, h) for s in range(c.num_seqs) for h in range(c.num_kv_heads)]
-    idx = rng.choice(len(all_units), size=min(n, len(all_units)), replace=False)
-    return [all_units[i] for i in sorted(idx)]
-
-
 @pytest.mark.parametrize("qg", [8, 6])
-def test_full_config_sampled(qg):
-    """4 seqs x 75000 tokens, 2 KV heads, block 64, 288-byte slots, P=147
-    (as the benchmark runs it); 3 sampled (seq, head) units against the oracle."""
+def test_full_config_all_units(qg):
+    """4 seqs x 75000 tokens, 2 KV heads, block 64, 288-byte slots, with the
+    benchmark's partition count; all 8 (seq, head) units against the oracle."""
     c = synth.uq_full(query_group=qg)
-    out, _, _ = UqDev(c).run(147)
-    got = out.cpu().double().numpy()
-    assert np.all(np.isfinite(got))
-    _check(c, got, units=_sampled_units(c, 3, qg), what=f"uq-full qg={qg}")
+    out, _, _ = UqDev(c).run(UQ_BENCH_P)
+    check_units(out.cpu().double().numpy(), uq_reference(c), c, what=f"uq-full qg={qg}")
 
 
 # ---- page formats: UE8M0 group scales and the e4m3 query haircut
@@ -157,14 +152,12 @@ def test_page_formats_with_lut_groups_and_blocks(qg, bs):
     _check(c, out.cpu().double().numpy(), what=f"ue8m0 haircut lut qg={qg} bs={bs}", q_haircut=True)
 
 
-def test_page_formats_full_config_sampled():
-    """4 seqs x 75000 tokens with UE8M0 scales and the query haircut, P=147;
-    3 sampled (seq, head) units against the oracle."""
+def test_page_formats_full_config_all_units():
+    """4 seqs x 75000 tokens with UE8M0 scales and the query haircut, with the
+    benchmark's partition count; all 8 (seq, head) units against the oracle."""
     c = synth.make_uq_case(1013, [75000] * 4, 2, 8, 64, 288, poison=False, scale_format="ue8m0")
-    out, _, _ = UqDev(c).run(147, q_haircut=True)
-    got = out.cpu().double().numpy()
-    assert np.all(np.isfinite(got))
-    _check(c, got, units=_sampled_units(c, 3, 9), what="uq-full ue8m0 haircut", q_haircut=True)
+    out, _, _ = UqDev(c).run(UQ_BENCH_P, q_haircut=True)
+    check_units(out.cpu().double().numpy(), uq_reference(c, q_haircut=True), c, what="uq-full ue8m0 haircut")
 
 
 # ---- the page's column-permuted rotation
