@@ -413,7 +413,7 @@ def _aggregate_gbs(bytes_per_rank, ms_max, world):
     return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
 
 
-UQ_P = 147          # partitions of the full hd256 workload
+UQ_P = 38           # partitions of the full hd256 workload: 152 items, one per SM
 
 
 def _profile_case(a):

@@ -57,7 +57,9 @@ int qpa_version(void);
  * returns and clears the device error word of the current device: 0 when no
  * kernel reported a problem, otherwise a positive code (1, 2: a wait gave up
  * after its time limit; 3: an invalid block id was met; 4: the fp8 work split
- * produced an out-of-range slot, which its own bounds rule out). Returns QPA_ERR_CUDA
+ * produced an out-of-range slot, which its own bounds rule out; 5: a value
+ * outside what the hd256 kernel represents, see QPA_UQ_UE8M0_SCALES and the
+ * centroid table). Returns QPA_ERR_CUDA
  * if the synchronisation fails. Diagnostic only; the decode entry points
  * never call it. */
 int qpa_kernel_error(void* stream);
@@ -206,10 +208,14 @@ int pa_decode_fp8_ext(const void* q, const uint8_t* kv_cache, const int32_t* blo
  *   bytes 264..271  V scales (e4m3fn), one per 32 dims
  * Q is rotated inside the partition kernel and the output is rotated back in
  * the combine kernel. Partition p owns the 256-token tile groups p, p+P,
- * p+2P, ... ([UQ] step F); a partition with no tokens writes m = -inf, l = 0,
- * O = 0; L = 0 gives 0. The workspace holds (O, m, l) partials laid out as
- * for pa_decode_fp8 with head_dim 256, in the rotated domain (no v_scale: the
- * scales are per group).
+ * p+2P, ... ([UQ] step F); L = 0 gives 0. The kernel splits each partition's
+ * 32-token slices over J warps (J = 1, 2, 4 or 8, fixed by num_kv_heads and
+ * query_group), each of which keeps its own softmax state, so the workspace
+ * holds P*J partial slots per (sequence, KV head): float32
+ * O [num_seqs][num_kv_heads][P*J][query_group][256] (rotated domain,
+ * normalised by l), m and l [num_seqs][num_kv_heads][P*J][query_group] at
+ * 256-byte aligned offsets; a slot without tokens has m = -inf, l = 0 and
+ * its O is not written. uq_decode_hd256_workspace_size() accounts for J.
  *
  * Layouts:
  *   q          bf16 [num_seqs][num_kv_heads*query_group][256] (not rotated),
@@ -217,15 +223,28 @@ int pa_decode_fp8_ext(const void* q, const uint8_t* kv_cache, const int32_t* blo
  *   kv_cache   uint8 [num_blocks][block_size][num_kv_heads][padded_slot]
  *   centroids  float32 [16] on the device (code -> value)
  *   block_table, seq_lens, out, workspace: as for pa_decode_fp8 (head_dim 256)
- * Supported: head_dim 256, query_group 1..8, block_size 16/32/64/128/256.
+ * Supported: head_dim 256, query_group 1..16, block_size 16/32/64/128/256.
  * Alignment: q, kv_cache and out 16-byte aligned; workspace 256-byte aligned.
+ *
+ * Precision: q_r enters the QK product rounded to f16, the probabilities
+ * too; K is exact (the group scale multiplies the f32 partial dot of each
+ * 32-dim group). A centroid table other than the e2m1 values is divided by
+ * the power of two 2^e that puts its largest |c| in [0.5, 1) and rounded to
+ * f16 (relative error 2^-11), then multiplied by the group scale in f16; the
+ * output takes 2^e back, so no table or scale magnitude overflows f16. A
+ * non-finite centroid raises error word 5.
  *
  * flags (other bits: QPA_ERR_SHAPE):
  *   QPA_UQ_UE8M0_SCALES  K and V scale bytes are UE8M0, the group scale
- *       format of [UQ] STEP C/F: scale = 2^(byte - 127), byte 0 = 0. The
- *       kernel multiplies codes by the scale in f16, so results are exact
- *       for bytes 104..140 (2^-23 .. 2^13); outside that window the product
- *       overflows or flushes and the result is not defined.
+ *       format of [UQ] STEP C/F: scale = 2^(byte - 127), byte 0 = 0. Every
+ *       byte 0..254 is decoded exactly: the K scale multiplies the f32
+ *       partial dot of its group, and each token's V scales are split into
+ *       the token's largest power of two (carried by the probability operand
+ *       and a per-item reference exponent) and 2^(b - max) <= 1 (applied in
+ *       f16). The results are float32 values, so inputs whose logits or
+ *       outputs lie beyond float32 are outside the supported range; a byte
+ *       255 (the OCP encoding's NaN) in a live token, or a logit that is not
+ *       a finite float32, raises error word 5.
  *   QPA_UQ_Q_HAIRCUT  the e4m3 query rounding of [UQ] STEP B' (after the
  *       rotation): the rotated query times softmax_scale is rounded to e4m3
  *       (nearest even, saturating at +-448) and the logits are that rounded

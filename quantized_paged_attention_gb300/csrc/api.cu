@@ -88,7 +88,7 @@ Fp8Layout fp8x_layout(const qpa_fp8_ext_desc* d, int P) {
 
 // ------------------------------------------------------------------ uq hd256
 bool uq_shape_ok(const qpa_uq_desc* d) {
-  if (d->num_seqs < 0 || d->num_kv_heads < 1 || d->query_group < 1 || d->query_group > 8) return false;
+  if (d->num_seqs < 0 || d->num_kv_heads < 1 || d->query_group < 1 || d->query_group > 16) return false;
   if (d->head_dim != 256) return false;
   const int bs = d->block_size;
   if (!(bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256)) return false;
@@ -100,8 +100,11 @@ bool uq_shape_ok(const qpa_uq_desc* d) {
   return true;
 }
 
+// Partial slots per (sequence, KV head): P times the kernel's slots per item.
+int uq_slots(const qpa_uq_desc* d, int P) { return P * uq_plan(d->num_kv_heads, d->query_group).jw; }
+
 Fp8Layout uq_layout(const qpa_uq_desc* d, int P) {
-  const size_t rows = size_t(d->num_seqs) * d->num_kv_heads * P * d->query_group;
+  const size_t rows = size_t(d->num_seqs) * d->num_kv_heads * uq_slots(d, P) * d->query_group;
   Fp8Layout L;
   L.o_off = 0;
   L.m_off = round_up(rows * 256 * sizeof(float), 256);
@@ -115,7 +118,7 @@ int uq_check(const void* q, const uint8_t* kv, const float* cent, const int32_t*
   if (!d) return QPA_ERR_NULL;
   if (!uq_shape_ok(d)) return QPA_ERR_SHAPE;
   if (P < 1) return QPA_ERR_PARTITIONS;
-  if ((long long)d->num_seqs * d->num_kv_heads * P * d->query_group > 0x7fffffffLL) return QPA_ERR_SHAPE;
+  if ((long long)d->num_seqs * d->num_kv_heads * P * 8 * d->query_group > 0x7fffffffLL) return QPA_ERR_SHAPE;
   if (d->num_seqs == 0) return QPA_OK;
   if (!q || !kv || !cent || !bt || !sl || !ws) return QPA_ERR_NULL;
   const long long sh = d->q_stride_head ? d->q_stride_head : 256;
@@ -390,7 +393,7 @@ int uq_decode_hd256_combine(int num_partitions, void* out, const qpa_uq_desc* d,
   c.num_seqs = d->num_seqs;
   c.num_kv_heads = d->num_kv_heads;
   c.qg = d->query_group;
-  c.num_partitions = num_partitions;
+  c.num_partitions = uq_slots(d, num_partitions);
   c.d = 256;
   c.out_stride_head = 256;
   c.out_stride_seq = (long long)d->num_kv_heads * d->query_group * 256;

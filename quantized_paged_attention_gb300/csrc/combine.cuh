@@ -1,6 +1,7 @@
 // Flash-combine of split-KV partials for one query row (the [PA] page's
 // cross-partition reduce): M = max_p m_p, w_p = l_p exp(m_p - M),
-// o = sum_p w_p O_p / sum_p w_p. An empty partition (m_p = -inf or l_p = 0)
+// o = sum_p (w_p / sum_q w_q) O_p (the weights are normalised before the sum,
+// so no partial sum exceeds the largest |O_p|). An empty partition (m_p = -inf or l_p = 0)
 // has weight exactly 0 and its O is never read, so it need not be written;
 // the exponent argument is clamped so no NaN can arise.
 //
@@ -71,7 +72,7 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) {
       const int pp = base + sub + k * nsub;
-      w[k] = pp < P ? weight(pp) : 0.f;
+      w[k] = pp < P ? weight(pp) * inv : 0.f;     // normalised first: no partial sum exceeds max |O_p|
       o[k] = w[k] != 0.f ? __ldg(reinterpret_cast<const float4*>(ob + pp * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
@@ -86,10 +87,10 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
       const float4 b = part[s * NVEC + v4];
       acc.x += b.x; acc.y += b.y; acc.z += b.z; acc.w += b.w;
     }
-    vec[4 * v4 + 0] = acc.x * inv;
-    vec[4 * v4 + 1] = acc.y * inv;
-    vec[4 * v4 + 2] = acc.z * inv;
-    vec[4 * v4 + 3] = acc.w * inv;
+    vec[4 * v4 + 0] = acc.x;
+    vec[4 * v4 + 1] = acc.y;
+    vec[4 * v4 + 2] = acc.z;
+    vec[4 * v4 + 3] = acc.w;
   }
   __syncthreads();
 }

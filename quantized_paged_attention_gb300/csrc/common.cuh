@@ -9,7 +9,8 @@ namespace qpa {
 
 // Error word raised by a kernel that gave up waiting or met an invalid block
 // id (the library's only device-side state). 0 = no error.
-enum : int { KERR_NONE = 0, KERR_TIMEOUT_FULL = 1, KERR_TIMEOUT_EMPTY = 2, KERR_BAD_BLOCK = 3, KERR_SCHEDULE = 4 };
+enum : int { KERR_NONE = 0, KERR_TIMEOUT_FULL = 1, KERR_TIMEOUT_EMPTY = 2, KERR_BAD_BLOCK = 3, KERR_SCHEDULE = 4,
+             KERR_RANGE = 5 };
 extern __device__ int g_kernel_error;
 
 // Any wait gives up after this many nanoseconds and reports an error rather
@@ -264,6 +265,13 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
+}
+// Four 8x8 b16 matrices from shared memory: lanes 8i..8i+7 give the row
+// addresses of matrix i (16-byte aligned); r_i receives matrix i with lane
+// (g, c) = (lane / 4, lane % 4) holding row g, b16 elements 2c and 2c+1.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t r;

@@ -106,8 +106,15 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t stream);
 cudaError_t launch_fp8x_partition(const Fp8ExtLaunch& a, cudaStream_t stream);
 cudaError_t launch_fp8x_combine(const Fp8ExtCombineLaunch& a, cudaStream_t stream);
+// How the hd256 partition kernel splits a launch: hg KV heads per work item,
+// nh 8-row halves of the query group, jw partial slots per item and head
+// (the combine merges num_partitions * jw slots per query row), a ring of
+// depth stages, smem bytes of dynamic shared memory.
+struct UqPlan {
+  int hg, nh, jw, depth, smem;
+};
+UqPlan uq_plan(int num_kv_heads, int query_group);
 cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream);
-int uq_warps_per_item(long long items, int max_blocks, int block_size, int num_partitions, int num_sms);
 cudaError_t launch_uq_combine(const CombineLaunch& a, cudaStream_t stream);
 cudaError_t launch_idx_score(const IdxLaunch& a, cudaStream_t stream);
 

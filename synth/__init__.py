@@ -15,7 +15,8 @@ Workload shapes follow the five configurations of the decode study:
   fp8 GQA        16 seqs x 16384 tokens, 8 KV heads, group 8, D 128, block 16
   fp8 ragged     128 seqs, lengths U[1024, 16384], 8 KV heads, group 8
   uq hd256       4 seqs x 75000 tokens, 2 KV heads, group 8 or 6, block 64,
-                 288-byte slots (272 used)
+                 288-byte slots (272 used); UE8M0 caches also drawn byte
+                 by byte over windows of the scale-byte range
   nvfp4 scorer   64 requests, lengths U[4096, 32768], query_len 4,
                  2 index heads, D 128, 128-token pages of 72 B/token
 """
@@ -94,18 +95,14 @@ def group_scales_e4m3(x: np.ndarray, group: int, qmax: float) -> np.ndarray:
     return s
 
 
-# UE8M0 scale bytes the generators emit: 2^-23 .. 2^13, the powers of two for
-# which every e2m1 code times the scale is an exact f16 value.
-UE8M0_MIN_BYTE, UE8M0_MAX_BYTE = 104, 140
-
-
 def group_scales_ue8m0(x: np.ndarray, group: int, qmax: float) -> np.ndarray:
     """Per-group UE8M0 scale bytes for x[..., D]: the smallest power of two
-    2^(byte-127) with absmax / 2^(byte-127) <= qmax, clipped to the window."""
+    2^(byte-127) with absmax / 2^(byte-127) <= qmax (bytes 1..254; an
+    all-zero group gets the smallest power, byte 1)."""
     shp = x.shape[:-1] + (x.shape[-1] // group, group)
     amax = np.abs(x.reshape(shp)).max(axis=-1).astype(np.float64)
-    e = np.ceil(np.log2(np.maximum(amax / qmax, 2.0 ** -30)))
-    return np.clip(127 + e, UE8M0_MIN_BYTE, UE8M0_MAX_BYTE).astype(np.uint8)
+    e = np.ceil(np.log2(np.maximum(amax / qmax, 2.0 ** -126)))
+    return np.clip(127 + e, 1, 254).astype(np.uint8)
 
 
 def e2m1_table() -> np.ndarray:
@@ -374,7 +371,9 @@ def make_uq_case(seed: int, seq_lens, num_kv_heads: int = 2, query_group: int = 
                  block_size: int = 64, padded_slot: int = 288, centroids=None,
                  num_blocks: int | None = None, softmax_scale: float | None = None,
                  poison: bool = True, chunk_tokens: int = 1 << 15,
-                 scale_format: str = "e4m3", rot_perm: bool = False) -> UqCase:
+                 scale_format: str = "e4m3", rot_perm: bool = False, v_gain: float = 1.0) -> UqCase:
+    """v_gain multiplies the logical V draws (so that a centroid table of
+    another magnitude still quantises a spread of values)."""
     if scale_format not in ("e4m3", "ue8m0"):
         raise ValueError(scale_format)
     r = rng(seed)
@@ -400,7 +399,7 @@ def make_uq_case(seed: int, seq_lens, num_kv_heads: int = 2, query_group: int = 
     for o in range(0, ntok, chunk_tokens):
         n = min(chunk_tokens, ntok - o)
         kl = r.standard_normal((n, UQ_D), dtype=np.float32) @ rot
-        vl = r.standard_normal((n, UQ_D), dtype=np.float32) @ rot
+        vl = (r.standard_normal((n, UQ_D), dtype=np.float32) * np.float32(v_gain)) @ rot
         if scale_format == "e4m3":
             ks = group_scales_e4m3(kl, 32, 6.0)
             vs = group_scales_e4m3(vl, 32, cmax)
@@ -439,6 +438,48 @@ def sorted_random_centroids(seed: int) -> np.ndarray:
     """A seeded, sorted 16-entry centroid table (the second table of the
     hd256 runs)."""
     return np.sort(rng(seed).standard_normal(16).astype(np.float32) * 2.0)
+
+
+def make_uq_ue8m0_window_case(seed: int, seq_lens, k_bytes, v_bytes, num_kv_heads: int = 2,
+                              query_group: int = 8, block_size: int = 64, padded_slot: int = 288,
+                              centroids=None, q_gain: float = 1.0, zero_frac: float = 0.03,
+                              poison: bool = True) -> UqCase:
+    """A UE8M0 slot cache drawn byte by byte: every K and V code uniform over
+    the 16 codes, every K group-scale byte uniform in k_bytes = (lo, hi), every
+    V group-scale byte in v_bytes, and a zero_frac share of the scale bytes
+    set to the 0 sentinel (a zero group). q = q_gain * N(0, 1) in bf16. Used to
+    cover the whole UE8M0 byte range window by window (a case's scales span at
+    most a few dozen binades, so its tolerance, 2e-3 * max|V|, still sees the
+    small ones)."""
+    r = rng(seed)
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    B = seq_lens.shape[0]
+    nblk = [int(math.ceil(int(L) / block_size)) for L in seq_lens]
+    max_blocks = max(1, max(nblk))
+    num_blocks = max(1, sum(nblk))
+    if centroids is None:
+        centroids = e2m1_table()
+    Hq = num_kv_heads * query_group
+    q_bits = round_to_bf16_bits(r.standard_normal((B, Hq, UQ_D), dtype=np.float32) * np.float32(q_gain))
+    ntok = num_blocks * block_size * num_kv_heads
+    cache = r.integers(0, 256, size=(ntok, padded_slot), dtype=np.uint8)   # codes (and padding) uniform
+    ks = r.integers(k_bytes[0], k_bytes[1] + 1, size=(ntok, 8)).astype(np.uint8)
+    vs = r.integers(v_bytes[0], v_bytes[1] + 1, size=(ntok, 8)).astype(np.uint8)
+    ks[r.random((ntok, 8)) < zero_frac] = 0
+    vs[r.random((ntok, 8)) < zero_frac] = 0
+    cache[:, 128:136] = ks
+    cache[:, 264:272] = vs
+    cache = cache.reshape(num_blocks, block_size, num_kv_heads, padded_slot)
+    bt = _assign_blocks(r, nblk, num_blocks, max_blocks)
+    if poison:
+        for s in range(B):
+            L = int(seq_lens[s])
+            if L % block_size and nblk[s]:
+                blk = bt[s, nblk[s] - 1]
+                cache[blk, L % block_size:, :, 128:136] = 0xFF
+                cache[blk, L % block_size:, :, 264:272] = 0xFF
+    return UqCase(q_bits, cache, np.asarray(centroids, dtype=np.float32), bt, seq_lens, num_kv_heads,
+                  query_group, block_size, padded_slot, 1.0 / math.sqrt(UQ_D), "ue8m0", False)
 
 
 def uq_full(seed: int = 1003, query_group: int = 8, centroids=None, scale_format: str = "e4m3",

@@ -5,12 +5,13 @@ import pytest
 import torch
 
 import oracle
+import quantized_paged_attention_gb300 as qpa
 import synth
 from _gpu import UqDev, check_attention, uq_v_absmax
 from _oracle_pool import check_units, uq_reference
 
 # the partition count the benchmark runs the full hd256 workload with
-UQ_BENCH_P = 147
+UQ_BENCH_P = 38
 
 pytestmark = pytest.mark.gpu
 
@@ -78,38 +79,106 @@ def test_bf16_output_and_determinism():
     assert torch.max(torch.abs(o16.float() - a)).item() <= torch.max(torch.abs(a)).item() * 2 ** -8 + 1e-6
 
 
-def _warps_per_item(items, max_tokens, P, sms):
-    """The launcher's choice of warps per item: the smallest W among those with
-    the fewest slices per warp (rounds x slices of an item / W) on one
-    8-warp CTA per SM."""
-    tiles_per_item = max(1, -(-(-(-max_tokens // 256)) // P))
-    best_w, best = 4, None
-    for w in (1, 2, 4):
-        slots = sms * (8 // w)
-        cost = -(-items // slots) * tiles_per_item * 8 // w
-        if best is None or cost < best:
-            best, best_w = cost, w
-    return best_w
+def _plan(hk, qg):
+    """The launcher's split: heads per item HG (the largest of 8, 4, 2, 1
+    dividing Hk with HG * halves <= 8), the 8-row halves of the query group,
+    and J = 8 / (HG * halves) partial slots per item and head."""
+    nh = -(-qg // 8)
+    for hg in (8, 4, 2, 1):
+        if hk % hg == 0 and hg * nh <= 8:
+            return hg, nh, 8 // (hg * nh)
 
 
-@pytest.mark.parametrize("lens,P,want_w,rand", [
-    ([64000, 9000], 250, 1, False),     # 1000 items: one warp per item on 152 SMs
-    ([64000, 9000], 250, 1, True),
-    ([30720, 7000], 120, 2, False),     # 480 items: two warps per item
-    ([30720, 7000], 40, 4, False),      # 160 items: four warps per item
+@pytest.mark.parametrize("hk,qg,P", [
+    (1, 8, 3),      # one head per item, every 8th slice per warp
+    (1, 16, 2),     # two row halves, J = 4
+    (2, 16, 5),     # J = 2
+    (4, 16, 1),     # eight (head, half) pairs, J = 1
+    (8, 8, 2),      # eight heads per item, J = 1
+    (4, 12, 3),     # query group 12: the second half has 4 live rows
+    (2, 3, 4),
 ])
-def test_warps_per_item(lens, P, want_w, rand):
-    """Item groups of 1, 2 and 4 warps (the launcher picks W from the item
-    count); ragged lengths leave most partitions of the short sequence empty."""
-    cent = synth.sorted_random_centroids(7) if rand else None
-    c = synth.make_uq_case(260 + P + int(rand), lens, 2, 8, 64, 288, centroids=cent)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    max_tokens = c.block_table.shape[1] * c.block_size
-    w = _warps_per_item(c.num_seqs * c.num_kv_heads * P, max_tokens, P, sms)
-    if sms == 152:
-        assert w == want_w
-    out, _, _ = UqDev(c).run(P)
-    _check(c, out.cpu().double().numpy(), what=f"W={w} P={P}")
+def test_head_groups_and_row_halves(hk, qg, P):
+    """Every way the launcher splits a launch over its eight consumer warps,
+    with sequences shorter than J slices (warps left without a slice write
+    empty slots)."""
+    hg, nh, j = _plan(hk, qg)
+    c = synth.make_uq_case(260 + 10 * hk + qg + P, [1, 31, 33, 64, 200, 257, 1300], hk, qg, 64, 288,
+                           centroids=synth.sorted_random_centroids(hk + qg))
+    out, ws, desc = UqDev(c).run(P)
+    assert qpa.uq_decode_hd256_workspace_size(desc, P) >= c.num_seqs * hk * P * j * qg * 256 * 4
+    _check(c, out.cpu().double().numpy(), what=f"Hk={hk} qg={qg} (HG={hg}, halves={nh}, J={j}) P={P}")
+
+
+def test_query_group_16_long():
+    """Query group 16 (the builder's largest group) on 2 x 20000 tokens."""
+    c = synth.make_uq_case(275, [20000, 7777], 2, 16, 64, 288)
+    out, _, _ = UqDev(c).run(9)
+    check_units(out.cpu().double().numpy(), uq_reference(c), c, what="qg16 long")
+
+
+# ---- UE8M0 group scales over the whole byte range, window by window
+UE8_WINDOWS = [
+    ((1, 45), (1, 45), 1.0),
+    ((40, 90), (40, 90), 1.0),
+    ((85, 125), (85, 125), 1.0),
+    ((118, 140), (118, 140), 1.0),
+    ((135, 180), (135, 180), 1.0),
+    ((175, 215), (175, 215), 1.0),
+    # the top bytes: the query is scaled down so that the largest logits stay
+    # inside float32, and V stops at 248 so that the un-rotated output (up to
+    # 16 times the largest rotated value) does too
+    ((210, 254), (210, 248), 2.0 ** -12),
+]
+
+
+@pytest.mark.parametrize("kb,vb,gain", UE8_WINDOWS)
+@pytest.mark.parametrize("lut", [False, True])
+def test_ue8m0_byte_windows(kb, vb, gain, lut):
+    """Scale bytes drawn uniformly from each window (with 0 sentinels), codes
+    uniform over all 16 codes: together the windows cover bytes 0..254 of K
+    and 0..248 of V (the last V bytes: next test)."""
+    cent = synth.sorted_random_centroids(11) if lut else None
+    c = synth.make_uq_ue8m0_window_case(700 + kb[0] + (1 if lut else 0), [1, 63, 200, 700], kb, vb,
+                                        q_gain=gain, centroids=cent)
+    out, _, _ = UqDev(c).run(3)
+    _check(c, out.cpu().double().numpy(), what=f"ue8m0 K{kb} V{vb} lut={lut}")
+
+
+def test_ue8m0_top_v_bytes_with_small_centroids():
+    """V scale bytes up to 254 (2^127) with a centroid table below 2^-6, so
+    that every V value and the un-rotated output are float32 values."""
+    cent = (synth.sorted_random_centroids(13) * np.float32(2.0 ** -7)).astype(np.float32)
+    c = synth.make_uq_ue8m0_window_case(760, [1, 63, 200, 700], (200, 254), (230, 254), q_gain=2.0 ** -12,
+                                        centroids=cent)
+    out, _, _ = UqDev(c).run(3)
+    _check(c, out.cpu().double().numpy(), what="ue8m0 top V bytes")
+
+
+def test_ue8m0_byte_255_raises_the_range_error_word():
+    """0xFF is not a power of two of the format (the OCP encoding's NaN): a
+    live token with that K scale byte raises error word 5."""
+    c = synth.make_uq_ue8m0_window_case(790, [100], (120, 130), (120, 130))
+    t = 37
+    c.kv_cache[c.block_table[0, t // 64], t % 64, 0, 128 + 3] = 0xFF
+    d = UqDev(c)
+    desc = d.desc()
+    ws = qpa.alloc_workspace(qpa.uq_decode_hd256_workspace_size(desc, 2), d.q.device)
+    qpa.uq_decode_hd256(d.q, d.kv, d.cent, d.bt, d.sl, 2, 8, workspace=ws, desc=desc)
+    assert qpa.kernel_error() == 5
+    assert qpa.kernel_error() == 0
+
+
+@pytest.mark.parametrize("gain,v_gain", [(1000.0, 1000.0 * 200), (1e-5, 1e-5 / 200)])
+def test_centroid_tables_of_any_magnitude(gain, v_gain):
+    """Centroid tables whose products with the e4m3 group scales (here near
+    200 and near 1/200) lie far outside f16 (|c| * scale > 65504, or below
+    f16's smallest subnormal): the kernel's table is normalised and the
+    output scaled back."""
+    cent = (synth.sorted_random_centroids(12) * np.float32(gain)).astype(np.float32)
+    c = synth.make_uq_case(795 + int(gain > 1), [1, 100, 900], 2, 8, 64, 288, centroids=cent, v_gain=v_gain)
+    out, _, _ = UqDev(c).run(2)
+    _check(c, out.cpu().double().numpy(), what=f"centroids x{gain}")
 
 
 @pytest.mark.parametrize("qg", [8, 6])

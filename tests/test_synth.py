@@ -53,7 +53,7 @@ def test_uq_scale_formats():
     e = synth.make_uq_case(12, [200], 1, 8, 64, 288, poison=False)
     u = synth.make_uq_case(12, [200], 1, 8, 64, 288, poison=False, scale_format="ue8m0")
     ub = np.concatenate([u.kv_cache[..., 128:136].ravel(), u.kv_cache[..., 264:272].ravel()])
-    assert ub.min() >= synth.UE8M0_MIN_BYTE and ub.max() <= synth.UE8M0_MAX_BYTE
+    assert ub.min() >= 1 and ub.max() <= 254
     assert e.kv_cache.shape == u.kv_cache.shape and e.scale_format == "e4m3" and u.scale_format == "ue8m0"
     # a UE8M0 group scale is the smallest power of two that keeps the group inside the e2m1 range
     k_e, _ = oracle.uq.dense_kv_uq(u.kv_cache, u.centroids, u.block_table, 0, 0, 200, "ue8m0")
@@ -85,3 +85,22 @@ def test_scorer_shared_prefix_layout():
     # no NaN scales were written into a shared page (request 2 ends inside one)
     for b in c.block_table[0, :2]:
         assert not np.any(c.pages[b, 8192:] == 0x7F)
+
+
+def test_uq_ue8m0_window_cases_cover_their_windows():
+    """The byte-level UE8M0 generator draws every K and V scale byte from its
+    window (plus 0 sentinels), codes uniform over all 16 codes, and NaN-class
+    bytes (0xFF) only past a sequence's end."""
+    c = synth.make_uq_ue8m0_window_case(13, [300, 65], (1, 45), (200, 252), poison=True)
+    nb = -(-c.seq_lens.astype(np.int64) // c.block_size)
+    for s, L in enumerate(c.seq_lens):
+        t = np.arange(int(L))
+        slots = c.kv_cache[c.block_table[s, t // c.block_size], t % c.block_size]     # [L, Hk, slot]
+        kb, vb = slots[..., 128:136], slots[..., 264:272]
+        assert kb.max() <= 45 and vb.max() <= 252
+        assert set(np.unique(kb[kb > 0])) <= set(range(1, 46))
+        assert vb[vb > 0].min() >= 200
+        assert 0 < np.mean(kb == 0) < 0.1 and 0 < np.mean(vb == 0) < 0.1
+    codes = c.kv_cache[..., :128].ravel()
+    assert len(np.unique(codes & 0xF)) == 16 and len(np.unique(codes >> 4)) == 16
+    assert c.scale_format == "ue8m0" and int(nb.sum()) == c.kv_cache.shape[0]
