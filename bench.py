@@ -582,7 +582,8 @@ def main():
         c64 = synth.make_fp8_case(1006 + rank, [16384] * 16, 8, 8, head_dim=64, poison=False)
         extra["fp8_hd64_b16x16k"] = run(fp8_steps(c64, 32, dev)[0], c64.kv_bytes)
         del c64
-        for name, ql, qg, pt in (("fp8x_ql4_qg4_pertok", 4, 4, True), ("fp8x_ql2_qg8", 2, 8, False)):
+        for name, ql, qg, pt in (("fp8x_ql4_qg4_pertok", 4, 4, True), ("fp8x_ql2_qg8", 2, 8, False),
+                                 ("fp8x_ql4_qg8_pertok", 4, 8, True)):
             ce = synth.fp8_ext_long(seed=1005 + rank, query_group=qg, query_len=ql, per_token=pt)
             extra[name] = run(fp8_ext_step(ce, 32, dev), ce.kv_bytes)
             del ce

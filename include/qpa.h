@@ -105,8 +105,10 @@ int qpa_kernel_error(void* stream);
  *               (sum of exp(logit - m), 0 for an empty slot); O is
  *               normalised by l and already multiplied by v_scale. The
  *               combine reads O only where l > 0 and m > -inf.
- * Supported: head_dim 64 or 128 ([PA]), query_group 1..16, block_size
- * 16/32/64/128/256. Layouts above with head_dim in place of 128.
+ * Supported: head_dim 64 or 128 ([PA]), query_group 1..64 (the page's wide
+ * GQA; above 16 the kernel runs blocks of 16 query rows of a KV head as
+ * separate work streams over the same pages), block_size 16/32/64/128/256.
+ * Layouts above with head_dim in place of 128.
  * Alignment: q, kv_cache and out 16-byte aligned.
  * ====================================================================== */
 typedef struct qpa_fp8_desc {
@@ -174,9 +176,10 @@ int pa_decode_fp8_combine(int num_partitions, void* out, const qpa_fp8_desc* d,
  *             of tile groups as for pa_decode_fp8 (empty slot: m = -inf,
  *             l = 0, O not written); a row that sees no token of a run has
  *             m = -inf, l = 0, O = 0 in that slot.
- * Supported: head_dim 128, block_size 16..256, query_len 1..4 with
- * query_len * query_group <= 16. Errors as pa_decode_fp8; an unsupported
- * query_len or row count is QPA_ERR_SHAPE.
+ * Supported: head_dim 64 or 128, block_size 16..256, query_len 1..4 with
+ * query_len * query_group <= 64 (blocks of 16 rows, as for pa_decode_fp8's
+ * wide groups). Layouts above with head_dim in place of 128. Errors as
+ * pa_decode_fp8; an unsupported query_len or row count is QPA_ERR_SHAPE.
  * ====================================================================== */
 typedef struct qpa_fp8_ext_desc {
   qpa_fp8_desc base;

@@ -33,7 +33,7 @@ struct Fp8Layout {
 };
 
 bool fp8_shape_ok(const qpa_fp8_desc* d) {
-  if (d->num_seqs < 0 || d->num_kv_heads < 1 || d->query_group < 1 || d->query_group > 16) return false;
+  if (d->num_seqs < 0 || d->num_kv_heads < 1 || d->query_group < 1 || d->query_group > 64) return false;
   if (d->head_dim != 128 && d->head_dim != 64) return false;
   const int bs = d->block_size;
   if (!(bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256)) return false;
@@ -73,9 +73,9 @@ int fp8_check(const void* q, const uint8_t* kv, const int32_t* bt, const int32_t
 int fp8x_query_len(const qpa_fp8_ext_desc* d) { return d->query_len > 1 ? d->query_len : 1; }
 
 bool fp8x_shape_ok(const qpa_fp8_ext_desc* d) {
-  if (!fp8_shape_ok(&d->base) || d->base.head_dim != 128) return false;
+  if (!fp8_shape_ok(&d->base)) return false;
   if (d->query_len < 0 || d->query_len > 4) return false;
-  if (fp8x_query_len(d) * d->base.query_group > 16) return false;
+  if (fp8x_query_len(d) * d->base.query_group > 64) return false;
   if (d->kv_scale_per_token != 0 && d->kv_scale_per_token != 1) return false;
   return true;
 }
@@ -314,6 +314,7 @@ int pa_decode_fp8_ext(const void* q, const uint8_t* kv_cache, const int32_t* blo
   a.max_blocks = b->max_blocks_per_seq;
   a.num_partitions = num_partitions;
   a.softmax_scale = b->softmax_scale != 0.f ? b->softmax_scale : 1.0f / std::sqrt((float)b->head_dim);
+  a.head_dim = b->head_dim;
   a.num_sms = num_sms_current();
   if (a.num_sms <= 0) return QPA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -329,6 +330,7 @@ int pa_decode_fp8_ext(const void* q, const uint8_t* kv_cache, const int32_t* blo
   c.qg = b->query_group;
   c.query_len = QL;
   c.num_partitions = num_partitions;
+  c.head_dim = b->head_dim;
   c.out_stride_head = b->head_dim;
   c.out_stride_tok = hq * b->head_dim;
   c.out_stride_seq = QL * hq * b->head_dim;

@@ -1,6 +1,6 @@
 // fp8 (e4m3fn) paged-attention decode: split-KV partition kernel (head_dim
-// 64 or 128, up to 16 query rows per KV head, a multi-token / per-token-scale
-// variant) and flash-combine kernel.
+// 64 or 128, up to 16 query rows per work stream and 64 per KV head, a
+// multi-token / per-token-scale variant) and flash-combine kernel.
 //
 // What it computes follows the ROCm/FlyDSL PR #825 page ("perf(pa tile):
 // readable tile-programming PA decode kernel": per-tensor fp8 K/V, query
@@ -10,7 +10,9 @@
 //
 // GB300 design (not the pages' AMD design): one persistent CTA per SM with
 // three warp roles around the 5th-generation tensor core.
-//  * Work split: the CTAs form groups of Hk, one per KV head; the groups cut
+//  * Work split: a KV head with more than 16 query rows is RB = rows / 16
+//    (rounded up) virtual heads that read its pages and each own 16 rows;
+//    the CTAs form groups of Hk * RB, one per virtual head; the groups cut
 //    each head's tile groups (in sequence order) into equal contiguous
 //    ranges, so the CTAs of a group read the same pages together and every
 //    CTA gets the same number of tile groups in a few items. The part of a
@@ -74,8 +76,8 @@ struct Smem {
   static constexpr int redOff = cOff + 2 * R * 4;          // [2 S buffers][row blocks][4 warps][8] tile maxima
   static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][8 warps][8] row sums per warp
   static constexpr int msmOff = lredOff + 2 * 4 * NWG * R * 4;   // [2][2 groups][8] row maxima per group
-  static constexpr int infoOff = msmOff + 2 * NWG * R * 4; // [2] {item row, L, tiles, first tile group}
-  static constexpr int scOff = infoOff + 2 * 16;           // EXT: [NS][K, V][128] f32 per-token scales
+  static constexpr int infoOff = msmOff + 2 * NWG * R * 4; // [2] {item, L, tiles, first tile group}, {row block, ..}
+  static constexpr int scOff = infoOff + 2 * 32;           // EXT: [NS][K, V][128] f32 per-token scales
   static constexpr int barOff = (scOff + (EXT ? NS * 2 * TILE * 4 : 0) + 7) & ~7;
   static constexpr int NBAR = 2 * NS + 27;
   static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag, QK total
@@ -103,6 +105,9 @@ struct Fp8Params {
   // ([num_blocks][Hk][block_size] in k_scale / v_scale)
   long long q_stride_tok;
   int query_len, per_token;
+  // query rows per KV head above 16: blocks of 16 rows run as separate
+  // "virtual heads" (KV head vh / row_blocks, rows 16 (vh % row_blocks) ..)
+  int row_blocks;
 };
 
 // HD: the cache's head_dim (64 or 128). Shared-memory rows stay 128 bytes
@@ -200,6 +205,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 
   const int P = p.num_partitions;
   const int Hk = p.num_kv_heads;
+  const int RB = p.row_blocks;             // row blocks (virtual heads) per KV head
+  const int Hv = Hk * RB;
   const int G = gridDim.x;
   const int QL = EXT ? p.query_len : 1;
   const int rows = EXT ? QL * p.qg : p.qg;   // partial rows per item
@@ -257,7 +264,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     while (ok) {
       const int qb = qcnt & 1;
       if (!warp_wait(&qfull[qb], (qcnt >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
-      const int4 inf = lds_i4(info_s + 16 * qb);
+      const int4 inf = lds_i4(info_s + 32 * qb);
+      const int rbase = 16 * lds_i4(info_s + 32 * qb + 16).x;   // the row block's first row
 #pragma unroll
       for (int q4 = 0; q4 < RG / 4; ++q4) {
         const float4 cv = lds_f4(cbuf_s + 4 * (qb * R + RG * rblk + 4 * q4));
@@ -304,7 +312,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           for (int r = 0; r < RG; ++r) {
             // row qoff * qg + g sees the tokens below L - QL + 1 + qoff
             const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
-            x[r] = (start + t < L - QL + 1 + (RG * rblk + r) / p.qg) ? sv * c[r] * ks_t : -INFINITY;
+            x[r] = (start + t < L - QL + 1 + (rbase + RG * rblk + r) / p.qg) ? sv * c[r] * ks_t : -INFINITY;
           }
         } else {
 #pragma unroll
@@ -434,7 +442,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         if (!warp_wait(mbar, kph, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
         const uint32_t lr = lred_s + qb * 4 * NWG * RG * 4;
         const uint32_t mr = msm_s + qb * NWG * RG * 4;
-        const long long row0 = (long long)item * rows;
+        const long long row0 = (long long)item * rows + rbase;
+        const int rows_here = rows - rbase;
         // [0]: this group, [1]: the other (8 rows only)
         float lsum[2][RG], mg[2][RG];
 #pragma unroll
@@ -472,14 +481,14 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           // (lt >= 1: the row maximum's own term is exactly 1; EXT: lt = 0 for a
           // row that saw no token)
           const int row = RG * rblk + r;
-          if (row < rows && t < HD)
+          if (row < rows_here && t < HD)
             p.part_o[(row0 + row) * HD + t] = (EXT && lt == 0.f) ? 0.f : ot * (vscale * rcp_approx(lt));
           if (t == r) {
             lt_mine = lt;
             mt_mine = mt;
           }
         }
-        if (t < RG && RG * rblk + t < rows) {
+        if (t < RG && RG * rblk + t < rows_here) {
           p.part_m[row0 + RG * rblk + t] = mt_mine * kLn2;
           p.part_l[row0 + RG * rblk + t] = lt_mine;
         }
@@ -512,13 +521,14 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     bool ok = true;
 
     auto seq_len = [&](int sq) -> int { return max(0, min(__ldg(p.seq_lens + sq), p.max_blocks * bs)); };
-    auto load_q = [&](int seq, int kvh, uint4 (&qv)[NT]) {
+    auto load_q = [&](int seq, int vh, uint4 (&qv)[NT]) {
 #pragma unroll
       for (int h = 0; h < NT; ++h) qv[h] = make_uint4(0, 0, 0, 0);
       if (seq < 0) return;
+      const int kvh = vh / RB;
 #pragma unroll
       for (int h = 0; h < NT; ++h) {
-        const int row = qrow + 8 * h;       // EXT: row qoff * qg + g
+        const int row = 16 * (vh % RB) + qrow + 8 * h;       // EXT: row qoff * qg + g
         const int qoff = EXT ? row / p.qg : 0, g = EXT ? row - qoff * p.qg : row;
         if (row < rows && h16 < HD / 8)
           qv[h] = __ldg(reinterpret_cast<const uint4*>(p.q + seq * p.q_stride_seq + (EXT ? qoff * p.q_stride_tok : 0) +
@@ -550,9 +560,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       W += (long long)__reduce_add_sync(0xffffffffu, (unsigned)T);
       Tmax = max(Tmax, __reduce_max_sync(0xffffffffu, T));
     }
-    int NG, g, h_first, h_step;
-    if (G >= Hk) {
-      NG = G / Hk; g = blockIdx.x / Hk; h_first = blockIdx.x % Hk; h_step = Hk;
+    int NG, g, h_first, h_step;     // over the virtual heads
+    if (G >= Hv) {
+      NG = G / Hv; g = blockIdx.x / Hv; h_first = blockIdx.x % Hv; h_step = Hv;
     } else {
       NG = 1; g = 0; h_first = blockIdx.x; h_step = G;
     }
@@ -617,7 +627,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           ++sq;                                   // no tile groups: the offset stays
         }
         h += h_step;
-        if (h >= Hk || s_first >= B) return Cur{-1, h, 0, 0};
+        if (h >= Hv || s_first >= B) return Cur{-1, h, 0, 0};
         sq = s_first;
         off = off_first;
       }
@@ -639,7 +649,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         nc = (int)(range_of(cur.off + T - 1) - r0 + 1);
       }
       const int L = cur.L;
-      const int kvh = cur.h;
+      const int kvh = cur.h / RB;              // the KV head of the virtual head
+      const int rblock = cur.h % RB;
       const int nt = 2 * (tg_e - tg_b) - (((tg_e - 1) * TG + TILE < L) ? 0 : 1);
       const int item = (cur.s * Hk + kvh) * P + slot;
       // next item's query rows and first table entries
@@ -707,9 +718,12 @@ pa_fp8_partition_kernel(const Fp8Params p) {
               asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(e[0] | (e[1] << 16)),
                            "r"(e[2] | (e[3] << 16)) : "memory");
           }
-          if (h16 == 0) stsf(cbuf_s + 4 * (qb * R + row), row < rows ? base_scale * down : 0.f);
+          if (h16 == 0) stsf(cbuf_s + 4 * (qb * R + row), 16 * rblock + row < rows ? base_scale * down : 0.f);
         }
-        if (pt == 0) sts_i4(info_s + 16 * qb, make_int4(item, L, nt, tg_b));
+        if (pt == 0) {
+          sts_i4(info_s + 32 * qb, make_int4(item, L, nt, tg_b));
+          sts_i4(info_s + 32 * qb + 16, make_int4(rblock, 0, 0, 0));
+        }
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(&qfull[qb]);
@@ -778,7 +792,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       // final entry: no more items
       const int qb = qcnt & 1;
       if (qcnt < 2 || warp_wait(&qempty[qb], ((qcnt >> 1) - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) {
-        if (pt == 0) sts_i4(info_s + 16 * qb, make_int4(0, 0, 0, 0));
+        if (pt == 0) sts_i4(info_s + 32 * qb, make_int4(0, 0, 0, 0));
         __syncwarp();
         if (lane == 0) mbar_arrive(&qfull[qb]);
       }
@@ -794,7 +808,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       while (ok) {
         const int qb = qcnt & 1;
         if (!role_wait(&qfull[qb], (qcnt >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) break;
-        const int nt = lds_i4(info_s + 16 * qb).z;
+        const int nt = lds_i4(info_s + 32 * qb).z;
         ++qcnt;
         if (nt == 0) break;
         const uint32_t qa = qsm + qb * S::qBytes;
@@ -935,7 +949,8 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
   p.q_stride_tok = 0;
   p.query_len = 1;
   p.per_token = 0;
-  const long long items = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
+  p.row_blocks = (a.qg + 15) / 16;
+  const long long items = (long long)a.num_seqs * a.num_kv_heads * p.row_blocks * a.num_partitions;
   if (items <= 0) return cudaSuccess;
   const int grid = (int)std::min<long long>(items, (long long)a.num_sms);
   auto launch = [&](auto kernel, int threads, int smem) {
@@ -953,7 +968,7 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
 }
 
 // The multi-token / per-token decode on the same kernel (rows = query_len *
-// qg <= 16; head_dim 128).
+// qg <= 64, in blocks of 16; head_dim 64 or 128).
 cudaError_t launch_fp8x_partition(const Fp8ExtLaunch& a, cudaStream_t stream) {
   Fp8Params p;
   p.q = static_cast<const uint16_t*>(a.q);
@@ -980,17 +995,26 @@ cudaError_t launch_fp8x_partition(const Fp8ExtLaunch& a, cudaStream_t stream) {
   p.q_stride_tok = a.q_stride_tok;
   p.query_len = a.query_len;
   p.per_token = a.per_token;
-  const long long items = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
+  const int rows = a.query_len * a.qg;
+  p.row_blocks = (rows + 15) / 16;
+  const long long items = (long long)a.num_seqs * a.num_kv_heads * p.row_blocks * a.num_partitions;
   if (items <= 0) return cudaSuccess;
   const int grid = (int)std::min<long long>(items, (long long)a.num_sms);
   auto launch = [&](auto kernel, int threads, int smem) {
     cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     kernel<<<grid, threads, smem, stream>>>(p);
   };
-  if (a.query_len * a.qg <= 8)
-    launch(pa_fp8_partition_kernel<1, 128, true>, fp8::Smem<1, true>::THREADS, fp8::Smem<1, true>::total);
-  else
-    launch(pa_fp8_partition_kernel<2, 128, true>, fp8::Smem<2, true>::THREADS, fp8::Smem<2, true>::total);
+  if (a.head_dim == 64) {
+    if (rows <= 8)
+      launch(pa_fp8_partition_kernel<1, 64, true>, fp8::Smem<1, true>::THREADS, fp8::Smem<1, true>::total);
+    else
+      launch(pa_fp8_partition_kernel<2, 64, true>, fp8::Smem<2, true>::THREADS, fp8::Smem<2, true>::total);
+  } else {
+    if (rows <= 8)
+      launch(pa_fp8_partition_kernel<1, 128, true>, fp8::Smem<1, true>::THREADS, fp8::Smem<1, true>::total);
+    else
+      launch(pa_fp8_partition_kernel<2, 128, true>, fp8::Smem<2, true>::THREADS, fp8::Smem<2, true>::total);
+  }
   return cudaGetLastError();
 }
 

@@ -38,6 +38,7 @@ struct Fp8ExtLaunch {
   long long q_stride_seq, q_stride_tok, q_stride_head;
   int num_seqs, num_kv_heads, qg, query_len, per_token, block_size, num_blocks, max_blocks, num_partitions;
   float softmax_scale;
+  int head_dim;     // 64 or 128
   int num_sms;
 };
 
@@ -48,6 +49,7 @@ struct Fp8ExtCombineLaunch {
   void* out;
   int out_bf16;
   int num_seqs, num_kv_heads, qg, query_len, num_partitions;
+  int head_dim;     // 64 or 128
   long long out_stride_seq, out_stride_tok, out_stride_head;
 };
 

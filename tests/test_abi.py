@@ -63,7 +63,7 @@ def test_host_validation(lib):
     assert _call(lib, _desc(), P=0) == -5
     assert _call(lib, _desc(head_dim=96)) == -2
     assert _call(lib, _desc(block_size=24)) == -2
-    assert _call(lib, _desc(query_group=17)) == -2
+    assert _call(lib, _desc(query_group=65)) == -2               # up to 64 query rows per KV head
     assert _call(lib, _desc(), q=ctypes.c_void_p(0)) == -1
     assert _call(lib, _desc(), q=ctypes.c_void_p(0x100008)) == -3
     assert _call(lib, _desc(q_stride_head=100)) == -3
@@ -97,7 +97,7 @@ def _call_ext(lib, d, P=2, ws_bytes=1 << 20, ks=FAKE):
 def test_ext_host_validation(lib):
     assert _call_ext(lib, _ext_desc(), P=0) == -5
     assert _call_ext(lib, _ext_desc(query_len=5)) == -2
-    assert _call_ext(lib, _ext_desc(query_len=4, query_group=8)) == -2      # 32 rows
+    assert _call_ext(lib, _ext_desc(query_len=4, query_group=17)) == -2     # 68 rows > 64
     assert _call_ext(lib, _ext_desc(query_len=4, query_group=4), ws_bytes=16) == -4
     assert _call_ext(lib, _ext_desc(per_token=2)) == -2
     assert _call_ext(lib, _ext_desc(), ks=ctypes.c_void_p(0x100004)) == -3    # per-token scales need 16 B
@@ -109,12 +109,16 @@ def test_ext_workspace_size(lib):
     n = lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=2, query_group=8)), 3)
     rows = 2 * 1 * 3 * 16
     assert n >= rows * 130 * 4 and n % 256 == 0
-    assert lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=3, query_group=8)), 3) == 0
+    n24 = lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=3, query_group=8)), 3)
+    assert n24 >= 2 * 1 * 3 * 24 * 130 * 4                       # 24 rows: two row blocks
+    assert lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=4, query_group=17)), 3) == 0
     # query_len 0 means one query token
     one = lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=0)), 2)
     assert one == lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc()), 2)
-    # head_dim 64 is served by pa_decode_fp8 only
-    assert lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=1, head_dim=64)), 2) == 0
+    # head_dim 64: rows of 64 partial values
+    n64 = lib.pa_decode_fp8_ext_workspace_size(ctypes.byref(_ext_desc(query_len=2, head_dim=64)), 2)
+    assert n64 >= 2 * 1 * 2 * 16 * 66 * 4 and n64 < lib.pa_decode_fp8_ext_workspace_size(
+        ctypes.byref(_ext_desc(query_len=2)), 2)
 
 
 def _uq_desc(**kw):

@@ -98,3 +98,25 @@ def test_benchmark_shapes_are_balanced():
     r = random.Random(1)
     work = _check([r.randint(1024, 16384) for _ in range(128)], 8, 32, 152)
     assert max(work) - min(work) <= 1
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_row_blocks_share_their_heads_slots(seed):
+    """Above 16 query rows per KV head the kernel schedules Hk * RB virtual
+    heads (virtual head vh reads KV head vh // RB and writes rows 16 (vh % RB)
+    .. of it): every row block of a head must get the same runs in the same
+    slots, or its rows would be combined with another block's state."""
+    r = random.Random(100 + seed)
+    for _ in range(60):
+        B = r.choice([1, 3, 16, 40])
+        lens = [r.choice([0, 1, 257, r.randint(1, 20000)]) for _ in range(B)]
+        Hk, RB = r.choice([1, 2, 8]), r.choice([2, 3, 4])
+        P, G = r.choice([1, 2, 7, 32]), r.choice([5, 64, 152])
+        Ts, cover, empties, _ = _schedule(lens, Hk * RB, P, G)
+        _check(lens, Hk * RB, P, G)
+        for s in range(B):
+            for h in range(Hk):
+                runs = [sorted(cover.get((s, h * RB + rb), [])) for rb in range(RB)]
+                assert all(x == runs[0] for x in runs)
+                emp = [empties.get((s, h * RB + rb), set()) for rb in range(RB)]
+                assert all(x == emp[0] for x in emp)

@@ -105,7 +105,7 @@ def test_block_sizes(bs):
     _check(c, out.cpu().double().numpy(), what=f"bs={bs}")
 
 
-@pytest.mark.parametrize("qg", [1, 4, 6, 8, 12, 16])
+@pytest.mark.parametrize("qg", [1, 4, 6, 8, 12, 16, 24, 32, 64])
 def test_query_groups(qg):
     c = synth.make_fp8_case(80 + qg, [5, 129, 600], 2, qg, 128, 16)
     out, _, _ = Fp8Dev(c).run(2)
@@ -178,7 +178,7 @@ def test_full_ragged_config_all_units():
 
 # ---- head_dim 64 ([PA]: head_dim 64 or 128)
 @pytest.mark.parametrize("P", [1, 3, 32])
-@pytest.mark.parametrize("qg", [8, 16, 5])
+@pytest.mark.parametrize("qg", [8, 16, 5, 48])
 def test_head_dim_64(P, qg):
     c = synth.make_fp8_case(900 + P + qg, [0, 1, 127, 128, 129, 255, 256, 257, 1000, 3000], 2, qg, head_dim=64)
     out, _, _ = Fp8Dev(c).run(P)
@@ -193,6 +193,15 @@ def test_head_dim_64_block_sizes_and_bf16(bs):
     _check(c, out.cpu().double().numpy(), what=f"hd64 bs={bs}")
     o16, _, _ = d.run(4, out_dtype=torch.bfloat16)
     assert torch.max(torch.abs(o16.float() - out)).item() <= torch.max(torch.abs(out)).item() * 2 ** -8 + 1e-6
+
+
+@pytest.mark.parametrize("P", [1, 5, 32])
+def test_wide_group_partition_counts(P):
+    """Query group 32 (two blocks of 16 rows over one KV head's pages) with
+    ragged lengths and several partition counts."""
+    c = synth.make_fp8_case(970 + P, [0, 1, 255, 257, 1500, 4000], 3, 32, 128, 16)
+    out, _, _ = Fp8Dev(c).run(P)
+    _check(c, out.cpu().double().numpy(), what=f"qg32 P={P}")
 
 
 def test_head_dim_64_long_all_units():

@@ -73,10 +73,22 @@ LENS = [0, 1, 2, 3, 15, 16, 17, 63, 64, 65, 255, 256, 257, 1000, 2049]
 
 
 @pytest.mark.parametrize("per_token", [False, True])
-@pytest.mark.parametrize("ql,qg", [(1, 8), (2, 8), (3, 4), (4, 4), (1, 16), (4, 2)])
+@pytest.mark.parametrize("ql,qg", [(1, 8), (2, 8), (3, 4), (4, 4), (1, 16), (4, 2),
+                                   # above 16 rows: blocks of 16 query rows
+                                   (3, 8), (4, 8), (2, 16), (4, 16), (1, 24), (3, 7)])
 def test_query_len_and_scales(ql, qg, per_token):
     c = synth.make_fp8_ext_case(500 + 10 * ql + qg + (7 if per_token else 0), LENS, 2, qg, ql, per_token)
     _check(c, _run(c, 3), what=f"ql={ql} qg={qg} per_token={per_token}")
+
+
+@pytest.mark.parametrize("per_token", [False, True])
+@pytest.mark.parametrize("ql,qg,P", [(1, 8, 2), (4, 4, 3), (2, 8, 1), (4, 8, 7), (3, 16, 2)])
+def test_head_dim_64(ql, qg, P, per_token):
+    """head_dim 64 with several query tokens and per-token scales ([PA]'s
+    phase-split head_dim 64 commit times per_token MTP shapes)."""
+    c = synth.make_fp8_ext_case(620 + 10 * ql + qg + P + (5 if per_token else 0), LENS, 2, qg, ql, per_token,
+                                head_dim=64)
+    _check(c, _run(c, P), what=f"hd64 ql={ql} qg={qg} P={P} per_token={per_token}")
 
 
 @pytest.mark.parametrize("P", [1, 2, 7, 32, 300])
@@ -108,6 +120,14 @@ def test_bf16_output():
     a = _run(c, 2)
     b = _run(c, 2, out_dtype=torch.bfloat16)
     assert np.max(np.abs(a - b)) <= np.max(np.abs(a)) * 2 ** -8 + 1e-6
+
+
+def test_long_group8_four_tokens_all_units():
+    """16 seqs x 16384 tokens, 8 KV heads, group 8, 4 query tokens (32 rows:
+    two row blocks), per-token scales, P = 32 (the benchmark's line); all 128
+    units against the oracle."""
+    c = synth.make_fp8_ext_case(610, [16384] * 16, 8, 8, 4, True, poison=False)
+    check_units(_run(c, 32), fp8_ext_reference(c), c, what="long ql4 qg8")
 
 
 def test_long_sequences_all_units():
