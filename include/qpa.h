@@ -123,7 +123,15 @@ typedef struct qpa_fp8_desc {
   int64_t q_stride_seq;     /* elements; 0 = num_kv_heads*query_group*head_dim */
   int64_t q_stride_head;    /* elements; 0 = head_dim */
   float softmax_scale;      /* 0 = 1/sqrt(head_dim) */
+  int32_t test_flags;       /* 0; QPA_TEST_WITHHOLD_ARRIVAL only in tests of the timeout path */
 } qpa_fp8_desc;
+
+/* Test-only: the partition kernel's first copy warp withholds its arrival on
+ * the barrier of its CTA's first K/V tile, so that the roles waiting for that
+ * tile run into their time limit. The call returns, the tile's partials are
+ * not defined, and qpa_kernel_error() reports 1 or 2. Exercises the bounded
+ * waits and the teardown that follows a timeout; not for use otherwise. */
+#define QPA_TEST_WITHHOLD_ARRIVAL 1
 
 size_t pa_decode_fp8_workspace_size(const qpa_fp8_desc* d, int num_partitions);
 

@@ -23,6 +23,7 @@ QPA_UQ_UE8M0_SCALES = 1
 QPA_UQ_Q_HAIRCUT = 2
 QPA_UQ_ROT_PERM = 4
 QPA_IDX_PER_TOKEN = 1
+QPA_TEST_WITHHOLD_ARRIVAL = 1
 _lib = None
 
 
@@ -39,7 +40,7 @@ class Fp8Desc(ctypes.Structure):
                 ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
                 ("max_blocks_per_seq", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
                 ("q_stride_seq", ctypes.c_int64), ("q_stride_head", ctypes.c_int64),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("test_flags", ctypes.c_int32)]
 
 
 class Fp8ExtDesc(ctypes.Structure):

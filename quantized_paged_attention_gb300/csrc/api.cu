@@ -214,6 +214,7 @@ int pa_decode_fp8_partition(const void* q, const uint8_t* kv_cache, const int32_
   a.num_partitions = num_partitions;
   a.softmax_scale = d->softmax_scale != 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
   a.head_dim = d->head_dim;
+  a.test_flags = d->test_flags;
   a.num_sms = num_sms_current();
   if (a.num_sms <= 0) return QPA_ERR_CUDA;
   return launch_fp8_partition(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;

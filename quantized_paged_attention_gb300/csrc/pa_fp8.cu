@@ -43,6 +43,7 @@
 // sees K and V unconverted and the products carry no fp8 rounding of q or p.
 // Every wait has a time limit; a timeout raises the error word and all roles
 // leave through the common teardown.
+#include "qpa.h"
 #include "common.cuh"
 #include "qpa_internal.h"
 #include "combine.cuh"
@@ -108,6 +109,7 @@ struct Fp8Params {
   // query rows per KV head above 16: blocks of 16 rows run as separate
   // "virtual heads" (KV head vh / row_blocks, rows 16 (vh % row_blocks) ..)
   int row_blocks;
+  int test_flags;   // QPA_TEST_WITHHOLD_ARRIVAL: copy warp 0 withholds its first tile's arrival
 };
 
 // HD: the cache's head_dim (64 or 128). Shared-memory rows stay 128 bytes
@@ -779,7 +781,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             cp_async16_zfill(dst, src, tok0 + 4 * ch < L, pol);
           }
           // the slot's barrier counts this lane once all its copies so far have landed
-          cp_async_arrive_noinc(&full[s]);
+          // (the timeout test withholds copy warp 0's arrival on the CTA's first tile)
+          if (!((p.test_flags & QPA_TEST_WITHHOLD_ARRIVAL) && j == 0 && pw == 0)) cp_async_arrive_noinc(&full[s]);
           ++j;
         }
       }
@@ -950,6 +953,7 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
   p.query_len = 1;
   p.per_token = 0;
   p.row_blocks = (a.qg + 15) / 16;
+  p.test_flags = a.test_flags;
   const long long items = (long long)a.num_seqs * a.num_kv_heads * p.row_blocks * a.num_partitions;
   if (items <= 0) return cudaSuccess;
   const int grid = (int)std::min<long long>(items, (long long)a.num_sms);
@@ -995,6 +999,7 @@ cudaError_t launch_fp8x_partition(const Fp8ExtLaunch& a, cudaStream_t stream) {
   p.q_stride_tok = a.q_stride_tok;
   p.query_len = a.query_len;
   p.per_token = a.per_token;
+  p.test_flags = 0;
   const int rows = a.query_len * a.qg;
   p.row_blocks = (rows + 15) / 16;
   const long long items = (long long)a.num_seqs * a.num_kv_heads * p.row_blocks * a.num_partitions;

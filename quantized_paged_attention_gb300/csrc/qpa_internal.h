@@ -22,6 +22,7 @@ struct Fp8Launch {
   int num_seqs, num_kv_heads, qg, block_size, num_blocks, max_blocks, num_partitions;
   float softmax_scale;
   int head_dim;     // 64 or 128
+  int test_flags;   // QPA_TEST_WITHHOLD_ARRIVAL
   int num_sms;
 };
 

@@ -149,6 +149,26 @@ def test_repeat_is_deterministic():
     assert torch.equal(a, b)
 
 
+def test_bounded_wait_runs_out_and_the_next_call_is_clean():
+    """The timeout path: with the test-only flag, copy warp 0 withholds its
+    arrival on its CTA's first tile, so the roles waiting for that tile run
+    into their time limit. The call returns, the error word reports a timeout
+    (1 or 2), and a normal call in the same process then passes parity."""
+    import time
+    c = synth.make_fp8_case(96, [700, 300, 5000], 2, 8, 128, 16)
+    d = Fp8Dev(c)
+    desc = d.desc()
+    desc.test_flags = qpa.QPA_TEST_WITHHOLD_ARRIVAL
+    ws = qpa.alloc_workspace(qpa.pa_decode_fp8_workspace_size(desc, 3), d.q.device)
+    t0 = time.time()
+    qpa.pa_decode_fp8(d.q, d.kv, d.bt, d.sl, d.ks, d.vs, 3, 8, workspace=ws, desc=desc)
+    assert qpa.kernel_error() in (1, 2)
+    assert time.time() - t0 < 60
+    assert qpa.kernel_error() == 0                      # reading cleared it
+    out, _, _ = d.run(3)                                # a normal call: error word stays 0 (checked in run)
+    _check(c, out.cpu().double().numpy(), what="after the timeout")
+
+
 def test_invalid_block_id_raises_error_word():
     c = synth.make_fp8_case(95, [40], 1, 8, 128, 16)
     c.block_table[0, 1] = c.kv_cache.shape[0] + 5       # past the cache
