@@ -322,7 +322,7 @@ def uq_steps(c, P, dev, q_haircut=False):
     return step, part
 
 
-def idx_step(c, dev, per_token_cols=None):
+def idx_step(c, dev, per_token_cols=None, shared_pages=False):
     import torch
     import quantized_paged_attention_gb300 as qpa
     q = torch.from_numpy(c.q_codes).to(dev)
@@ -331,7 +331,8 @@ def idx_step(c, dev, per_token_cols=None):
     sl = torch.from_numpy(c.seq_lens).to(dev)
     cols = c.num_cols if per_token_cols is None else per_token_cols
     scores = torch.empty((c.num_heads, q.shape[0], cols), dtype=torch.float32, device=dev)
-    desc = qpa.idx_desc(q, pages, bt, c.query_len, cols, scores, per_token=per_token_cols is not None)
+    desc = qpa.idx_desc(q, pages, bt, c.query_len, cols, scores, per_token=per_token_cols is not None,
+                        shared_pages=shared_pages)
 
     def step():
         qpa.nvfp4_index_score(q, pages, bt, sl, c.query_len, cols, scores=scores, desc=desc)
@@ -588,9 +589,10 @@ def main():
             extra[name] = run(fp8_ext_step(ce, 32, dev), ce.kv_bytes)
             del ce
         cs = synth.idx_shared_prefix(seed=1007 + rank)
-        extra["score_shared_prefix"] = run(idx_step(cs, dev), cs.kv_bytes,
-                                           unique_gbs_is="see unique_page_bytes",
-                                           unique_page_bytes=cs.unique_page_bytes)
+        extra["score_shared_prefix"] = run(idx_step(cs, dev), cs.kv_bytes)
+        extra["score_shared_prefix_dedup"] = run(idx_step(cs, dev, shared_pages=True), cs.unique_page_bytes,
+                                                 bytes_are="distinct pages")
+        extra["score_64req_dedup_split"] = run(idx_step(ci, dev, shared_pages=True), ci.kv_bytes)
         del cs
         out_bytes = ci.num_heads * ci.num_reqs * ci.query_len * 32768 * 4
         extra["score_per_token_32k"] = run(idx_step(ci, dev, per_token_cols=32768), ci.kv_bytes + out_bytes,

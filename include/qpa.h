@@ -320,6 +320,12 @@ int uq_decode_hd256_combine(int num_partitions, void* out, const qpa_uq_desc* d,
  *       dots before the page max ([IDX] frag_max reduces them):
  *           scores[h][r*query_len + qoff][t] = dot[t] if t <= L - query_len + qoff
  *       (t < L follows), else -inf, for every t in [0, num_cols).
+ *   QPA_IDX_SHARED_PAGES  the same scores, computed page by page as [IDX]'s
+ *       launch loop does: for each block position, the pages of a group of
+ *       8 consecutive requests are compared, and a page that several of them
+ *       map is loaded and dequantised once and scored for each of them. For
+ *       requests that share pages (a common prefix); without sharing the
+ *       default request-by-request split is faster.
  *
  * Layouts:
  *   q          uint8 (e4m3fn) [num_reqs*query_len][num_heads][128] with byte
@@ -338,6 +344,7 @@ int uq_decode_hd256_combine(int num_partitions, void* out, const qpa_uq_desc* d,
  * Alignment: q and kv_pages 16-byte aligned, scores 4-byte aligned.
  * ====================================================================== */
 #define QPA_IDX_PER_TOKEN 1
+#define QPA_IDX_SHARED_PAGES 2
 
 typedef struct qpa_idx_desc {
   int32_t num_reqs;

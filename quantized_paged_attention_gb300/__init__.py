@@ -23,6 +23,7 @@ QPA_UQ_UE8M0_SCALES = 1
 QPA_UQ_Q_HAIRCUT = 2
 QPA_UQ_ROT_PERM = 4
 QPA_IDX_PER_TOKEN = 1
+QPA_IDX_SHARED_PAGES = 2
 QPA_TEST_WITHHOLD_ARRIVAL = 1
 _lib = None
 
@@ -351,8 +352,10 @@ def uq_decode_hd256_combine(num_partitions, out, desc, workspace, stream=None):
 
 
 # --------------------------------------------------------------------- nvfp4 index scorer
-def idx_desc(q_codes, pages, block_table, query_len, num_cols, scores=None, per_token=False):
-    """num_cols counts blocks, or tokens with per_token (one column per token)."""
+def idx_desc(q_codes, pages, block_table, query_len, num_cols, scores=None, per_token=False, shared_pages=False):
+    """num_cols counts blocks, or tokens with per_token (one column per token);
+    shared_pages: score page by page over groups of 8 requests, loading a page
+    that several requests map once (for requests that share pages)."""
     RQ, H, D = q_codes.shape
     assert D == 128 and RQ % query_len == 0
     d = IdxDesc()
@@ -362,12 +365,12 @@ def idx_desc(q_codes, pages, block_table, query_len, num_cols, scores=None, per_
     d.q_stride_tok, d.q_stride_head = q_codes.stride(0), q_codes.stride(1)
     if scores is not None:
         d.s_stride_head, d.s_stride_row = scores.stride(0), scores.stride(1)
-    d.flags = QPA_IDX_PER_TOKEN if per_token else 0
+    d.flags = (QPA_IDX_PER_TOKEN if per_token else 0) | (QPA_IDX_SHARED_PAGES if shared_pages else 0)
     return d
 
 
 def nvfp4_index_score(q_codes, pages, block_table, seq_lens, query_len: int, num_cols: int, scores=None,
-                      stream=None, desc=None, per_token=False):
+                      stream=None, desc=None, per_token=False, shared_pages=False):
     """Paged NVFP4 index scores. q_codes uint8 (e4m3) [R*QL, H, 128]; pages
     uint8 [NB, 9216]; returns float32 scores [H, R*QL, num_cols] (columns are
     blocks, or tokens with per_token)."""
@@ -377,7 +380,7 @@ def nvfp4_index_score(q_codes, pages, block_table, seq_lens, query_len: int, num
         scores = torch.empty((q_codes.shape[1], q_codes.shape[0], num_cols), dtype=torch.float32,
                              device=q_codes.device)
     if desc is None:
-        desc = idx_desc(q_codes, pages, block_table, query_len, num_cols, scores, per_token)
+        desc = idx_desc(q_codes, pages, block_table, query_len, num_cols, scores, per_token, shared_pages)
     st = lib.nvfp4_index_score(_ptr(q_codes), _ptr(pages), _ptr(block_table), _ptr(seq_lens), _ptr(scores),
                                ctypes.byref(desc), _stream(stream))
     _check("nvfp4_index_score", st)

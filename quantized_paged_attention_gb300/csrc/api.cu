@@ -137,7 +137,7 @@ int idx_check(const uint8_t* q, const uint8_t* pages, const int32_t* bt, const i
   if (d->query_len * d->num_heads > 16 || d->num_blocks < 1 || d->max_blocks_per_seq < 1 || d->num_cols < 1)
     return QPA_ERR_SHAPE;
   if ((long long)d->num_reqs * d->query_len > 0x7fffffffLL) return QPA_ERR_SHAPE;
-  if (d->flags & ~QPA_IDX_PER_TOKEN) return QPA_ERR_SHAPE;
+  if (d->flags & ~(QPA_IDX_PER_TOKEN | QPA_IDX_SHARED_PAGES)) return QPA_ERR_SHAPE;
   if (d->num_reqs == 0) return QPA_OK;
   if (!q || !pages || !bt || !sl || !sc) return QPA_ERR_NULL;
   const long long ps = d->page_stride ? d->page_stride : 9216;
@@ -440,6 +440,7 @@ int nvfp4_index_score(const uint8_t* q, const uint8_t* kv_pages, const int32_t* 
   a.num_cols = d->num_cols;
   a.num_blocks = d->num_blocks;
   a.per_token = (d->flags & QPA_IDX_PER_TOKEN) != 0;
+  a.shared_pages = (d->flags & QPA_IDX_SHARED_PAGES) != 0;
   a.num_sms = num_sms_current();
   if (a.num_sms <= 0) return QPA_ERR_CUDA;
   return launch_idx_score(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;

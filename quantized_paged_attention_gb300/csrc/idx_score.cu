@@ -25,6 +25,8 @@
 //    the query rows (e4m3 -> f16, exact) on f16 mma.sync, m16n8k16 tiles of
 //    16 tokens x 8 query rows; masking is by selection, the block max is a
 //    register max plus a 3-step shuffle reduction.
+#include <type_traits>
+
 #include "common.cuh"
 #include "qpa_internal.h"
 
@@ -313,6 +315,282 @@ idx_score_kernel(const IdxParams p) {
   cp_async_wait<0>();
 }
 
+// ---------------------------------------------------------------------------
+// Shared-page variant (QPA_IDX_SHARED_PAGES): the [IDX] launch loop's dedup.
+// Requests form groups of 8; a work pair is (group, block position b). For a
+// pair, lanes 0..7 hold the group's block ids at b, __match_any_sync groups
+// equal ids, and each distinct page is loaded and dequantised once and scored
+// for every request of the group that maps it. Pairs are dealt to CTAs
+// round-robin (position-major), so every SM gets a mix of shared and unshared
+// positions; the distinct pages of a CTA's pairs go to its warps in turn.
+// A job is one distinct page and up to MC of the requests mapping it (a page
+// that more requests map is several jobs): the page is loaded once per job
+// and each 16-token tile dequantised once for the job's requests, whose query
+// fragments and block maxima stay in registers. Per warp: two page slots, the
+// next page streaming in while the current one is scored.
+namespace idxd {
+constexpr int RGS = 8;            // requests per group
+constexpr int NW = 4;
+constexpr int THREADS = NW * 32;
+constexpr int PAGE = 9216;
+constexpr int SLOTS = 2;
+constexpr int WARP_BYTES = SLOTS * PAGE;
+constexpr int SMEM = NW * WARP_BYTES;
+constexpr int CTAS_PER_SM = 3;
+}  // namespace idxd
+
+template <int NT, bool PER_TOKEN>
+__global__ void __launch_bounds__(idxd::THREADS, idxd::CTAS_PER_SM)
+idx_score_shared_kernel(const IdxParams p) {
+  using namespace idxd;
+  // requests scored per job with their query fragments in registers: a
+  // tile is dequantised once for up to MC of a page's requests
+  constexpr int MC = NT == 1 ? 4 : 2;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int R = p.num_reqs, QL = p.query_len, H = p.num_heads, S = p.num_cols;
+  const int rows = QL * H;
+  const uint64_t pol = policy_evict_first();
+  const uint32_t wbase = smem_u32(smem) + warp * WARP_BYTES;
+  const int col_blocks = PER_TOKEN ? (S + idx::BLK - 1) / idx::BLK : S;
+  auto nblocks = [&](int L) { return min((max(L, 0) + idx::BLK - 1) / idx::BLK, col_blocks); };
+  const long long GW = (long long)gridDim.x * NW;
+  const long long gw = (long long)blockIdx.x * NW + warp;
+
+  // ---- columns past each request's last block are -inf (as the plain kernel)
+  {
+    constexpr int CH = 1024;
+    const int chunks = (S + CH - 1) / CH;
+    const long long fill_units = (long long)R * rows * chunks;
+    for (long long u = gw; u < fill_units; u += GW) {
+      const int ch = (int)(u % chunks);
+      const long long rn = u / chunks;
+      const int n = (int)(rn % rows), r = (int)(rn / rows);
+      const int nb = nblocks(__ldg(p.seq_lens + r));
+      const int col0 = max(min(PER_TOKEN ? nb * idx::BLK : nb, S), ch * CH);
+      const int col1 = min(S, (ch + 1) * CH);
+      float* row = p.scores + (n % H) * p.s_stride_head + (long long)(r * QL + n / H) * p.s_stride_row;
+      for (int col = col0 + lane; col < col1; col += 32) row[col] = -INFINITY;
+    }
+  }
+
+  // ---- this warp's jobs: distinct pages of the CTA's pairs, every NW-th one
+  const int NG = (R + RGS - 1) / RGS;
+  const long long NP = (long long)NG * min(p.max_blocks, col_blocks);
+  long long v = blockIdx.x;          // the CTA's current pair
+  int pc = 0;                        // the CTA's distinct pages so far
+  unsigned pend = 0;                 // leaders of the current pair not yet dealt
+  int32_t pbid = 0;                  // this lane's block id at the current pair (lanes < RGS)
+  unsigned pmatch = 0;
+  unsigned pleft = 0;                // requests of the current page not yet dealt
+  // the next pair's length and table entry of this lane's request, loaded one
+  // pair ahead (the entry is inside the table's row even when b is past L)
+  int nL = 0;
+  int32_t nbid = 0;
+  auto prefetch_pair = [&](long long vv) {
+    if (vv < NP && lane < RGS) {
+      const int b = (int)(vv / NG), req = (int)(vv % NG) * RGS + lane;
+      if (req < R) {
+        nL = __ldg(p.seq_lens + req);
+        nbid = __ldg(p.block_table + (long long)req * p.max_blocks + b);
+      }
+    }
+  };
+  prefetch_pair(v);
+  struct Job { int b, grp, page; unsigned mappers; };
+  // next job of this warp, or page < 0 when there is none
+  auto next_job = [&]() -> Job {
+    while (true) {
+      while (pend == 0) {
+        if (v >= NP) return Job{0, 0, -1, 0u};
+        const int b = (int)(v / NG), grp = (int)(v % NG);
+        const int req = grp * RGS + lane;
+        const bool act = lane < RGS && req < R && b < nblocks(nL);
+        int32_t bid = -2 - lane;     // inactive lanes: ids no page has
+        if (act) {
+          bid = nbid;
+          if (bid < 0 || bid >= p.num_blocks) {
+            atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+            bid = 0;
+          }
+        }
+        prefetch_pair(v + gridDim.x);
+        pbid = bid;
+        pmatch = __match_any_sync(0xffffffffu, bid);
+        pend = __ballot_sync(0xffffffffu, act && lane == __ffs(pmatch) - 1);
+        if (pend == 0) v += gridDim.x;
+      }
+      // the next chunk of at most MC of the current page's requests
+      const int lead = __ffs(pend) - 1;
+      if (pleft == 0) pleft = __shfl_sync(0xffffffffu, pmatch, lead);
+      unsigned chunk = 0;
+#pragma unroll
+      for (int i = 0; i < MC; ++i)
+        if (pleft) {
+          chunk |= pleft & (0u - pleft);
+          pleft &= pleft - 1;
+        }
+      if (pleft == 0) pend &= pend - 1;
+      const int mine = (pc++ % NW) == warp;
+      const Job j{(int)(v / NG), (int)(v % NG), __shfl_sync(0xffffffffu, pbid, lead), chunk};
+      if (pend == 0) v += gridDim.x;
+      if (mine) return j;
+    }
+  };
+  auto load_page = [&](uint32_t slot, int page) {
+    const uint8_t* pg = p.pages + (long long)page * p.page_stride;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      cp_async_halfpage(slot + h * idx::HALF_CODES + 16 * lane, slot + idx::PAGE_CODES + h * idx::HALF_SCALES + 16 * lane,
+                        pg + h * idx::HALF_CODES + 16 * lane, pg + idx::PAGE_CODES + h * idx::HALF_SCALES + 16 * lane, pol);
+  };
+
+  const int g = lane >> 2;
+  const int c = lane & 3;
+  // query fragments of the job's requests: row 8 nt + g, dims [32c, 32c+32), f16x2
+  uint32_t qf[MC][NT][16];
+  auto load_q = [&](int slot_i, int req) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = nt * 8 + g;
+      uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+      if (n < rows) {
+        const uint8_t* src = p.q + (long long)(req * QL + n / H) * p.q_stride_tok + (long long)(n % H) * p.q_stride_head + 32 * c;
+        w0 = __ldg(reinterpret_cast<const uint4*>(src));
+        w1 = __ldg(reinterpret_cast<const uint4*>(src + 16));
+      }
+      const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        qf[slot_i][nt][2 * j] = e4m3x2_lo_to_f16x2(ws[j]);
+        qf[slot_i][nt][2 * j + 1] = e4m3x2_hi_to_f16x2(ws[j]);
+      }
+    }
+  };
+
+  Job cur = next_job();
+  if (cur.page >= 0) load_page(wbase, cur.page);
+  cp_async_commit();
+  for (int jn = 0; cur.page >= 0; ++jn) {
+    const Job nxt = next_job();
+    const uint32_t slot = wbase + (jn & 1) * PAGE;
+    if (nxt.page >= 0) load_page(wbase + ((jn + 1) & 1) * PAGE, nxt.page);
+    cp_async_commit();
+    const int b = cur.b;
+    // the job's requests (lanes of the group, lowest first)
+    int reqs[MC], last0[MC];
+    int nreq = 0;
+    {
+      unsigned mm = cur.mappers;
+#pragma unroll
+      for (int i = 0; i < MC; ++i) {
+        reqs[i] = mm ? cur.grp * RGS + __ffs(mm) - 1 : -1;
+        if (mm) { mm &= mm - 1; ++nreq; }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < MC; ++i)
+      if (i < nreq) {
+        load_q(i, reqs[i]);
+        last0[i] = __ldg(p.seq_lens + reqs[i]) - QL;    // row qoff sees tokens <= last0 + qoff
+      }
+    cp_async_wait<1>();
+    __syncwarp();
+    // the page's tiles for exactly K requests (no predicated-off MMAs)
+    auto score = [&](auto kc) {
+      constexpr int K = decltype(kc)::value;
+      float mx[K][NT][2];
+#pragma unroll
+      for (int i = 0; i < K; ++i)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mx[i][nt][0] = mx[i][nt][1] = -INFINITY;
+#pragma unroll (K == 1 ? 2 : 1)
+      for (int mt = 0; mt < 8; ++mt) {           // 16-token tiles of the page
+        const int half = mt >> 2, m = mt & 3;
+        const uint32_t hs = slot + half * idx::HALF_CODES;
+        const uint32_t ss = slot + idx::PAGE_CODES + half * idx::HALF_SCALES;
+        const int ra = 16 * m + g, rb = ra + 8;
+        const uint4 ka = lds128(hs + ra * 64 + 16 * c), kb = lds128(hs + rb * 64 + 16 * c);
+        const uint32_t sa = e4m3x2_lo_to_f16x2(lds32(ss + ra * 8 + 4 * (c >> 1)) >> (16 * (c & 1)));
+        const uint32_t sb = e4m3x2_lo_to_f16x2(lds32(ss + rb * 8 + 4 * (c >> 1)) >> (16 * (c & 1)));
+        const uint32_t sa0 = prmt(sa, sa, 0x1010), sa1 = prmt(sa, sa, 0x3232);
+        const uint32_t sb0 = prmt(sb, sb, 0x1010), sb1 = prmt(sb, sb, 0x3232);
+        const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+        float acc[K][NT][4];
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) acc[i][nt][0] = acc[i][nt][1] = acc[i][nt][2] = acc[i][nt][3] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t gsa = j < 2 ? sa0 : sa1, gsb = j < 2 ? sb0 : sb1;
+          const uint32_t a0 = hmul2(e2m1x2_to_f16x2<0>(wa[j]), gsa), a2 = hmul2(e2m1x2_to_f16x2<1>(wa[j]), gsa);
+          const uint32_t a4 = hmul2(e2m1x2_to_f16x2<2>(wa[j]), gsa), a6 = hmul2(e2m1x2_to_f16x2<3>(wa[j]), gsa);
+          const uint32_t b0 = hmul2(e2m1x2_to_f16x2<0>(wb[j]), gsb), b2 = hmul2(e2m1x2_to_f16x2<1>(wb[j]), gsb);
+          const uint32_t b4 = hmul2(e2m1x2_to_f16x2<2>(wb[j]), gsb), b6 = hmul2(e2m1x2_to_f16x2<3>(wb[j]), gsb);
+#pragma unroll
+          for (int i = 0; i < K; ++i)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              // k-step 2j: dims 32c+8j+{0,1} | {2,3}; k-step 2j+1: dims +{4,5} | {6,7}
+              mma_f16_16816(acc[i][nt], a0, b0, a2, b2, qf[i][nt][4 * j], qf[i][nt][4 * j + 1]);
+              mma_f16_16816(acc[i][nt], a4, b4, a6, b6, qf[i][nt][4 * j + 2], qf[i][nt][4 * j + 3]);
+            }
+        }
+        const int ta = b * idx::BLK + 16 * mt + g, tb = ta + 8;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int n = nt * 8 + 2 * c + hh;
+              const int lim = last0[i] + n / H;
+              const float va = ta <= lim ? acc[i][nt][hh] : -INFINITY;
+              const float vb = tb <= lim ? acc[i][nt][2 + hh] : -INFINITY;
+              if constexpr (PER_TOKEN) {
+                if (n < rows) {
+                  float* row = p.scores + (n % H) * p.s_stride_head + (long long)(reqs[i] * QL + n / H) * p.s_stride_row;
+                  if (ta < S) row[ta] = va;
+                  if (tb < S) row[tb] = vb;
+                }
+              } else {
+                mx[i][nt][hh] = fmaxf(mx[i][nt][hh], fmaxf(va, vb));
+              }
+            }
+          }
+        }
+      }
+      if constexpr (!PER_TOKEN) {
+        // block maxima: reduce over the 8 token lanes, lanes g == 0 store rows 8 nt + 2c + hh
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              float v = mx[i][nt][hh];
+#pragma unroll
+              for (int sh = 4; sh < 32; sh <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, sh));
+              const int n = nt * 8 + 2 * c + hh;
+              if (g == 0 && n < rows)
+                p.scores[(n % H) * p.s_stride_head + (long long)(reqs[i] * QL + n / H) * p.s_stride_row + b] = v;
+            }
+      }
+    };
+    if (nreq == 1) score(std::integral_constant<int, 1>{});
+    else if (nreq == 2) score(std::integral_constant<int, 2>{});
+    else if constexpr (MC > 2) {
+      if (nreq == 3) score(std::integral_constant<int, 3>{});
+      else score(std::integral_constant<int, MC>{});
+    }
+    __syncwarp();
+    cur = nxt;
+  }
+  cp_async_wait<0>();
+}
+
 cudaError_t launch_idx_score(const IdxLaunch& a, cudaStream_t stream) {
   IdxParams p;
   p.q = a.q;
@@ -339,6 +617,19 @@ cudaError_t launch_idx_score(const IdxLaunch& a, cudaStream_t stream) {
     kernel<<<grid, idx::THREADS, idx::SMEM, stream>>>(p);
   };
   const bool two = a.query_len * a.num_heads > 8;
+  if (a.shared_pages) {
+    const int sgrid = idxd::CTAS_PER_SM * a.num_sms;
+    auto launch_s = [&](auto kernel) {
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, idxd::SMEM);
+      kernel<<<sgrid, idxd::THREADS, idxd::SMEM, stream>>>(p);
+    };
+    if (a.per_token) {
+      if (two) launch_s(idx_score_shared_kernel<2, true>); else launch_s(idx_score_shared_kernel<1, true>);
+    } else {
+      if (two) launch_s(idx_score_shared_kernel<2, false>); else launch_s(idx_score_shared_kernel<1, false>);
+    }
+    return cudaGetLastError();
+  }
   if (a.per_token) {
     if (two) launch(idx_score_kernel<2, true>); else launch(idx_score_kernel<1, true>);
   } else {

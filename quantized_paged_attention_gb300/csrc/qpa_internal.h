@@ -91,6 +91,7 @@ struct IdxLaunch {
   long long s_stride_head, s_stride_row;                // elements
   int num_reqs, query_len, num_heads, max_blocks, num_cols, num_blocks;
   int per_token;    // one column per token (QPA_IDX_PER_TOKEN)
+  int shared_pages; // page-major dedup over groups of 8 requests (QPA_IDX_SHARED_PAGES)
   int num_sms;
 };
 

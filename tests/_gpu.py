@@ -119,12 +119,13 @@ class IdxDev:
         self.bt = torch.from_numpy(c.block_table).to(device)
         self.sl = torch.from_numpy(c.seq_lens).to(device)
 
-    def run(self, scores=None, per_token_cols=None):
+    def run(self, scores=None, per_token_cols=None, shared_pages=False):
         """Block scores over c.num_cols columns, or with per_token_cols the
-        per-token scores over that many token columns."""
+        per-token scores over that many token columns; shared_pages selects
+        the page-by-page dedup split."""
         cols = self.c.num_cols if per_token_cols is None else per_token_cols
         out = qpa.nvfp4_index_score(self.q, self.pages, self.bt, self.sl, self.c.query_len, cols,
-                                    scores=scores, per_token=per_token_cols is not None)
+                                    scores=scores, per_token=per_token_cols is not None, shared_pages=shared_pages)
         torch.cuda.synchronize()
         assert qpa.kernel_error() == 0
         return out

@@ -137,11 +137,12 @@ def test_idx_flags_validation(lib):
     d = qpa.IdxDesc()
     d.num_reqs, d.query_len, d.num_heads, d.head_dim = 2, 4, 2, 128
     d.num_blocks, d.max_blocks_per_seq, d.num_cols = 8, 4, 512
-    for f, want in ((2, -2), (-1, -2)):
+    for f, want in ((4, -2), (-1, -2)):
         d.flags = f
         assert lib.nvfp4_index_score(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(d), None) == want
-    d.flags = 1
-    assert lib.nvfp4_index_score(ctypes.c_void_p(0), FAKE, FAKE, FAKE, FAKE, ctypes.byref(d), None) == -1
+    for f in (1, 2, 3):        # per-token output, shared-page split, both
+        d.flags = f
+        assert lib.nvfp4_index_score(ctypes.c_void_p(0), FAKE, FAKE, FAKE, FAKE, ctypes.byref(d), None) == -1
 
 
 def test_uq_flags_validation(lib):

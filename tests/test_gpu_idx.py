@@ -126,3 +126,47 @@ def test_shared_prefix_full_all_requests():
     benchmark's shared-prefix line); all 64 requests against the oracle."""
     c = synth.idx_shared_prefix()
     _check_all_requests(c, IdxDev(c).run().cpu().double().numpy(), what="shared prefix full")
+
+
+# ---- page-by-page dedup of shared pages (QPA_IDX_SHARED_PAGES)
+@pytest.mark.parametrize("ql,h", [(4, 2), (1, 1), (3, 4), (2, 4)])
+@pytest.mark.parametrize("shared", [0, 2, 5])
+def test_shared_pages_flag_small(ql, h, shared):
+    """The dedup split against the oracle and bit for bit against the default
+    split, with and without a shared prefix, on ragged lengths (requests
+    shorter than the prefix, empty requests, a group of 8 cut short)."""
+    lens = [0, 1, 130, 300, 700, 1000, 256, 129, 900, 5, 640, 777, 3]
+    c = synth.make_idx_case(400 + 10 * ql + h + shared, lens, query_len=ql, num_heads=h, num_cols=9,
+                            shared_prefix_blocks=shared)
+    d = IdxDev(c)
+    got = d.run(shared_pages=True)
+    check_scores(got.cpu().double().numpy(), _ref(c), what=f"shared flag ql={ql} h={h} prefix={shared}")
+    assert torch.equal(got, d.run())
+
+
+@pytest.mark.parametrize("cols", [1536, 700])
+def test_shared_pages_flag_per_token(cols):
+    c = synth.make_idx_case(430, [300, 700, 1000, 256, 129, 900, 64, 1100, 33], query_len=4, num_heads=2,
+                            num_cols=9, shared_prefix_blocks=3)
+    d = IdxDev(c)
+    got = d.run(per_token_cols=cols, shared_pages=True)
+    check_scores(got.cpu().double().numpy(), _ref_tok(c, cols), what=f"shared flag per-token cols={cols}")
+    assert torch.equal(got, d.run(per_token_cols=cols))
+
+
+def test_shared_pages_flag_full_prefix_workload_all_requests():
+    """The benchmark's shared-prefix workload (64 requests sharing 128 prefix
+    pages) through the dedup split: all requests against the oracle."""
+    c = synth.idx_shared_prefix()
+    d = IdxDev(c)
+    got = d.run(shared_pages=True)
+    _check_all_requests(c, got.cpu().double().numpy(), what="shared prefix dedup")
+    assert torch.equal(got, d.run())
+
+
+def test_shared_pages_flag_unshared_full_workload():
+    """The unshared 64-request workload through the dedup split (every page
+    has one mapper): identical to the default split."""
+    c = synth.idx_full()
+    d = IdxDev(c)
+    assert torch.equal(d.run(shared_pages=True), d.run())
