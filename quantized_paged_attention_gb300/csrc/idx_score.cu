@@ -34,7 +34,6 @@ namespace qpa {
 
 namespace idx {
 constexpr int BLK = 128;          // tokens per page
-constexpr int D = 128;
 constexpr int PAGE_CODES = 8192;
 constexpr int NW = 4;
 constexpr int THREADS = NW * 32;
@@ -45,19 +44,6 @@ constexpr int SLOT_BYTES = HALF_CODES + HALF_SCALES;   // 4608 (query rows need 
 constexpr int SMEM = NW * DEPTH * SLOT_BYTES;
 constexpr int CTAS_PER_SM = 3;
 }  // namespace idx
-
-struct IdxParams {
-  const uint8_t* q;
-  const uint8_t* pages;
-  const int32_t* block_table;
-  const int32_t* seq_lens;
-  float* scores;
-  long long page_stride;                  // bytes
-  long long q_stride_tok, q_stride_head;  // bytes
-  long long s_stride_head, s_stride_row;  // elements
-  int num_reqs, query_len, num_heads, max_blocks, num_cols, num_blocks;
-  int per_token;    // one column per token instead of the block max
-};
 
 enum : int { IEV_NONE = 0, IEV_ITEM = 1, IEV_HALF = 2 };
 
@@ -198,6 +184,19 @@ idx_score_kernel(const IdxParams p) {
   // ---------------------------------------------------------------- consume side
   const int g = lane >> 2;
   const int c = lane & 3;
+  // this lane's accumulator rows n = 8 nt + 2c + hh: query offset n / H and
+  // the score row's offset without the request's (divisions once, not per tile)
+  int qo[NT][2];
+  long long ro[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int n = nt * 8 + 2 * c + hh;
+      qo[nt][hh] = n / H;
+      ro[nt][hh] = (long long)(n % H) * p.s_stride_head + (long long)qo[nt][hh] * p.s_stride_row;
+    }
+  const long long req_stride = (long long)QL * p.s_stride_row;
   uint32_t qf[NT][16];     // query row 8 nt + g, dims [32c, 32c+32), f16x2
   float mx[NT][2];         // running block max of rows 8nt+2c, 8nt+2c+1
 
@@ -277,13 +276,13 @@ idx_score_kernel(const IdxParams p) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int n = nt * 8 + 2 * c + hh;
-          const int lim = last0 + n / H;
+          const int lim = last0 + qo[nt][hh];
           const float va = ta <= lim ? acc[nt][hh] : -INFINITY;
           const float vb = tb <= lim ? acc[nt][2 + hh] : -INFINITY;
           if constexpr (PER_TOKEN) {
             // 8 lanes of equal c write 8 consecutive tokens of one row
             if (n < rows) {
-              float* row = p.scores + (n % H) * p.s_stride_head + (long long)(er * QL + n / H) * p.s_stride_row;
+              float* row = p.scores + er * req_stride + ro[nt][hh];
               if (ta < S) row[ta] = va;
               if (tb < S) row[tb] = vb;
             }
@@ -303,10 +302,7 @@ idx_score_kernel(const IdxParams p) {
 #pragma unroll
           for (int sh = 4; sh < 32; sh <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, sh));
           const int n = nt * 8 + 2 * c + hh;
-          if (g == 0 && n < rows) {
-            const int qoff = n / H, h = n % H;
-            p.scores[h * p.s_stride_head + (long long)(er * QL + qoff) * p.s_stride_row + b] = v;
-          }
+          if (g == 0 && n < rows) p.scores[er * req_stride + ro[nt][hh] + b] = v;
         }
       }
     }
@@ -448,6 +444,19 @@ idx_score_shared_kernel(const IdxParams p) {
 
   const int g = lane >> 2;
   const int c = lane & 3;
+  // this lane's accumulator rows n = 8 nt + 2c + hh: query offset n / H and
+  // the score row's offset without the request's
+  int qo[NT][2];
+  long long ro[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int n = nt * 8 + 2 * c + hh;
+      qo[nt][hh] = n / H;
+      ro[nt][hh] = (long long)(n % H) * p.s_stride_head + (long long)qo[nt][hh] * p.s_stride_row;
+    }
+  const long long req_stride = (long long)QL * p.s_stride_row;
   // query fragments of the job's requests: row 8 nt + g, dims [32c, 32c+32), f16x2
   uint32_t qf[MC][NT][16];
   auto load_q = [&](int slot_i, int req) {
@@ -545,13 +554,12 @@ idx_score_shared_kernel(const IdxParams p) {
           for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-              const int n = nt * 8 + 2 * c + hh;
-              const int lim = last0[i] + n / H;
+              const int lim = last0[i] + qo[nt][hh];
               const float va = ta <= lim ? acc[i][nt][hh] : -INFINITY;
               const float vb = tb <= lim ? acc[i][nt][2 + hh] : -INFINITY;
               if constexpr (PER_TOKEN) {
-                if (n < rows) {
-                  float* row = p.scores + (n % H) * p.s_stride_head + (long long)(reqs[i] * QL + n / H) * p.s_stride_row;
+                if (nt * 8 + 2 * c + hh < rows) {
+                  float* row = p.scores + reqs[i] * req_stride + ro[nt][hh];
                   if (ta < S) row[ta] = va;
                   if (tb < S) row[tb] = vb;
                 }
@@ -575,7 +583,7 @@ idx_score_shared_kernel(const IdxParams p) {
               for (int sh = 4; sh < 32; sh <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, sh));
               const int n = nt * 8 + 2 * c + hh;
               if (g == 0 && n < rows)
-                p.scores[(n % H) * p.s_stride_head + (long long)(reqs[i] * QL + n / H) * p.s_stride_row + b] = v;
+                p.scores[reqs[i] * req_stride + ro[nt][hh] + b] = v;
             }
       }
     };

@@ -81,6 +81,20 @@ struct UqLaunch {
   int num_sms;
 };
 
+// kernel parameters of the scorer kernels
+struct IdxParams {
+  const uint8_t* q;
+  const uint8_t* pages;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* scores;
+  long long page_stride;                  // bytes
+  long long q_stride_tok, q_stride_head;  // bytes
+  long long s_stride_head, s_stride_row;  // elements
+  int num_reqs, query_len, num_heads, max_blocks, num_cols, num_blocks;
+  int per_token;    // one column per token instead of the block max
+};
+
 struct IdxLaunch {
   const uint8_t* q;
   const uint8_t* pages;
@@ -121,5 +135,12 @@ UqPlan uq_plan(int num_kv_heads, int query_group);
 cudaError_t launch_uq_partition(const UqLaunch& a, cudaStream_t stream);
 cudaError_t launch_uq_combine(const CombineLaunch& a, cudaStream_t stream);
 cudaError_t launch_idx_score(const IdxLaunch& a, cudaStream_t stream);
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link-time dependency on the driver library); null if the driver lacks it.
+EncodeTiledFn encode_tiled();
 
 }  // namespace qpa

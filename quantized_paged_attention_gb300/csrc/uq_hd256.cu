@@ -690,13 +690,7 @@ UqPlan uq_plan(int num_kv_heads, int query_group) {
   return pl;   // hg = 0: not reachable for query_group <= 16 (hg = 1 always fits)
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// The driver's tensor-map encoder, looked up once through the runtime (no
-// link-time dependency on the driver library); null if the driver lacks it.
-static EncodeTiledFn encode_tiled() {
+EncodeTiledFn encode_tiled() {
   static EncodeTiledFn fn = [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;

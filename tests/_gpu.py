@@ -111,11 +111,19 @@ def uq_v_absmax(c, s, h):
 
 
 class IdxDev:
-    def __init__(self, c, device=None):
+    def __init__(self, c, device=None, stride_pad=0):
+        """stride_pad > 0 stores the pages at a stride of 9216 + stride_pad
+        bytes (a view into a wider buffer)."""
         device = device or dev()
         self.c = c
         self.q = torch.from_numpy(c.q_codes).to(device)
-        self.pages = torch.from_numpy(c.pages).to(device)
+        pages = torch.from_numpy(c.pages)
+        if stride_pad:
+            wide = torch.zeros((pages.shape[0], pages.shape[1] + stride_pad), dtype=torch.uint8)
+            wide[:, :pages.shape[1]] = pages
+            self.pages = wide.to(device)[:, :pages.shape[1]]
+        else:
+            self.pages = pages.to(device)
         self.bt = torch.from_numpy(c.block_table).to(device)
         self.sl = torch.from_numpy(c.seq_lens).to(device)
 

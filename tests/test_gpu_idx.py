@@ -10,6 +10,9 @@ from _oracle_pool import idx_reference
 
 pytestmark = pytest.mark.gpu
 
+# page strides: the dense 9216 bytes and 9232 (pages in a wider buffer)
+KERNELS = {"dense": 0, "stride9232": 16}
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
@@ -22,12 +25,25 @@ def _ref(c, reqs=None):
                                     reqs=reqs)
 
 
-@pytest.mark.parametrize("ql,h", [(4, 2), (1, 1), (2, 4), (3, 2), (4, 4)])
-def test_small_ragged(ql, h):
+@pytest.mark.parametrize("kernel", list(KERNELS))
+@pytest.mark.parametrize("ql,h", [(4, 2), (1, 1), (2, 4), (3, 2), (4, 4), (1, 16), (8, 2)])
+def test_small_ragged(ql, h, kernel):
     lens = [0, 1, 3, 4, 5, 127, 128, 129, 255, 256, 257, 1000]
     c = synth.make_idx_case(300 + ql * 10 + h, lens, query_len=ql, num_heads=h, num_cols=12)
-    got = IdxDev(c).run().cpu().double().numpy()
-    check_scores(got, _ref(c), what=f"ql={ql} h={h}")
+    got = IdxDev(c, stride_pad=KERNELS[kernel]).run().cpu().double().numpy()
+    check_scores(got, _ref(c), what=f"{kernel} ql={ql} h={h}")
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+def test_many_short_requests_and_table_entries(kernel):
+    """300 requests of 0..700 tokens (most CTAs take pages of several
+    requests, so the query operand changes many times per CTA) and a table
+    wider than the columns."""
+    r = np.random.default_rng(9)
+    lens = [int(x) for x in r.integers(0, 700, 300)]
+    c = synth.make_idx_case(309, lens, query_len=2, num_heads=4, num_cols=5)
+    got = IdxDev(c, stride_pad=KERNELS[kernel]).run().cpu().double().numpy()
+    check_scores(got, _ref(c), what=f"{kernel} many requests")
 
 
 def test_columns_beyond_blocks_and_table_width():
@@ -66,11 +82,13 @@ def _check_all_requests(c, got, per_token_cols=None, what=""):
     check_scores(got, full, what=what)
 
 
-def test_full_config_all_requests():
+@pytest.mark.parametrize("kernel", list(KERNELS))
+def test_full_config_all_requests(kernel):
     """64 requests, lengths U[4096, 32768], query_len 4, 2 heads, S=256 (as
     the benchmark runs it); all 64 requests against the oracle."""
     c = synth.idx_full()
-    _check_all_requests(c, IdxDev(c).run().cpu().double().numpy(), what="idx-full")
+    _check_all_requests(c, IdxDev(c, stride_pad=KERNELS[kernel]).run().cpu().double().numpy(),
+                        what=f"idx-full {kernel}")
 
 
 # ---- per-token output
@@ -83,11 +101,12 @@ def _ref_tok(c, cols, reqs=None):
 @pytest.mark.parametrize("cols", [1536, 1000, 77])
 def test_per_token_small_ragged(ql, h, cols):
     """Token columns past the table (1536 > 12 blocks), ending inside a block
-    (1000) and short of most requests (77)."""
+    (1000) and short of most requests (77); both kernels."""
     lens = [0, 1, 3, 4, 5, 127, 128, 129, 255, 256, 257, 1000]
     c = synth.make_idx_case(330 + ql * 10 + h, lens, query_len=ql, num_heads=h, num_cols=12)
-    got = IdxDev(c).run(per_token_cols=cols).cpu().double().numpy()
-    check_scores(got, _ref_tok(c, cols), what=f"per-token ql={ql} h={h} cols={cols}")
+    for kernel, pad in KERNELS.items():
+        got = IdxDev(c, stride_pad=pad).run(per_token_cols=cols).cpu().double().numpy()
+        check_scores(got, _ref_tok(c, cols), what=f"{kernel} per-token ql={ql} h={h} cols={cols}")
 
 
 def test_per_token_strided_and_block_max():
@@ -132,41 +151,37 @@ def test_shared_prefix_full_all_requests():
 @pytest.mark.parametrize("ql,h", [(4, 2), (1, 1), (3, 4), (2, 4)])
 @pytest.mark.parametrize("shared", [0, 2, 5])
 def test_shared_pages_flag_small(ql, h, shared):
-    """The dedup split against the oracle and bit for bit against the default
-    split, with and without a shared prefix, on ragged lengths (requests
+    """The dedup split against the oracle and bit for bit against the
+    request-by-request split (the same dequantisation and MMA tiles), with and without a shared prefix, on ragged lengths (requests
     shorter than the prefix, empty requests, a group of 8 cut short)."""
     lens = [0, 1, 130, 300, 700, 1000, 256, 129, 900, 5, 640, 777, 3]
     c = synth.make_idx_case(400 + 10 * ql + h + shared, lens, query_len=ql, num_heads=h, num_cols=9,
                             shared_prefix_blocks=shared)
-    d = IdxDev(c)
-    got = d.run(shared_pages=True)
+    got = IdxDev(c).run(shared_pages=True)
     check_scores(got.cpu().double().numpy(), _ref(c), what=f"shared flag ql={ql} h={h} prefix={shared}")
-    assert torch.equal(got, d.run())
+    assert torch.equal(got, IdxDev(c, stride_pad=KERNELS["stride9232"]).run())
 
 
 @pytest.mark.parametrize("cols", [1536, 700])
 def test_shared_pages_flag_per_token(cols):
     c = synth.make_idx_case(430, [300, 700, 1000, 256, 129, 900, 64, 1100, 33], query_len=4, num_heads=2,
                             num_cols=9, shared_prefix_blocks=3)
-    d = IdxDev(c)
-    got = d.run(per_token_cols=cols, shared_pages=True)
+    got = IdxDev(c).run(per_token_cols=cols, shared_pages=True)
     check_scores(got.cpu().double().numpy(), _ref_tok(c, cols), what=f"shared flag per-token cols={cols}")
-    assert torch.equal(got, d.run(per_token_cols=cols))
+    assert torch.equal(got, IdxDev(c, stride_pad=KERNELS["stride9232"]).run(per_token_cols=cols))
 
 
 def test_shared_pages_flag_full_prefix_workload_all_requests():
     """The benchmark's shared-prefix workload (64 requests sharing 128 prefix
     pages) through the dedup split: all requests against the oracle."""
     c = synth.idx_shared_prefix()
-    d = IdxDev(c)
-    got = d.run(shared_pages=True)
+    got = IdxDev(c).run(shared_pages=True)
     _check_all_requests(c, got.cpu().double().numpy(), what="shared prefix dedup")
-    assert torch.equal(got, d.run())
+    assert torch.equal(got, IdxDev(c, stride_pad=KERNELS["stride9232"]).run())
 
 
 def test_shared_pages_flag_unshared_full_workload():
     """The unshared 64-request workload through the dedup split (every page
-    has one mapper): identical to the default split."""
+    has one mapper): identical to the request-by-request split."""
     c = synth.idx_full()
-    d = IdxDev(c)
-    assert torch.equal(d.run(shared_pages=True), d.run())
+    assert torch.equal(IdxDev(c).run(shared_pages=True), IdxDev(c, stride_pad=KERNELS["stride9232"]).run())
