@@ -31,7 +31,10 @@ inline int combine_threads(int d, int kmax, int num_partitions) {
 
 // Returns in vec[0..D) (shared memory) the combined row. `sw` is dynamic
 // shared scratch of combine_smem_bytes(P, threads) bytes (16-byte aligned).
-template <int D, int KMAX>
+// EAGER: the first round of O loads is issued together with the (m, l) loads
+// instead of after the weights are known (one round trip instead of two, for
+// rows whose slots are all written); an O of weight 0 is never used.
+template <int D, int KMAX, bool EAGER = false>
 __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, const float* __restrict__ part_m,
                                             const float* __restrict__ part_l, long long rbase, int qg,
                                             int num_partitions, float* sw, float* vec) {
@@ -46,6 +49,14 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
   // rbase = ((seq * Hk + kvh) * P) * qg + r: partition pp of the row is at rbase + pp * qg
   const float* ob = part_o + rbase * D + 4 * v4;
   const long long pstride = (long long)qg * D;
+  float4 o0[EAGER ? KMAX : 1];
+  if constexpr (EAGER) {
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      const int pp = sub + k * nsub;
+      o0[k] = pp < P ? __ldg(reinterpret_cast<const float4*>(ob + pp * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   for (int pp = tid; pp < P; pp += blockDim.x) {
     ms[pp] = part_m[rbase + (long long)pp * qg];
     ls[pp] = part_l[rbase + (long long)pp * qg];
@@ -66,7 +77,19 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
   for (int sh = 16; sh; sh >>= 1) den += __shfl_xor_sync(0xffffffffu, den, sh);
   const float inv = den > 0.f ? 1.f / den : 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int base = 0; base < P; base += KMAX * nsub) {
+  int base0 = 0;
+  if constexpr (EAGER) {
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      const int pp = sub + k * nsub;
+      const float w = pp < P ? weight(pp) * inv : 0.f;
+      if (w != 0.f) {
+        acc.x += w * o0[k].x; acc.y += w * o0[k].y; acc.z += w * o0[k].z; acc.w += w * o0[k].w;
+      }
+    }
+    base0 = KMAX * nsub;
+  }
+  for (int base = base0; base < P; base += KMAX * nsub) {
     float w[KMAX];
     float4 o[KMAX];
 #pragma unroll

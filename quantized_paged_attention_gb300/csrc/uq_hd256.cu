@@ -19,15 +19,15 @@
 // (the logits then take no further scale), and the rotation's column
 // permutation (a permuted q load here, a permuted store in the combine).
 //
-// GB300 design. One persistent CTA per SM: a producer warp streams 32-token
-// slices of a group of HG KV heads into a ring of shared-memory stages (one
-// tensor-map box of 32 token rows x 272 bytes per head, completion counted on
-// the stage's mbarrier), and eight consumer warps compute. A work item is
-// (sequence, head group, partition); consumer warp w owns one (head of the
-// group, 8-row half of the query group) and every J-th slice of the item
-// (J = 8 / (HG x halves)), keeps its own softmax state and writes it as its
-// own partial slot, so the combine merges P x J slots per query row and no
-// warp ever waits on another consumer. Per 16-token tile:
+// GB300 design. One persistent CTA per SM: two producer warps stream 32-token
+// slices of a group of HG KV heads into a ring of shared-memory stages,
+// alternate stages each (one tensor-map box of 32 token rows x 272 bytes per
+// head, completion counted on the stage's mbarrier), and eight consumer warps
+// compute. A work item is (sequence, head group, partition); consumer warp w
+// owns one (head of the group, 8-row half of the query group) and every J-th
+// slice of the item (J = 8 / (HG x halves)), keeps its own softmax state and
+// writes it as its own partial slot, so the combine merges P x J slots per
+// query row and no warp ever waits on another consumer. Per 16-token tile:
 //  * K by ldmatrix: lane (g, c) receives word c of each 32-dim group's codes
 //    for token rows g and g+8, so every f16 m16n8k16 MMA (e2m1 -> f16 with
 //    cvt, exact) stays inside one scale group; the group's scale multiplies
@@ -57,7 +57,8 @@ constexpr int D = 256;
 constexpr int TG = 256;
 constexpr int SLICE = 32;                        // tokens per stage: two 16-token MMA tiles
 constexpr int NC = 8;                            // consumer warps
-constexpr int THREADS = (NC + 1) * 32;           // + the producer warp
+constexpr int NPW = 2;                           // producer warps (alternate stages)
+constexpr int THREADS = (NC + NPW) * 32;
 constexpr int CONTENT = 272;                     // used bytes of a slot
 constexpr int HEAD_SLICE = SLICE * CONTENT;      // 8704: 32 slots of one head, dense
 constexpr int KS_OFF = 128, VC_OFF = 136, VS_OFF = 264;
@@ -192,17 +193,18 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
     return max(0, min(__ldg(p.seq_lens + seq), p.max_blocks * bs));
   };
 
-  if (warp == NC) {
+  if (warp >= NC) {
     // ================================================================ producer
+    // Two producer warps take alternate stages (one issuing thread streams
+    // only about 36 GB/s of tensor-map boxes from HBM; an SM needs ~45). The
+    // copy coordinates of an item's slices are computed 32 slices at a time,
+    // lane l taking slice 32 c + l (its block-table entries loaded in
+    // parallel, one chunk ahead); the per-stage path is then two shuffles,
+    // the stage's empty wait by lane 0, and lane 0's copies.
+    const int pw = warp - NC;
     const uint64_t pol = policy_evict_first();
-    const int bpt = TG / bs;     // block-table entries per tile group (1..16)
-    auto load_entries = [&](int seq, int tg, int L) -> int32_t {
-      const int e = tg * bpt + lane;
-      int32_t v = 0;
-      if (lane < bpt && (e << lbs) < L) v = __ldg(p.block_table + (long long)seq * p.max_blocks + e);
-      return v;
-    };
-    int g = 0;
+    const bool two_boxes = bs < SLICE;   // block size 16: a slice spans two blocks
+    int g = 0;                           // stages of the CTA so far (both warps count all)
     bool ok = true;
     for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
       const int seq = item / (NHG * P);
@@ -211,48 +213,68 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
       const int L = item_len(item);
       const int nsl = uq_slices(L, part, P);
       if (nsl == 0) continue;
-      int32_t ent = load_entries(seq, part, L);
-      int32_t nent = ((part + P) * TG < L) ? load_entries(seq, part + P, L) : 0;
-      for (int k = 0; k < nsl; ++k) {
-        const int j = k & 7;
-        const int tg = part + P * (k >> 3);
-        if (j == 0 && k > 0) {
-          ent = nent;
-          if ((tg + P) * TG < L) nent = load_entries(seq, tg + P, L);
+      const int32_t* bt = p.block_table + (long long)seq * p.max_blocks;
+      // token-row coordinates of slice k's first box (and second box, block size 16)
+      auto coords = [&](int k, int& za, int& zb) {
+        za = 0;
+        zb = 0;
+        if (k >= nsl) return;
+        const int t0 = (part + P * (k >> 3)) * TG + SLICE * (k & 7);
+        const int ea = t0 >> lbs;
+        int pa = (ea << lbs) < L ? __ldg(bt + ea) : 0;
+        if (pa < 0 || pa >= p.num_blocks) {
+          atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+          pa = 0;
         }
-        const int t0 = tg * TG + SLICE * j;
-        int pa = __shfl_sync(0xffffffffu, ent, (SLICE * j) >> lbs);
-        int pb = __shfl_sync(0xffffffffu, ent, (SLICE * j + 16) >> lbs);
-        if (pa < 0 || pa >= p.num_blocks || pb < 0 || pb >= p.num_blocks) {
-          if (lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
-          pa = (pa < 0 || pa >= p.num_blocks) ? 0 : pa;
-          pb = (pb < 0 || pb >= p.num_blocks) ? 0 : pb;
+        if (!two_boxes) {
+          za = pa * bs + (t0 & (bs - 1));
+        } else {
+          const int eb = (t0 + 16) >> lbs;
+          int pb = (eb << lbs) < L ? __ldg(bt + eb) : 0;
+          if (pb < 0 || pb >= p.num_blocks) {
+            atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+            pb = 0;
+          }
+          za = pa * bs;
+          zb = pb * bs;
         }
-        const int s = g % depth;
-        const uint32_t n = (uint32_t)(g / depth);
-        if (!warp_wait(&empty[s], (n & 1u) ^ 1u, abort_flag, KERR_TIMEOUT_EMPTY)) {
-          ok = false;
-          break;
+      };
+      int za, zb, na, nb;
+      coords(lane, za, zb);
+      coords(32 + lane, na, nb);
+      int chunk = 0;
+      const uint32_t head0 = hgi * p.hg;
+      // this warp's slices: stage g + k with (g + k) % NPW == pw
+      for (int k = (pw - g % NPW + NPW) % NPW; k < nsl; k += NPW) {
+        if ((k >> 5) != chunk) {
+          chunk = k >> 5;
+          za = na;
+          zb = nb;
+          coords(32 * (chunk + 1) + lane, na, nb);
         }
+        const int ya = __shfl_sync(0xffffffffu, za, k & 31);
+        const int yb = __shfl_sync(0xffffffffu, zb, k & 31);
+        const int gs = g + k;
+        const int s = gs % depth;
+        const uint32_t eph = ((uint32_t)(gs / depth) & 1u) ^ 1u;   // a fresh barrier passes parity 1
         if (lane == 0) {
-          // every head's 32 token slots, 272 bytes each, land densely in the
-          // stage; slots past the end of the sequence are read from the blocks
-          // the table names (or block 0) and masked by the consumers
-          mbar_arrive_expect_tx(&full[s], stage_bytes);
-          const uint32_t dst0 = ring + s * stage_bytes;
-          for (int hh = 0; hh < p.hg; ++hh) {
-            const int head = hgi * p.hg + hh;
-            const uint32_t dst = dst0 + hh * HEAD_SLICE;
-            if (bs >= SLICE) {
-              tma_load_3d(dst, &kv_map, 0, head, pa * bs + (t0 & (bs - 1)), &full[s], pol);
-            } else {
-              tma_load_3d(dst, &kv_map, 0, head, pa * bs, &full[s], pol);
-              tma_load_3d(dst + 16 * CONTENT, &kv_map, 0, head, pb * bs, &full[s], pol);
+          if (!mbar_try_wait(&empty[s], eph)) ok = role_wait(&empty[s], eph, abort_flag, KERR_TIMEOUT_EMPTY);
+          if (ok) {
+            // every head's 32 token slots, 272 bytes each, land densely in the
+            // stage; slots past the end of the sequence are read from the blocks
+            // the table names (or block 0) and masked by the consumers
+            mbar_arrive_expect_tx(&full[s], stage_bytes);
+            uint32_t dst = ring + s * stage_bytes;
+            for (int hh = 0; hh < p.hg; ++hh, dst += HEAD_SLICE) {
+              tma_load_3d(dst, &kv_map, 0, head0 + hh, ya, &full[s], pol);
+              if (two_boxes) tma_load_3d(dst + 16 * CONTENT, &kv_map, 0, head0 + hh, yb, &full[s], pol);
             }
           }
         }
-        ++g;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
       }
+      g += nsl;
     }
     // give the copies still in flight a bounded time to land before the CTA's
     // shared memory goes away (they complete whether or not anyone consumes them)
@@ -379,11 +401,17 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
       for (int k = 0; k < 4; ++k) o[i][k] = 0.f;
 
     bool aborted = false;
+    // stage of slice k: (gbase + k) % depth and its phase, kept incrementally
+    // (J < depth)
+    int s = (gbase + jr) % depth;
+    uint32_t fph = (uint32_t)((gbase + jr) / depth) & 1u;
 #pragma unroll 1
     for (int k = jr; k < nsl; k += J) {
-      const int gs = gbase + k;
-      const int s = gs % depth;
-      if (!warp_wait(&full[s], (uint32_t)(gs / depth) & 1u, abort_flag, KERR_TIMEOUT_FULL)) {
+      if (k > jr && (s += J) >= depth) {
+        s -= depth;
+        fph ^= 1u;
+      }
+      if (!warp_wait(&full[s], fph, abort_flag, KERR_TIMEOUT_FULL)) {
         aborted = true;
         break;
       }
@@ -639,31 +667,41 @@ uq_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ pa
   const int sk = row / qg;
   const int seq = sk / num_kv_heads, kvh = sk % num_kv_heads;
   const int tid = threadIdx.x;
-  combine_row<D, kCombineKmax256>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg,
-                                  num_partitions, sw, vec);
-  // the 1/16 of the rotation first: no butterfly sum then exceeds the final
-  // output's bound (16 max |o_r|)
-  for (int i = tid; i < D; i += blockDim.x) vec[i] *= 0.0625f;
-  __syncthreads();
-  const int pa = tid, pb = tid + blockDim.x;      // this thread's pairs (pb only when blockDim is 64)
-  for (int st = 1; st < D; st <<= 1) {
-    const int ia = ((pa & ~(st - 1)) << 1) | (pa & (st - 1));   // index with bit `st` clear
-    const int ib = ((pb & ~(st - 1)) << 1) | (pb & (st - 1));
-    float xa = 0.f, ya = 0.f, xb = 0.f, yb = 0.f;
-    if (pa < D / 2) { xa = vec[ia]; ya = vec[ia + st]; }
-    if (pb < D / 2) { xb = vec[ib]; yb = vec[ib + st]; }
-    __syncthreads();
-    if (pa < D / 2) { vec[ia] = xa + ya; vec[ia + st] = xa - ya; }
-    if (pb < D / 2) { vec[ib] = xb + yb; vec[ib + st] = xb - yb; }
-    __syncthreads();
+  combine_row<D, kCombineKmax256, true>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg,
+                                        num_partitions, sw, vec);
+  // o = o_r H / 16 by one warp: lane l holds dims 8l .. 8l + 7, the butterflies
+  // of index bits 0..2 in registers and of bits 3..7 across lanes, in stride
+  // order 1, 2, ..., 128; the 1/16 first, so that no butterfly sum exceeds the
+  // final output's bound (16 max |o_r|)
+  if (tid >= 32) return;
+  float x[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) x[j] = vec[8 * tid + j] * 0.0625f;
+#pragma unroll
+  for (int st = 1; st < 8; st <<= 1)
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (!(j & st)) {
+        const float a = x[j], b = x[j + st];
+        x[j] = a + b;
+        x[j + st] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool hi = (tid & m) != 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float other = __shfl_xor_sync(0xffffffffu, x[j], m);
+      x[j] = hi ? other - x[j] : x[j] + other;
+    }
   }
-  if (tid < D / 4) {
-    // with the column-permuted rotation M, out[i] = (o_r H / 16)[perm(i)]
-    // (perm keeps bits 0..3, so four consecutive dims stay together)
-    const int src = rot_perm ? rot_perm_dest(4 * tid) : 4 * tid;
-    OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + 4 * tid;
-    store4(dst, vec[src], vec[src + 1], vec[src + 2], vec[src + 3]);
-  }
+  // with the column-permuted rotation M, out[i] = (o_r H / 16)[perm(i)]; perm
+  // keeps bits 0..3, so this lane's 8 dims are the outputs from
+  // rot_perm_source(8 l) on
+  const int dst0 = rot_perm ? rot_perm_source(8 * tid) : 8 * tid;
+  OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + dst0;
+  store4(dst, x[0], x[1], x[2], x[3]);
+  store4(dst + 4, x[4], x[5], x[6], x[7]);
 }
 
 // ------------------------------------------------------------------ host side
