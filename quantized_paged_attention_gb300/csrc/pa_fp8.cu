@@ -280,10 +280,15 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       if (lane == 0) mbar_arrive(&qempty[qb]);
       const int item = inf.x, L = inf.y, nt = inf.z, tg0 = inf.w;   // tiles of tile groups tg0, tg0 + 1, ...
       if (nt == 0) break;
+      // EXT: row qoff * qg + g sees the tokens below L - QL + 1 + qoff; the
+      // bound per row, computed once per item (the division by qg is not in
+      // the tile loop)
+      int vis[RG];
 #pragma unroll
       for (int r = 0; r < RG; ++r) {
         m[r] = -INFINITY;
         l[r] = 0.f;
+        vis[r] = EXT ? L - QL + 1 + (rbase + RG * rblk + r) / p.qg : L;
       }
       for (int i = 0; i < nt; ++i, ++j) {
         if (!RS && (j & 1) != wg) continue;
@@ -312,9 +317,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           }
 #pragma unroll
           for (int r = 0; r < RG; ++r) {
-            // row qoff * qg + g sees the tokens below L - QL + 1 + qoff
             const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
-            x[r] = (start + t < L - QL + 1 + (rbase + RG * rblk + r) / p.qg) ? sv * c[r] * ks_t : -INFINITY;
+            x[r] = start + t < vis[r] ? sv * c[r] * ks_t : -INFINITY;
           }
         } else {
 #pragma unroll
