@@ -26,22 +26,26 @@ inline int combine_threads(int d, int kmax, int num_partitions) {
   int nsub = (num_partitions + kmax - 1) / kmax;
   if (nsub < 1) nsub = 1;
   if (nsub > kCombineMaxThreads / nvec) nsub = kCombineMaxThreads / nvec;
+  while ((nvec * nsub) % 32) ++nsub;   // whole warps: the reductions shuffle over 32 lanes
   return nvec * nsub;
 }
 
-// Returns in vec[0..D) (shared memory) the combined row. `sw` is dynamic
-// shared scratch of combine_smem_bytes(P, threads) bytes (16-byte aligned).
+// Returns in vec[0..D) (shared memory) the combined row. `sw` is shared
+// scratch of combine_smem_bytes(P, nthr) bytes (16-byte aligned). The row is
+// combined by the nthr threads tid = 0 .. nthr - 1 of a group (a whole warp
+// or more); every group of the CTA calls this together (it holds CTA-wide
+// barriers), each with its own row, scratch and vec.
 // EAGER: the first round of O loads is issued together with the (m, l) loads
 // instead of after the weights are known (one round trip instead of two, for
 // rows whose slots are all written); an O of weight 0 is never used.
 template <int D, int KMAX, bool EAGER = false>
 __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, const float* __restrict__ part_m,
                                             const float* __restrict__ part_l, long long rbase, int qg,
-                                            int num_partitions, float* sw, float* vec) {
+                                            int num_partitions, float* sw, float* vec, int tid, int nthr) {
   constexpr int NVEC = D / 4;                  // float4 per row
-  const int nsub = blockDim.x / NVEC;          // partition subsets
+  const int nsub = nthr / NVEC;                // partition subsets
   const int P = num_partitions;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int lane = tid & 31;
   const int v4 = tid % NVEC, sub = tid / NVEC;
   float* ms = sw;
   float* ls = sw + P;
@@ -57,7 +61,7 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
       o0[k] = pp < P ? __ldg(reinterpret_cast<const float4*>(ob + pp * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  for (int pp = tid; pp < P; pp += blockDim.x) {
+  for (int pp = tid; pp < P; pp += nthr) {
     ms[pp] = part_m[rbase + (long long)pp * qg];
     ls[pp] = part_l[rbase + (long long)pp * qg];
   }
@@ -118,8 +122,18 @@ __device__ __forceinline__ void combine_row(const float* __restrict__ part_o, co
   __syncthreads();
 }
 
-inline size_t combine_smem_bytes(int num_partitions, int threads) {
+__host__ __device__ inline size_t combine_smem_bytes(int num_partitions, int threads) {
   return (size_t((2 * num_partitions + 3) & ~3) + 4 * size_t(threads)) * sizeof(float);
+}
+
+// Rows per CTA of a multi-row combine: the largest divisor of the rows of a
+// (sequence, KV head) whose thread groups fit kCombineMaxThreads, so that a
+// CTA never holds a partial group.
+inline int combine_rows_per_cta(int rows, int threads) {
+  int best = 1;
+  for (int k = 1; k <= rows; ++k)
+    if (rows % k == 0 && k * threads <= kCombineMaxThreads) best = k;
+  return best;
 }
 
 }  // namespace qpa

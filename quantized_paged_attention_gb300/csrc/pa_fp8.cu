@@ -203,7 +203,6 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_launch_dependents();   // the combine kernel waits for this grid before reading
 
   const int P = p.num_partitions;
   const int Hk = p.num_kv_heads;
@@ -906,26 +905,29 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   }
 }
 
-// Flash-combine of the partitions ([PA] reduce kernel): one CTA per query
-// row (seq, kv_head, r), see combine_row.
+// Flash-combine of the partitions ([PA] reduce kernel), see combine_row: a
+// CTA holds rows_per_cta consecutive query rows (seq, kv_head, r), one thread
+// group of threads_per_row each, so that a launch is a few hundred CTAs.
 template <typename OutT, int HD>
 __global__ void __launch_bounds__(kCombineMaxThreads)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
                const float* __restrict__ part_l, OutT* __restrict__ out, int num_kv_heads, int qg,
-               int num_partitions, long long out_stride_seq, long long out_stride_head) {
+               int num_partitions, long long out_stride_seq, long long out_stride_head, int rows_per_cta,
+               int threads_per_row) {
   extern __shared__ __align__(16) float sw[];
-  __shared__ __align__(16) float vec[HD];
-  pdl_wait_primary();
-  const int row = blockIdx.x;                 // ((seq * Hk) + kvh) * qg + r
+  const int grp = threadIdx.x / threads_per_row, tid = threadIdx.x - grp * threads_per_row;
+  const int row = blockIdx.x * rows_per_cta + grp;   // ((seq * Hk) + kvh) * qg + r
   const int r = row % qg;
   const int sk = row / qg;                    // seq * Hk + kvh
   const int seq = sk / num_kv_heads, kvh = sk % num_kv_heads;
+  const int gfl = (int)(combine_smem_bytes(num_partitions, threads_per_row) / sizeof(float)) + HD;
+  float* my = sw + grp * gfl;
+  float* vec = my + gfl - HD;
   combine_row<HD, kCombineKmax128>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg,
-                                   num_partitions, sw, vec);
-  if (threadIdx.x < HD / 4) {
-    const int t = threadIdx.x;
-    OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + 4 * t;
-    store4(dst, vec[4 * t], vec[4 * t + 1], vec[4 * t + 2], vec[4 * t + 3]);
+                                   num_partitions, my, vec, tid, threads_per_row);
+  if (tid < HD / 4) {
+    OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + 4 * tid;
+    store4(dst, vec[4 * tid], vec[4 * tid + 1], vec[4 * tid + 2], vec[4 * tid + 3]);
   }
 }
 
@@ -1029,23 +1031,21 @@ cudaError_t launch_fp8x_partition(const Fp8ExtLaunch& a, cudaStream_t stream) {
 
 template <typename OutT, int HD>
 static cudaError_t launch_combine_t(const CombineLaunch& a, OutT* out, cudaStream_t stream) {
-  const int grid = a.num_seqs * a.num_kv_heads * a.qg;
   const int threads = combine_threads(HD, kCombineKmax128, a.num_partitions);
-  const size_t smem = combine_smem_bytes(a.num_partitions, threads);
+  const int rpc = combine_rows_per_cta(a.qg, threads);
+  const int grid = a.num_seqs * a.num_kv_heads * (a.qg / rpc);
+  const size_t smem = size_t(rpc) * (combine_smem_bytes(a.num_partitions, threads) + HD * sizeof(float));
   if (smem > 40 * 1024)
     cudaFuncSetAttribute(combine_kernel<OutT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
+  cfg.blockDim = dim3(threads * rpc);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // plain stream order: launched as a programmatic dependent of the partition
+  // grid (its CTAs cannot sit beside the partition CTAs) the step took ~5 us more
   return cudaLaunchKernelEx(&cfg, combine_kernel<OutT, HD>, a.part_o, a.part_m, a.part_l, out, a.num_kv_heads,
-                            a.qg, a.num_partitions, a.out_stride_seq, a.out_stride_head);
+                            a.qg, a.num_partitions, a.out_stride_seq, a.out_stride_head, rpc, threads);
 }
 
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t stream) {

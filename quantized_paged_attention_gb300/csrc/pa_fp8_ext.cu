@@ -15,29 +15,31 @@
 
 namespace qpa {
 
-// Flash-combine of the partitions ([PA] reduce) of one query row (sequence,
-// KV head, query position, group row), see combine_row.
+// Flash-combine of the partitions ([PA] reduce) of the query rows (sequence,
+// KV head, query position, group row), see combine_row: rows_per_cta
+// consecutive rows per CTA, one thread group of threads_per_row each.
 template <typename OutT, int HD>
 __global__ void __launch_bounds__(kCombineMaxThreads)
 combine_ext_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
                    const float* __restrict__ part_l, OutT* __restrict__ out, int num_kv_heads, int qg,
                    int query_len, int num_partitions, long long out_stride_seq, long long out_stride_tok,
-                   long long out_stride_head) {
+                   long long out_stride_head, int rows_per_cta, int threads_per_row) {
   extern __shared__ __align__(16) float sw[];
-  __shared__ __align__(16) float vec[HD];
-  pdl_wait_primary();
   const int rows = query_len * qg;
-  const int row = blockIdx.x;                 // ((seq * Hk) + kvh) * rows + r
+  const int grp = threadIdx.x / threads_per_row, tid = threadIdx.x - grp * threads_per_row;
+  const int row = blockIdx.x * rows_per_cta + grp;   // ((seq * Hk) + kvh) * rows + r
   const int r = row % rows;
   const int sk = row / rows;                  // seq * Hk + kvh
   const int seq = sk / num_kv_heads, kvh = sk % num_kv_heads;
   const int qoff = r / qg, gq = r % qg;
+  const int gfl = (int)(combine_smem_bytes(num_partitions, threads_per_row) / sizeof(float)) + HD;
+  float* my = sw + grp * gfl;
+  float* vec = my + gfl - HD;
   combine_row<HD, kCombineKmax128>(part_o, part_m, part_l, (long long)sk * num_partitions * rows + r, rows,
-                                   num_partitions, sw, vec);
-  if (threadIdx.x < HD / 4) {
-    const int t = threadIdx.x;
-    OutT* dst = out + seq * out_stride_seq + qoff * out_stride_tok + (long long)(kvh * qg + gq) * out_stride_head + 4 * t;
-    store4(dst, vec[4 * t], vec[4 * t + 1], vec[4 * t + 2], vec[4 * t + 3]);
+                                   num_partitions, my, vec, tid, threads_per_row);
+  if (tid < HD / 4) {
+    OutT* dst = out + seq * out_stride_seq + qoff * out_stride_tok + (long long)(kvh * qg + gq) * out_stride_head + 4 * tid;
+    store4(dst, vec[4 * tid], vec[4 * tid + 1], vec[4 * tid + 2], vec[4 * tid + 3]);
   }
 }
 
@@ -45,24 +47,22 @@ combine_ext_kernel(const float* __restrict__ part_o, const float* __restrict__ p
 template <typename OutT, int HD>
 static cudaError_t launch_fp8x_combine_t(const Fp8ExtCombineLaunch& a, OutT* out, cudaStream_t stream) {
   const int rows = a.query_len * a.qg;
-  const int grid = a.num_seqs * a.num_kv_heads * rows;
   const int threads = combine_threads(HD, kCombineKmax128, a.num_partitions);
-  const size_t smem = combine_smem_bytes(a.num_partitions, threads);
+  const int rpc = combine_rows_per_cta(rows, threads);
+  const int grid = a.num_seqs * a.num_kv_heads * (rows / rpc);
+  const size_t smem = size_t(rpc) * (combine_smem_bytes(a.num_partitions, threads) + HD * sizeof(float));
   if (smem > 40 * 1024)
     cudaFuncSetAttribute(combine_ext_kernel<OutT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
+  cfg.blockDim = dim3(threads * rpc);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // plain stream order: launched as a programmatic dependent of the partition
+  // grid (its CTAs cannot sit beside the partition CTAs) the step took ~5 us more
   return cudaLaunchKernelEx(&cfg, combine_ext_kernel<OutT, HD>, a.part_o, a.part_m, a.part_l, out, a.num_kv_heads,
                             a.qg, a.query_len, a.num_partitions, a.out_stride_seq, a.out_stride_tok,
-                            a.out_stride_head);
+                            a.out_stride_head, rpc, threads);
 }
 
 cudaError_t launch_fp8x_combine(const Fp8ExtCombineLaunch& a, cudaStream_t stream) {

@@ -180,7 +180,6 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
     }
   }
   __syncthreads();
-  pdl_launch_dependents();
 
   const int P = p.num_partitions;
   const int NHG = p.num_kv_heads / p.hg;
@@ -661,14 +660,13 @@ uq_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ pa
   constexpr int D = 256;
   extern __shared__ __align__(16) float sw[];
   __shared__ __align__(16) float vec[D];
-  pdl_wait_primary();
   const int row = blockIdx.x;
   const int r = row % qg;
   const int sk = row / qg;
   const int seq = sk / num_kv_heads, kvh = sk % num_kv_heads;
   const int tid = threadIdx.x;
   combine_row<D, kCombineKmax256, true>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg,
-                                        num_partitions, sw, vec);
+                                        num_partitions, sw, vec, threadIdx.x, blockDim.x);
   // o = o_r H / 16 by one warp: lane l holds dims 8l .. 8l + 7, the butterflies
   // of index bits 0..2 in registers and of bits 3..7 across lanes, in stride
   // order 1, 2, ..., 128; the 1/16 first, so that no butterfly sum exceeds the
@@ -808,11 +806,8 @@ static cudaError_t launch_uq_combine_t(const CombineLaunch& a, OutT* out, cudaSt
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // plain stream order: launched as a programmatic dependent of the partition
+  // grid (its CTAs cannot sit beside the partition CTAs) the step took ~5 us more
   return cudaLaunchKernelEx(&cfg, uq_combine_kernel<OutT>, a.part_o, a.part_m, a.part_l, out, a.num_kv_heads,
                             a.qg, a.num_partitions, a.out_stride_seq, a.out_stride_head, a.rot_perm);
 }
