@@ -108,7 +108,10 @@ int qpa_kernel_error(void* stream);
  * Supported: head_dim 64 or 128 ([PA]), query_group 1..64 (the page's wide
  * GQA; above 16 the kernel runs blocks of 16 query rows of a KV head as
  * separate work streams over the same pages), block_size 16/32/64/128/256.
- * Layouts above with head_dim in place of 128.
+ * Layouts above with head_dim in place of 128, except the workspace's O for
+ * head_dim 64 with query_group <= 8: its rows keep 128 floats, two 64-dim
+ * halves (the kernel takes a 256-token tile group per pass as two halves of
+ * 128 tokens) that the combine adds.
  * Alignment: q, kv_cache and out 16-byte aligned.
  * ====================================================================== */
 typedef struct qpa_fp8_desc {

@@ -43,11 +43,18 @@ bool fp8_shape_ok(const qpa_fp8_desc* d) {
   return true;
 }
 
-Fp8Layout fp8_layout(const qpa_fp8_desc* d, int P) {
+// Floats per partial O row: head_dim 64 with up to 8 query rows runs the
+// packed two-half kernel, whose partials keep both 64-dim halves (the combine
+// adds them).
+int fp8_part_dim(const qpa_fp8_desc* d, bool ext) {
+  return (!ext && d->head_dim == 64 && d->query_group <= 8) ? 128 : d->head_dim;
+}
+
+Fp8Layout fp8_layout(const qpa_fp8_desc* d, int P, bool ext = false) {
   const size_t rows = size_t(d->num_seqs) * d->num_kv_heads * P * d->query_group;
   Fp8Layout L;
   L.o_off = 0;
-  L.m_off = round_up(L.o_off + rows * d->head_dim * sizeof(float), 256);
+  L.m_off = round_up(L.o_off + rows * fp8_part_dim(d, ext) * sizeof(float), 256);
   L.l_off = round_up(L.m_off + rows * sizeof(float), 256);
   L.total = round_up(L.l_off + rows * sizeof(float), 256);
   return L;
@@ -83,7 +90,7 @@ bool fp8x_shape_ok(const qpa_fp8_ext_desc* d) {
 Fp8Layout fp8x_layout(const qpa_fp8_ext_desc* d, int P) {
   qpa_fp8_desc rows = d->base;
   rows.query_group = d->base.query_group * fp8x_query_len(d);   // partial rows per (seq, head, partition)
-  return fp8_layout(&rows, P);
+  return fp8_layout(&rows, P, true);
 }
 
 // ------------------------------------------------------------------ uq hd256
@@ -242,6 +249,7 @@ int pa_decode_fp8_combine(int num_partitions, void* out, const qpa_fp8_desc* d, 
   c.qg = d->query_group;
   c.num_partitions = num_partitions;
   c.d = d->head_dim;
+  c.part_d = fp8_part_dim(d, false);
   c.out_stride_head = d->head_dim;
   c.out_stride_seq = (long long)d->num_kv_heads * d->query_group * d->head_dim;
   return launch_combine(c, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPA_OK : QPA_ERR_CUDA;

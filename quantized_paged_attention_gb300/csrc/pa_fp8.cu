@@ -58,17 +58,23 @@ constexpr int TILE = 128;       // tokens per MMA tile
 constexpr int TILE_BYTES = 2 * TILE * D;   // K tile then V tile
 constexpr int V_OFF = TILE * D;
 
-template <int NT, bool EXT = false>
+// PK (head_dim 64, up to 8 query rows, one token per row): a ring slot holds a
+// whole 256-token tile group, its first 128 tokens in bytes 0..63 of the
+// 128-byte rows and the next 128 in bytes 64..127 ("halves" A and B); the MMA
+// N doubles (Q' and P' carry each row once per half) so that one QK and one
+// PV issue cover both halves and the softmax takes 256 tokens per pass.
+template <int NT, bool EXT = false, bool PK = false>
 struct Smem {
   static constexpr int NWG = 2;                    // softmax warp groups
   static constexpr int WARP_PROD0 = 4 * NWG;       // 4 copy warps
   static constexpr int WARP_MMA = WARP_PROD0 + 4;  // QK issuing warp, then the PV issuing warp
   static constexpr int THREADS = (WARP_MMA + 2) * 32;
-  static constexpr int NS = 5;                     // ring slots (tiles)
+  static constexpr int NS = PK ? 4 : 5;            // ring slots (tiles, PK: tile groups)
   static constexpr int R = 8 * NT;                 // query rows (padded)
-  static constexpr int NQ = 32 * NT;               // MMA N: 4 term slots x R rows
-  static constexpr int qBytes = NQ * D;            // Q' [NQ rows][128 dims] e4m3
-  static constexpr int pBytes = TILE * NQ;         // P'^T [128 tokens][NQ] e4m3
+  static constexpr int NQ = 32 * NT;               // 4 term slots x R rows
+  static constexpr int NQS = PK ? 2 * NQ : NQ;     // MMA N: NQ per half
+  static constexpr int qBytes = NQS * D;           // Q' [NQS rows][128 dims] e4m3
+  static constexpr int pBytes = TILE * NQS;        // P'^T [128 tokens][NQS] e4m3
   static constexpr int ringOff = 0;
   static constexpr int qOff = NS * TILE_BYTES;
   static constexpr int pOff = qOff + 2 * qBytes;
@@ -84,7 +90,7 @@ struct Smem {
   static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag, QK total
   static constexpr int total = miscOff + 16 + 1024;        // + alignment slack
   static_assert(total <= 227 * 1024, "shared memory");
-  static constexpr int TMEM_COLS = NT == 1 ? 256 : 512;   // S[2] then O[4] (6 NQ columns)
+  static constexpr int TMEM_COLS = (NT == 1 && !PK) ? 256 : 512;   // S[2] then O[4] (6 NQS columns)
 };
 }  // namespace fp8
 
@@ -124,11 +130,13 @@ template <int NT, int HD, bool EXT>
 __global__ void __launch_bounds__(fp8::Smem<NT>::THREADS, 1)
 pa_fp8_partition_kernel(const Fp8Params p) {
   using namespace fp8;
-  using S = Smem<NT, EXT>;
-  constexpr int R = S::R, NQ = S::NQ, NWG = S::NWG;
+  constexpr bool PK = HD == 64 && NT == 1 && !EXT;   // two 128-token halves per ring slot
+  using S = Smem<NT, EXT, PK>;
+  constexpr int R = S::R, NQ = S::NQ, NQS = S::NQS, NWG = S::NWG;
+  constexpr int PD = PK ? 2 * HD : HD;                // floats per partial O row
   constexpr int WARP_PROD0 = S::WARP_PROD0, WARP_MMA = S::WARP_MMA;
-  constexpr uint32_t IDESC_QK = idesc_e4m3(128, NQ, false, false);
-  constexpr uint32_t IDESC_PV = idesc_e4m3(128, NQ, true, true);
+  constexpr uint32_t IDESC_QK = idesc_e4m3(128, NQS, false, false);
+  constexpr uint32_t IDESC_PV = idesc_e4m3(128, NQS, true, true);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;     // swizzle atoms need 1024-byte alignment
@@ -233,7 +241,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     const float vscale = per_token ? 1.f : __ldg(p.v_scale);
     const int rblk = RS ? wg : 0;                      // this group's row block
     // this token's P' row, the group's 32 columns
-    const uint32_t ptok = psm + (t >> 3) * (8 * NQ) + (t & 7) * 16 + 256 * rblk;
+    // (PK: the B half's 32 columns follow at + 256)
+    const uint32_t ptok = psm + (t >> 3) * (8 * NQS) + (t & 7) * 16 + 256 * rblk;
     float m[RG], l[RG], o[RG], c[RG];
 #pragma unroll
     for (int r = 0; r < RG; ++r) { o[r] = 0.f; m[r] = -INFINITY; l[r] = 0.f; c[r] = 0.f; }
@@ -249,7 +258,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       if (!warp_wait(&ofull[ob], (pend_j >> 2) & 1, abort_flag, KERR_TIMEOUT_FULL)) return false;
       tc_fence_after();
       float w[32];
-      tmem_ld32(tl + 2 * NQ + ob * NQ + 32 * rblk, w);
+      // (PK: lanes 64..127, the B half's dims, read the B columns)
+      tmem_ld32(tl + 2 * NQS + ob * NQS + 32 * rblk + (PK && wq >= 2 ? NQ : 0), w);
       tmem_wait_ld();
       tc_fence_before();
 #pragma unroll
@@ -291,14 +301,16 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       }
       for (int i = 0; i < nt; ++i, ++j) {
         if (!RS && (j & 1) != wg) continue;
-        const int start = (tg0 + (i >> 1)) * TG + (i & 1) * TILE;
+        const int start = PK ? (tg0 + i) * TG : (tg0 + (i >> 1)) * TG + (i & 1) * TILE;
         const int b = j & 1;                 // S buffer
         const int ob = 2 * b + ((j >> 1) & 1);   // P' and O buffer (alternate per group)
         // ---- softmax of tile j
         if (!warp_wait(&sfull[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
         tc_fence_after();
         float v[32];
-        tmem_ld32(tl + b * NQ + 32 * rblk, v);
+        float vB[PK ? 32 : 1];               // PK: the B half's scores (token start + TILE + t)
+        tmem_ld32(tl + b * NQS + 32 * rblk, v);
+        if constexpr (PK) tmem_ld32(tl + b * NQS + NQ, vB);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -326,11 +338,20 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             x[r] = valid ? sv * c[r] : -INFINITY;
           }
         }
+        float xB[PK ? RG : 1];
+        if constexpr (PK) {
+          const bool validB = start + TILE + t < L;
+#pragma unroll
+          for (int r = 0; r < RG; ++r) {
+            const float sv = fmaf(fmaf(fmaf(vB[3 * RG + r], 0.0625f, vB[2 * RG + r]), 0.0625f, vB[RG + r]), 0.0625f, vB[r]);
+            xB[r] = validB ? sv * c[r] : -INFINITY;
+          }
+        }
         {
           // row maxima over the warp's 32 tokens (hardware warp reduction)
           float mx[RG];
 #pragma unroll
-          for (int r = 0; r < RG; ++r) mx[r] = warp_max(x[r]);
+          for (int r = 0; r < RG; ++r) mx[r] = warp_max(PK ? fmaxf(x[r], xB[r]) : x[r]);
           if (lane == 0) {
 #pragma unroll
             for (int q4 = 0; q4 < RG / 4; ++q4)
@@ -399,6 +420,36 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(tw[0][0]), "r"(tw[0][1]),
                        "r"(tw[1][0]), "r"(tw[1][1]) : "memory");
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(tw[2][0]), "r"(tw[2][1]),
+                       "r"(0u), "r"(0u) : "memory");
+        }
+        if constexpr (PK) {
+          // the B half: the same for token start + TILE + t, its columns after A's
+          uint32_t twB[3][RG / 4];
+#pragma unroll
+          for (int k = 0; k < RG / 2; ++k) {
+            const uint32_t p16 = f32x2_to_f16x2(ex2(xB[2 * k] - m[2 * k]), ex2(xB[2 * k + 1] - m[2 * k + 1]));
+            l[2 * k] += f16_lo_to_f32(p16);
+            l[2 * k + 1] += f16_hi_to_f32(p16);
+            uint32_t h = hmul2(p16, 0x5C005C00u);
+            const uint32_t e0 = f16x2_to_e4m3x2(h);
+            h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e0)), 0x4C004C00u);
+            const uint32_t e1 = f16x2_to_e4m3x2(h);
+            h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e1)), 0x4C004C00u);
+            const uint32_t e2 = f16x2_to_e4m3x2(h);
+            if (k & 1) {
+              twB[0][k >> 1] |= e0 << 16;
+              twB[1][k >> 1] |= e1 << 16;
+              twB[2][k >> 1] |= e2 << 16;
+            } else {
+              twB[0][k >> 1] = e0;
+              twB[1][k >> 1] = e1;
+              twB[2][k >> 1] = e2;
+            }
+          }
+          const uint32_t pb = ptok + ob * S::pBytes + 256;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(twB[0][0]), "r"(twB[0][1]),
+                       "r"(twB[1][0]), "r"(twB[1][1]) : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(twB[2][0]), "r"(twB[2][1]),
                        "r"(0u), "r"(0u) : "memory");
         }
         fence_proxy_async();
@@ -486,8 +537,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           // (lt >= 1: the row maximum's own term is exactly 1; EXT: lt = 0 for a
           // row that saw no token)
           const int row = RG * rblk + r;
-          if (row < rows_here && t < HD)
-            p.part_o[(row0 + row) * HD + t] = (EXT && lt == 0.f) ? 0.f : ot * (vscale * rcp_approx(lt));
+          if (row < rows_here && t < PD)
+            p.part_o[(row0 + row) * PD + t] = (EXT && lt == 0.f) ? 0.f : ot * (vscale * rcp_approx(lt));
           if (t == r) {
             lt_mine = lt;
             mt_mine = mt;
@@ -516,6 +567,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     const int lr = lane / CPR, cc = lane % CPR;
     const uint32_t doff_e = (uint32_t)((32 * pw + lr) * D + ((cc ^ (lr & 7)) << 4));
     const uint32_t doff_o = (uint32_t)((32 * pw + lr) * D + ((cc ^ ((lr + 4) & 7)) << 4));
+    // PK: the B half's chunks 4 .. 7 of the same rows
+    const uint32_t doffB_e = (uint32_t)((32 * pw + lr) * D + (((cc + 4) ^ (lr & 7)) << 4));
+    const uint32_t doffB_o = (uint32_t)((32 * pw + lr) * D + (((cc + 4) ^ ((lr + 4) & 7)) << 4));
     const size_t head_bytes = size_t(bs) * HD;
     const size_t v_off = size_t(Hk) * head_bytes;
     const size_t blk_bytes = 2 * v_off;
@@ -656,7 +710,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       const int L = cur.L;
       const int kvh = cur.h / RB;              // the KV head of the virtual head
       const int rblock = cur.h % RB;
-      const int nt = 2 * (tg_e - tg_b) - (((tg_e - 1) * TG + TILE < L) ? 0 : 1);
+      // ring slots of the item: 128-token tiles (the last one dropped when the
+      // tile group ends before it), PK: whole tile groups
+      const int nt = PK ? tg_e - tg_b : 2 * (tg_e - tg_b) - (((tg_e - 1) * TG + TILE < L) ? 0 : 1);
       const int item = (cur.s * Hk + kvh) * P + slot;
       // next item's query rows and first table entries
       const Cur nxt = walk(cur.s + 1, cur.off + T, cur.h);
@@ -722,6 +778,13 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             if (h16 < HD / 8)
               asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(e[0] | (e[1] << 16)),
                            "r"(e[2] | (e[3] << 16)) : "memory");
+            if (PK && h16 < HD / 8) {
+              // the B half's copy of the row: rows NQ.. , dims in bytes 64..127
+              const uint32_t addrB = qsm + qb * S::qBytes + (rr + NQ) * D + ((((h16 >> 1) + 4) ^ (rr & 7)) << 4) +
+                                     8 * (h16 & 1);
+              asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addrB), "r"(e[0] | (e[1] << 16)),
+                           "r"(e[2] | (e[3] << 16)) : "memory");
+            }
           }
           if (h16 == 0) stsf(cbuf_s + 4 * (qb * R + row), 16 * rblock + row < rows ? base_scale * down : 0.f);
         }
@@ -738,10 +801,10 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         const size_t kvh_off = size_t(kvh) * head_bytes;
         int32_t ent = ent0, nent = 0;
         for (int i = 0; i < nt; ++i) {
-          const int tg = tg_b + (i >> 1);
-          if ((i & 1) == 0) {
+          const int tg = tg_b + (PK ? i : (i >> 1));
+          if (PK || (i & 1) == 0) {
             if (i > 0) ent = nent;
-            nent = (i + 2 < nt) ? load_entries(cur.s, tg + 1) : 0;
+            nent = (i + (PK ? 1 : 2) < nt) ? load_entries(cur.s, tg + 1) : 0;
           }
           const int s = j % NS;
           const int rnd = j / NS;
@@ -749,7 +812,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             ok = false;
             break;
           }
-          const int tok0 = tg * TG + (i & 1) * TILE + 32 * pw;
+          const int tok0 = tg * TG + (PK ? 0 : (i & 1)) * TILE + 32 * pw;
           int pa = __shfl_sync(0xffffffffu, ent, (tok0 & (TG - 1)) >> lbs);
           int pb = __shfl_sync(0xffffffffu, ent, ((tok0 + 16) & (TG - 1)) >> lbs);
           if (pa < 0 || pa >= p.num_blocks) {
@@ -772,6 +835,30 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             const uint32_t dst = slot + (((RPI * ii) & 4) ? doff_o : doff_e) + RPI * D * ii;
             cp_async16_zfill(dst, src, valid, pol);
             cp_async16_zfill(dst + V_OFF, src + v_off, valid, pol);
+          }
+          if constexpr (PK) {
+            // the B half: tokens tok0 + TILE .., into chunks 4 .. 7 of the same rows
+            const int tokB = tok0 + TILE;
+            int qa = __shfl_sync(0xffffffffu, ent, (tokB & (TG - 1)) >> lbs);
+            int qb2 = __shfl_sync(0xffffffffu, ent, ((tokB + 16) & (TG - 1)) >> lbs);
+            if (qa < 0 || qa >= p.num_blocks) {
+              if (tokB < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+              qa = 0;
+            }
+            if (qb2 < 0 || qb2 >= p.num_blocks) {
+              if (tokB + 16 < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+              qb2 = 0;
+            }
+            const uint8_t* kaB = p.kv + size_t(qa) * blk_bytes + kvh_off + size_t(tokB & (bs - 1)) * HD + lr * HD + cc * 16;
+            const uint8_t* kbB = bs == 16 ? p.kv + size_t(qb2) * blk_bytes + kvh_off + lr * HD + cc * 16 : kaB + 16 * HD;
+#pragma unroll
+            for (int ii = 0; ii < NII; ++ii) {
+              const bool valid = tokB + lr + RPI * ii < L;
+              const uint8_t* src = ii < NII / 2 ? kaB + RPI * HD * ii : kbB + RPI * HD * (ii - NII / 2);
+              const uint32_t dst = slot + (((RPI * ii) & 4) ? doffB_o : doffB_e) + RPI * D * ii;
+              cp_async16_zfill(dst, src, valid, pol);
+              cp_async16_zfill(dst + V_OFF, src + v_off, valid, pol);
+            }
           }
           if (per_token && lane < 16) {
             // this warp's 32 tokens' K (lanes 0..7) or V (8..15) scales, 4 tokens
@@ -829,8 +916,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           tc_fence_after();
           const uint32_t ka = ring + s * TILE_BYTES;
 #pragma unroll
-          for (int k = 0; k < HD / 32; ++k)
-            mma_e4m3(tmem + b * NQ, umma_desc(ka + 32 * k, 16, 1024, kSwizzle128B),
+          for (int k = 0; k < (PK ? 4 : HD / 32); ++k)
+            mma_e4m3(tmem + b * NQS, umma_desc(ka + 32 * k, 16, 1024, kSwizzle128B),
                      umma_desc(qa + 32 * k, 16, 1024, kSwizzle128B), IDESC_QK, k);
           umma_commit(&sfull[b]);
           if (i == nt - 1) umma_commit(&qempty[qb]);
@@ -873,8 +960,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             const uint32_t pa = psm + ob * S::pBytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_e4m3(tmem + 2 * NQ + ob * NQ, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
-                       umma_desc(pa + k * 32 * NQ, 8 * NQ, 128, kSwizzleNone), IDESC_PV, k);
+              mma_e4m3(tmem + 2 * NQS + ob * NQS, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
+                       umma_desc(pa + k * 32 * NQS, 8 * NQS, 128, kSwizzleNone), IDESC_PV, k);
             umma_commit(&ofull[ob]);
             umma_commit(&empty[jj % NS]);
             pv_n[b] += 2;
@@ -908,7 +995,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 // Flash-combine of the partitions ([PA] reduce kernel), see combine_row: a
 // CTA holds rows_per_cta consecutive query rows (seq, kv_head, r), one thread
 // group of threads_per_row each, so that a launch is a few hundred CTAs.
-template <typename OutT, int HD>
+// HALVES: the partial rows hold two halves of the output's HD / 2 dims (the
+// packed head_dim 64 kernel), added after the combine.
+template <typename OutT, int HD, bool HALVES = false>
 __global__ void __launch_bounds__(kCombineMaxThreads)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
                const float* __restrict__ part_l, OutT* __restrict__ out, int num_kv_heads, int qg,
@@ -925,9 +1014,14 @@ combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_
   float* vec = my + gfl - HD;
   combine_row<HD, kCombineKmax128>(part_o, part_m, part_l, (long long)sk * num_partitions * qg + r, qg,
                                    num_partitions, my, vec, tid, threads_per_row);
-  if (tid < HD / 4) {
+  constexpr int DO = HALVES ? HD / 2 : HD;     // output dims
+  if (tid < DO / 4) {
     OutT* dst = out + seq * out_stride_seq + (long long)(kvh * qg + r) * out_stride_head + 4 * tid;
-    store4(dst, vec[4 * tid], vec[4 * tid + 1], vec[4 * tid + 2], vec[4 * tid + 3]);
+    if constexpr (HALVES)
+      store4(dst, vec[4 * tid] + vec[DO + 4 * tid], vec[4 * tid + 1] + vec[DO + 4 * tid + 1],
+             vec[4 * tid + 2] + vec[DO + 4 * tid + 2], vec[4 * tid + 3] + vec[DO + 4 * tid + 3]);
+    else
+      store4(dst, vec[4 * tid], vec[4 * tid + 1], vec[4 * tid + 2], vec[4 * tid + 3]);
   }
 }
 
@@ -968,7 +1062,8 @@ cudaError_t launch_fp8_partition(const Fp8Launch& a, cudaStream_t stream) {
     kernel<<<grid, threads, smem, stream>>>(p);
   };
   if (a.head_dim == 64) {
-    if (a.qg <= 8) launch(pa_fp8_partition_kernel<1, 64, false>, fp8::Smem<1>::THREADS, fp8::Smem<1>::total);
+    if (a.qg <= 8)
+      launch(pa_fp8_partition_kernel<1, 64, false>, fp8::Smem<1, false, true>::THREADS, fp8::Smem<1, false, true>::total);
     else launch(pa_fp8_partition_kernel<2, 64, false>, fp8::Smem<2>::THREADS, fp8::Smem<2>::total);
   } else {
     if (a.qg <= 8) launch(pa_fp8_partition_kernel<1, 128, false>, fp8::Smem<1>::THREADS, fp8::Smem<1>::total);
@@ -1029,14 +1124,14 @@ cudaError_t launch_fp8x_partition(const Fp8ExtLaunch& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <typename OutT, int HD>
+template <typename OutT, int HD, bool HALVES = false>
 static cudaError_t launch_combine_t(const CombineLaunch& a, OutT* out, cudaStream_t stream) {
   const int threads = combine_threads(HD, kCombineKmax128, a.num_partitions);
   const int rpc = combine_rows_per_cta(a.qg, threads);
   const int grid = a.num_seqs * a.num_kv_heads * (a.qg / rpc);
   const size_t smem = size_t(rpc) * (combine_smem_bytes(a.num_partitions, threads) + HD * sizeof(float));
   if (smem > 40 * 1024)
-    cudaFuncSetAttribute(combine_kernel<OutT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(combine_kernel<OutT, HD, HALVES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(threads * rpc);
@@ -1044,14 +1139,17 @@ static cudaError_t launch_combine_t(const CombineLaunch& a, OutT* out, cudaStrea
   cfg.stream = stream;
   // plain stream order: launched as a programmatic dependent of the partition
   // grid (its CTAs cannot sit beside the partition CTAs) the step took ~5 us more
-  return cudaLaunchKernelEx(&cfg, combine_kernel<OutT, HD>, a.part_o, a.part_m, a.part_l, out, a.num_kv_heads,
+  return cudaLaunchKernelEx(&cfg, combine_kernel<OutT, HD, HALVES>, a.part_o, a.part_m, a.part_l, out, a.num_kv_heads,
                             a.qg, a.num_partitions, a.out_stride_seq, a.out_stride_head, rpc, threads);
 }
 
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t stream) {
   if (a.num_seqs * a.num_kv_heads * a.qg <= 0) return cudaSuccess;
   cudaError_t e;
-  if (a.d == 64)
+  if (a.d == 64 && a.part_d == 128)
+    e = a.out_bf16 ? launch_combine_t<__nv_bfloat16, 128, true>(a, static_cast<__nv_bfloat16*>(a.out), stream)
+                   : launch_combine_t<float, 128, true>(a, static_cast<float*>(a.out), stream);
+  else if (a.d == 64)
     e = a.out_bf16 ? launch_combine_t<__nv_bfloat16, 64>(a, static_cast<__nv_bfloat16*>(a.out), stream)
                    : launch_combine_t<float, 64>(a, static_cast<float*>(a.out), stream);
   else

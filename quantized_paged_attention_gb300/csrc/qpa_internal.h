@@ -63,6 +63,7 @@ struct CombineLaunch {
   int num_seqs, num_kv_heads, qg, num_partitions, d;
   long long out_stride_seq, out_stride_head;
   int rot_perm = 0;   // uq only: undo the rotation's column permutation
+  int part_d = 0;     // fp8: floats per partial O row (2 d: two halves to add); 0 = d
 };
 
 struct UqLaunch {

@@ -77,8 +77,13 @@ def test_workspace_size(lib):
     rows = 2 * 1 * 2 * 8
     assert n >= rows * 130 * 4 and n % 256 == 0
     assert lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc(head_dim=96)), 2) == 0
+    # head_dim 64 with a group of at most 8 keeps both 64-dim halves of each
+    # partial row (the packed kernel): as many floats per row as head_dim 128
     n64 = lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc(head_dim=64)), 2)
-    assert n64 >= rows * 66 * 4 and n64 < n
+    assert n64 >= rows * 130 * 4
+    n64w = lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc(head_dim=64, query_group=16)), 2)
+    n128w = lib.pa_decode_fp8_workspace_size(ctypes.byref(_desc(query_group=16)), 2)
+    assert 2 * rows * 66 * 4 <= n64w < n128w
 
 
 def _ext_desc(query_len=2, per_token=1, **kw):
