@@ -215,6 +215,19 @@ def test_head_dim_64_block_sizes_and_bf16(bs):
     assert torch.max(torch.abs(o16.float() - out)).item() <= torch.max(torch.abs(out)).item() * 2 ** -8 + 1e-6
 
 
+@pytest.mark.parametrize("qg,P", [(1, 1), (3, 2), (8, 1), (8, 7), (5, 40)])
+def test_head_dim_64_packed_halves(qg, P):
+    """head_dim 64 with at most 8 query rows takes a 256-token tile group per
+    pass as two 128-token halves: sequences ending inside the first half, at
+    its end, one token into the second half and inside it, over block size 16
+    (a half spans several blocks), with partition counts from 1 to above the
+    tile groups of a sequence; all (seq, head) units against the oracle."""
+    lens = [0, 1, 100, 128, 129, 200, 256, 257, 383, 384, 385, 511, 700, 1500]
+    c = synth.make_fp8_case(990 + 10 * qg + P, lens, 3, qg, head_dim=64, block_size=16)
+    out, _, _ = Fp8Dev(c).run(P)
+    _check(c, out.cpu().double().numpy(), what=f"hd64 packed qg={qg} P={P}")
+
+
 @pytest.mark.parametrize("P", [1, 5, 32])
 def test_wide_group_partition_counts(P):
     """Query group 32 (two blocks of 16 rows over one KV head's pages) with
