@@ -613,9 +613,10 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     // an item get (m, l) = (-inf, 0) and no O.
     const int B = p.num_seqs;
     long long W = 0;
-    int Tmax = 0;
+    int Tmax = 0, T0 = 0;                // T0: tile groups of sequence lane (kept for the scan below)
     for (int s0 = 0; s0 < B; s0 += 32) {
       const int T = s0 + lane < B ? (seq_len(s0 + lane) + TG - 1) / TG : 0;
+      if (s0 == 0) T0 = T;
       W += (long long)__reduce_add_sync(0xffffffffu, (unsigned)T);
       Tmax = max(Tmax, __reduce_max_sync(0xffffffffu, T));
     }
@@ -645,7 +646,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       long long base = 0;
       for (int s0 = 0; s0 < B; s0 += 32) {
         const int sq = s0 + lane;
-        const int T = sq < B ? (seq_len(sq) + TG - 1) / TG : 0;
+        const int T = s0 == 0 ? T0 : (sq < B ? (seq_len(sq) + TG - 1) / TG : 0);
         int incl = T;
 #pragma unroll
         for (int sh = 1; sh < 32; sh <<= 1) {
@@ -730,6 +731,93 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             p.part_l[rb + i] = 0.f;
           }
         }
+        // ---- K/V tiles: this warp copies tokens [32 pw, 32 pw + 32) of each;
+        // issue_to(n) issues the item's tiles up to n
+        const size_t kvh_off = size_t(kvh) * head_bytes;
+        int32_t ent = ent0, nent = 0;
+        int ti = 0;
+        auto issue_to = [&](int i_end) -> bool {
+        for (; ti < i_end; ++ti) {
+          const int i = ti;
+          const int tg = tg_b + (PK ? i : (i >> 1));
+          if (PK || (i & 1) == 0) {
+            if (i > 0) ent = nent;
+            nent = (i + (PK ? 1 : 2) < nt) ? load_entries(cur.s, tg + 1) : 0;
+          }
+          const int s = j % NS;
+          const int rnd = j / NS;
+          if (rnd > 0 && !warp_wait(&empty[s], (rnd - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) return false;
+          const int tok0 = tg * TG + (PK ? 0 : (i & 1)) * TILE + 32 * pw;
+          int pa = __shfl_sync(0xffffffffu, ent, (tok0 & (TG - 1)) >> lbs);
+          int pb = __shfl_sync(0xffffffffu, ent, ((tok0 + 16) & (TG - 1)) >> lbs);
+          if (pa < 0 || pa >= p.num_blocks) {
+            if (tok0 < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+            pa = 0;
+          }
+          if (pb < 0 || pb >= p.num_blocks) {
+            if (tok0 + 16 < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+            pb = 0;
+          }
+          // tokens tok0 .. tok0 + 15 lie in block pa, tok0 + 16 .. in pb (the same
+          // block unless block_size is 16)
+          const uint8_t* ka = p.kv + size_t(pa) * blk_bytes + kvh_off + size_t(tok0 & (bs - 1)) * HD + lr * HD + cc * 16;
+          const uint8_t* kb = bs == 16 ? p.kv + size_t(pb) * blk_bytes + kvh_off + lr * HD + cc * 16 : ka + 16 * HD;
+          const uint32_t slot = ring + s * TILE_BYTES;
+#pragma unroll
+          for (int ii = 0; ii < NII; ++ii) {
+            const bool valid = tok0 + lr + RPI * ii < L;
+            const uint8_t* src = ii < NII / 2 ? ka + RPI * HD * ii : kb + RPI * HD * (ii - NII / 2);
+            const uint32_t dst = slot + (((RPI * ii) & 4) ? doff_o : doff_e) + RPI * D * ii;
+            cp_async16_zfill(dst, src, valid, pol);
+            cp_async16_zfill(dst + V_OFF, src + v_off, valid, pol);
+          }
+          if constexpr (PK) {
+            // the B half: tokens tok0 + TILE .., into chunks 4 .. 7 of the same rows
+            const int tokB = tok0 + TILE;
+            int qa = __shfl_sync(0xffffffffu, ent, (tokB & (TG - 1)) >> lbs);
+            int qb2 = __shfl_sync(0xffffffffu, ent, ((tokB + 16) & (TG - 1)) >> lbs);
+            if (qa < 0 || qa >= p.num_blocks) {
+              if (tokB < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+              qa = 0;
+            }
+            if (qb2 < 0 || qb2 >= p.num_blocks) {
+              if (tokB + 16 < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
+              qb2 = 0;
+            }
+            const uint8_t* kaB = p.kv + size_t(qa) * blk_bytes + kvh_off + size_t(tokB & (bs - 1)) * HD + lr * HD + cc * 16;
+            const uint8_t* kbB = bs == 16 ? p.kv + size_t(qb2) * blk_bytes + kvh_off + lr * HD + cc * 16 : kaB + 16 * HD;
+#pragma unroll
+            for (int ii = 0; ii < NII; ++ii) {
+              const bool valid = tokB + lr + RPI * ii < L;
+              const uint8_t* src = ii < NII / 2 ? kaB + RPI * HD * ii : kbB + RPI * HD * (ii - NII / 2);
+              const uint32_t dst = slot + (((RPI * ii) & 4) ? doffB_o : doffB_e) + RPI * D * ii;
+              cp_async16_zfill(dst, src, valid, pol);
+              cp_async16_zfill(dst + V_OFF, src + v_off, valid, pol);
+            }
+          }
+          if (per_token && lane < 16) {
+            // this warp's 32 tokens' K (lanes 0..7) or V (8..15) scales, 4 tokens
+            // per lane; the scale arrays are indexed like the cache's (block, head, slot)
+            const int ch = lane & 7;
+            const int blk = (bs == 16 && ch >= 4) ? pb : pa;
+            const float* sarr = lane < 8 ? p.k_scale : p.v_scale;
+            const float* src = sarr + (size_t(blk) * Hk + kvh) * bs + ((tok0 + 4 * ch) & (bs - 1));
+            const uint32_t dst = sc_s + 4 * (s * 2 * TILE + (lane < 8 ? 0 : TILE) + 32 * pw + 4 * ch);
+            cp_async16_zfill(dst, src, tok0 + 4 * ch < L, pol);
+          }
+          // the slot's barrier counts this lane once all its copies so far have landed
+          // (the timeout test withholds copy warp 0's arrival on the CTA's first tile)
+          if (!((p.test_flags & QPA_TEST_WITHHOLD_ARRIVAL) && j == 0 && pw == 0)) cp_async_arrive_noinc(&full[s]);
+          ++j;
+        }
+        return true;
+        };
+        // a CTA's first item: every ring slot is free, so its first tile goes
+        // out before its query operand is built (its copies overlap the build)
+        if (qcnt == 0 && !issue_to(1)) {
+          ok = false;
+          break;
+        }
         // ---- query operand: 4 e4m3 terms of q 2^a (a per row: max |q| 2^a in [128, 256))
         const int qb = qcnt & 1;
         if (qcnt >= 2 && !warp_wait(&qempty[qb], ((qcnt >> 1) - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) {
@@ -797,83 +885,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         if (lane == 0) mbar_arrive(&qfull[qb]);
         ++qcnt;
 
-        // ---- K/V tiles: this warp copies tokens [32 pw, 32 pw + 32) of each
-        const size_t kvh_off = size_t(kvh) * head_bytes;
-        int32_t ent = ent0, nent = 0;
-        for (int i = 0; i < nt; ++i) {
-          const int tg = tg_b + (PK ? i : (i >> 1));
-          if (PK || (i & 1) == 0) {
-            if (i > 0) ent = nent;
-            nent = (i + (PK ? 1 : 2) < nt) ? load_entries(cur.s, tg + 1) : 0;
-          }
-          const int s = j % NS;
-          const int rnd = j / NS;
-          if (rnd > 0 && !warp_wait(&empty[s], (rnd - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) {
-            ok = false;
-            break;
-          }
-          const int tok0 = tg * TG + (PK ? 0 : (i & 1)) * TILE + 32 * pw;
-          int pa = __shfl_sync(0xffffffffu, ent, (tok0 & (TG - 1)) >> lbs);
-          int pb = __shfl_sync(0xffffffffu, ent, ((tok0 + 16) & (TG - 1)) >> lbs);
-          if (pa < 0 || pa >= p.num_blocks) {
-            if (tok0 < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
-            pa = 0;
-          }
-          if (pb < 0 || pb >= p.num_blocks) {
-            if (tok0 + 16 < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
-            pb = 0;
-          }
-          // tokens tok0 .. tok0 + 15 lie in block pa, tok0 + 16 .. in pb (the same
-          // block unless block_size is 16)
-          const uint8_t* ka = p.kv + size_t(pa) * blk_bytes + kvh_off + size_t(tok0 & (bs - 1)) * HD + lr * HD + cc * 16;
-          const uint8_t* kb = bs == 16 ? p.kv + size_t(pb) * blk_bytes + kvh_off + lr * HD + cc * 16 : ka + 16 * HD;
-          const uint32_t slot = ring + s * TILE_BYTES;
-#pragma unroll
-          for (int ii = 0; ii < NII; ++ii) {
-            const bool valid = tok0 + lr + RPI * ii < L;
-            const uint8_t* src = ii < NII / 2 ? ka + RPI * HD * ii : kb + RPI * HD * (ii - NII / 2);
-            const uint32_t dst = slot + (((RPI * ii) & 4) ? doff_o : doff_e) + RPI * D * ii;
-            cp_async16_zfill(dst, src, valid, pol);
-            cp_async16_zfill(dst + V_OFF, src + v_off, valid, pol);
-          }
-          if constexpr (PK) {
-            // the B half: tokens tok0 + TILE .., into chunks 4 .. 7 of the same rows
-            const int tokB = tok0 + TILE;
-            int qa = __shfl_sync(0xffffffffu, ent, (tokB & (TG - 1)) >> lbs);
-            int qb2 = __shfl_sync(0xffffffffu, ent, ((tokB + 16) & (TG - 1)) >> lbs);
-            if (qa < 0 || qa >= p.num_blocks) {
-              if (tokB < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
-              qa = 0;
-            }
-            if (qb2 < 0 || qb2 >= p.num_blocks) {
-              if (tokB + 16 < L && lane == 0) atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
-              qb2 = 0;
-            }
-            const uint8_t* kaB = p.kv + size_t(qa) * blk_bytes + kvh_off + size_t(tokB & (bs - 1)) * HD + lr * HD + cc * 16;
-            const uint8_t* kbB = bs == 16 ? p.kv + size_t(qb2) * blk_bytes + kvh_off + lr * HD + cc * 16 : kaB + 16 * HD;
-#pragma unroll
-            for (int ii = 0; ii < NII; ++ii) {
-              const bool valid = tokB + lr + RPI * ii < L;
-              const uint8_t* src = ii < NII / 2 ? kaB + RPI * HD * ii : kbB + RPI * HD * (ii - NII / 2);
-              const uint32_t dst = slot + (((RPI * ii) & 4) ? doffB_o : doffB_e) + RPI * D * ii;
-              cp_async16_zfill(dst, src, valid, pol);
-              cp_async16_zfill(dst + V_OFF, src + v_off, valid, pol);
-            }
-          }
-          if (per_token && lane < 16) {
-            // this warp's 32 tokens' K (lanes 0..7) or V (8..15) scales, 4 tokens
-            // per lane; the scale arrays are indexed like the cache's (block, head, slot)
-            const int ch = lane & 7;
-            const int blk = (bs == 16 && ch >= 4) ? pb : pa;
-            const float* sarr = lane < 8 ? p.k_scale : p.v_scale;
-            const float* src = sarr + (size_t(blk) * Hk + kvh) * bs + ((tok0 + 4 * ch) & (bs - 1));
-            const uint32_t dst = sc_s + 4 * (s * 2 * TILE + (lane < 8 ? 0 : TILE) + 32 * pw + 4 * ch);
-            cp_async16_zfill(dst, src, tok0 + 4 * ch < L, pol);
-          }
-          // the slot's barrier counts this lane once all its copies so far have landed
-          // (the timeout test withholds copy warp 0's arrival on the CTA's first tile)
-          if (!((p.test_flags & QPA_TEST_WITHHOLD_ARRIVAL) && j == 0 && pw == 0)) cp_async_arrive_noinc(&full[s]);
-          ++j;
+        if (!issue_to(nt)) {
+          ok = false;
+          break;
         }
       }
       cur = nxt;
