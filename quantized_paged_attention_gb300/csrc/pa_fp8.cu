@@ -30,13 +30,16 @@
 //  * a QK warp and a PV warp issue tcgen05.mma kind::f8f6f4 straight on the
 //    e4m3 bytes: S^T = K Q'^T (M = 128 tokens, N = 32 or 64) and
 //    O^T = V^T P'^T (M = 128 dims, N = 32 or 64), accumulators in tensor
-//    memory (two S and four O buffers).
+//    memory (two S buffers, four O buffers with 8 rows, two with 16).
 //  * two groups of 4 softmax warps: thread t owns tensor-memory lane t, i.e.
 //    token t of an S tile and dim t of an O tile. With up to 8 query rows the
 //    groups take alternate tiles and merge per item; with 16 rows each group
-//    owns 8 rows of every tile. They turn S into probabilities (online
-//    softmax across the item's tiles), write P' for the next MMA, and fold
-//    each O tile into per-dim register accumulators with the softmax rescale.
+//    owns 8 rows of every tile and takes the tiles two at a time (one maxima
+//    exchange, one rescale and one O fold per 256 tokens; the second tile's
+//    PV accumulates onto the first's O). They turn S into probabilities
+//    (online softmax across the item's tiles), write P' for the next MMA, and
+//    fold each O buffer into per-dim register accumulators with the softmax
+//    rescale.
 // Exactness: the query (bf16) and the probabilities (f16) enter the fp8 MMA
 // as sums of e4m3 terms with power-of-two weights -- 4 terms for q (exact for
 // bf16 inputs), 3 terms for p (exact for its f16 value) -- so the tensor core
@@ -84,7 +87,8 @@ struct Smem {
   static constexpr int lredOff = redOff + 2 * 4 * R * 4;   // [2][8 warps][8] row sums per warp
   static constexpr int msmOff = lredOff + 2 * 4 * NWG * R * 4;   // [2][2 groups][8] row maxima per group
   static constexpr int infoOff = msmOff + 2 * NWG * R * 4; // [2] {item, L, tiles, first tile group}, {row block, ..}
-  static constexpr int scOff = infoOff + 2 * 32;           // EXT: [NS][K, V][128] f32 per-token scales
+  static constexpr int pdOff = infoOff + 2 * 32;           // [4] per P' buffer: O buffer, accumulate, commit (16 rows)
+  static constexpr int scOff = pdOff + 16;                 // EXT: [NS][K, V][128] f32 per-token scales
   static constexpr int barOff = (scOff + (EXT ? NS * 2 * TILE * 4 : 0) + 7) & ~7;
   static constexpr int NBAR = 2 * NS + 27;
   static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag, QK total
@@ -131,6 +135,7 @@ __global__ void __launch_bounds__(fp8::Smem<NT>::THREADS, 1)
 pa_fp8_partition_kernel(const Fp8Params p) {
   using namespace fp8;
   constexpr bool PK = HD == 64 && NT == 1 && !EXT;   // two 128-token halves per ring slot
+  constexpr bool RS = NT == 2;                        // 16 rows: row split, two tiles per softmax pass
   using S = Smem<NT, EXT, PK>;
   constexpr int R = S::R, NQ = S::NQ, NQS = S::NQS, NWG = S::NWG;
   constexpr int PD = PK ? 2 * HD : HD;                // floats per partial O row
@@ -163,6 +168,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   const uint32_t lred_s = sbase + S::lredOff;
   const uint32_t msm_s = sbase + S::msmOff;
   const uint32_t info_s = sbase + S::infoOff;
+  const uint32_t pd_s = sbase + S::pdOff;
   const uint32_t sc_s = sbase + S::scOff;
   const uint32_t stg_s = sbase + S::stgOff;
   const uint32_t ring = sbase + S::ringOff;
@@ -230,8 +236,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     // j & 1 == g (buffer b = g) and the groups merge their states per item;
     // with 16 rows (row split) group g owns rows 8g .. 8g + 7 of every tile,
     // reads its 32 columns of S and O and writes its 32 columns of P', and
-    // finishes its own rows. Either way a thread carries RG = 8 rows.
-    constexpr bool RS = NT == 2;
+    // finishes its own rows; its passes take two tiles (P' buffers (j + u) & 3,
+    // O buffer = pass & 1). Either way a thread carries RG = 8 rows.
     constexpr int RG = 8;
     constexpr int NG = RS ? 2 : 1;                     // row blocks
     const int wg = warp >> 2;
@@ -246,26 +252,24 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     float m[RG], l[RG], o[RG], c[RG];
 #pragma unroll
     for (int r = 0; r < RG; ++r) { o[r] = 0.f; m[r] = -INFINITY; l[r] = 0.f; c[r] = 0.f; }
-    int j = 0, qcnt = 0;
+    int j = 0, qcnt = 0, pc = 0;         // pc: passes (16 rows)
     bool ok = true;
-    int pend_j = -1;                     // this group's tile whose O is not folded in yet
-    float pend_alpha[RG];
-#pragma unroll
-    for (int r = 0; r < RG; ++r) pend_alpha[r] = 0.f;
-    // O of tile pend_j (rescale factor pend_alpha) into the accumulators
-    auto fold = [&]() -> bool {
-      const int ob = 2 * (pend_j & 1) + ((pend_j >> 1) & 1);
-      if (!warp_wait(&ofull[ob], (pend_j >> 2) & 1, abort_flag, KERR_TIMEOUT_FULL)) return false;
+    int pend_ob = -1;                    // this group's O buffer not folded in yet
+    uint32_t pend_oph = 0;               // (its ofull phase)
+    // o = (o + O buffer pend_ob) alpha: o and that O are relative to the
+    // previous pass's maxima, alpha takes them to the current ones
+    auto fold = [&](const float (&alpha)[RG]) -> bool {
+      if (!warp_wait(&ofull[pend_ob], pend_oph, abort_flag, KERR_TIMEOUT_FULL)) return false;
       tc_fence_after();
       float w[32];
       // (PK: lanes 64..127, the B half's dims, read the B columns)
-      tmem_ld32(tl + 2 * NQS + ob * NQS + 32 * rblk + (PK && wq >= 2 ? NQ : 0), w);
+      tmem_ld32(tl + 2 * NQS + pend_ob * NQS + 32 * rblk + (PK && wq >= 2 ? NQ : 0), w);
       tmem_wait_ld();
       tc_fence_before();
 #pragma unroll
       for (int r = 0; r < RG; ++r) {
         const float sv = fmaf(fmaf(w[2 * RG + r], 0.0625f, w[RG + r]), 0.0625f, w[r]);
-        o[r] = fmaf(sv, 0.00390625f, o[r] * pend_alpha[r]);
+        o[r] = fmaf(sv, 0.00390625f, o[r]) * alpha[r];
       }
       return true;
     };
@@ -299,72 +303,96 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         l[r] = 0.f;
         vis[r] = EXT ? L - QL + 1 + (rbase + RG * rblk + r) / p.qg : L;
       }
-      for (int i = 0; i < nt; ++i, ++j) {
-        if (!RS && (j & 1) != wg) continue;
-        const int start = PK ? (tg0 + i) * TG : (tg0 + (i >> 1)) * TG + (i & 1) * TILE;
-        const int b = j & 1;                 // S buffer
-        const int ob = 2 * b + ((j >> 1) & 1);   // P' and O buffer (alternate per group)
-        // ---- softmax of tile j
-        if (!warp_wait(&sfull[b], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
-        tc_fence_after();
-        float v[32];
-        float vB[PK ? 32 : 1];               // PK: the B half's scores (token start + TILE + t)
-        tmem_ld32(tl + b * NQS + 32 * rblk, v);
-        if constexpr (PK) tmem_ld32(tl + b * NQS + NQ, vB);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sfree[b]);
-        const bool valid = start + t < L;
-        float x[RG];
-        float vs_t = 1.f;                    // this token's V scale (EXT, per token)
-        if constexpr (EXT) {
-          float ks_t = 1.f;
-          if (per_token) {
-            // the tile's scales landed with its copies (the slot's full barrier)
-            if (!warp_wait(&full[j % NS], (j / NS) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
-            ks_t = ldsf(sc_s + 4 * ((j % NS) * 2 * TILE + t));
-            vs_t = valid ? ldsf(sc_s + 4 * ((j % NS) * 2 * TILE + TILE + t)) : 0.f;
-          }
+      // a pass takes NP consecutive tiles of the item (16 rows: two, so that
+      // the maxima exchange, the rescale and the O fold run once per 256
+      // tokens and the PV of the second tile accumulates onto the first's O;
+      // 8 rows: one, every other tile being the other group's)
+      for (int i = 0; i < nt;) {
+        int np = 1;
+        if constexpr (RS) np = min(2, nt - i);
+        if (!RS && (j & 1) != wg) {
+          ++i;
+          ++j;
+          continue;
+        }
+        const int xs = RS ? (pc & 1) : (j & 1);                         // maxima exchange slot
+        const uint32_t xph = RS ? (pc >> 1) & 1 : (j >> 1) & 1;
+        const int ob = RS ? (pc & 1) : 2 * (j & 1) + ((j >> 1) & 1);    // O buffer (8 rows: also the P' buffer)
+        const uint32_t oph = RS ? (pc >> 1) & 1 : (j >> 2) & 1;
+        // ---- scores of tile j + u (S buffer (j + u) & 1) into xo
+        float x0[RG], x1[RG];
+        float vs0 = 1.f, vs1 = 1.f;          // the token's V scale per tile (EXT, per token)
+        float xB[PK ? RG : 1];               // PK: the B half's scores (token start + TILE + t)
+        auto scores = [&](int u, float (&xo)[RG], float& vso) -> bool {
+          const int iu = i + u, ju = j + u, b = ju & 1;
+          const int start = PK ? (tg0 + iu) * TG : (tg0 + (iu >> 1)) * TG + (iu & 1) * TILE;
+          if (!warp_wait(&sfull[b], (ju >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) return false;
+          tc_fence_after();
+          float v[32];
+          float vB[PK ? 32 : 1];
+          tmem_ld32(tl + b * NQS + 32 * rblk, v);
+          if constexpr (PK) tmem_ld32(tl + b * NQS + NQ, vB);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sfree[b]);
+          const bool valid = start + t < L;
+          if constexpr (EXT) {
+            float ks_t = 1.f;
+            if (per_token) {
+              // the tile's scales landed with its copies (the slot's full barrier)
+              if (!warp_wait(&full[ju % NS], (ju / NS) & 1, abort_flag, KERR_TIMEOUT_FULL)) return false;
+              ks_t = ldsf(sc_s + 4 * ((ju % NS) * 2 * TILE + t));
+              vso = valid ? ldsf(sc_s + 4 * ((ju % NS) * 2 * TILE + TILE + t)) : 0.f;
+            }
 #pragma unroll
-          for (int r = 0; r < RG; ++r) {
-            const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
-            x[r] = start + t < vis[r] ? sv * c[r] * ks_t : -INFINITY;
+            for (int r = 0; r < RG; ++r) {
+              const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
+              xo[r] = start + t < vis[r] ? sv * c[r] * ks_t : -INFINITY;
+            }
+          } else {
+#pragma unroll
+            for (int r = 0; r < RG; ++r) {
+              const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
+              xo[r] = valid ? sv * c[r] : -INFINITY;
+            }
           }
+          if constexpr (PK) {
+            const bool validB = start + TILE + t < L;
+#pragma unroll
+            for (int r = 0; r < RG; ++r) {
+              const float sv = fmaf(fmaf(fmaf(vB[3 * RG + r], 0.0625f, vB[2 * RG + r]), 0.0625f, vB[RG + r]), 0.0625f,
+                                    vB[r]);
+              xB[r] = validB ? sv * c[r] : -INFINITY;
+            }
+          }
+          return true;
+        };
+        if (!scores(0, x0, vs0)) { ok = false; break; }
+        if (RS && np > 1) {
+          if (!scores(1, x1, vs1)) { ok = false; break; }
         } else {
 #pragma unroll
-          for (int r = 0; r < RG; ++r) {
-            const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
-            x[r] = valid ? sv * c[r] : -INFINITY;
-          }
-        }
-        float xB[PK ? RG : 1];
-        if constexpr (PK) {
-          const bool validB = start + TILE + t < L;
-#pragma unroll
-          for (int r = 0; r < RG; ++r) {
-            const float sv = fmaf(fmaf(fmaf(vB[3 * RG + r], 0.0625f, vB[2 * RG + r]), 0.0625f, vB[RG + r]), 0.0625f, vB[r]);
-            xB[r] = validB ? sv * c[r] : -INFINITY;
-          }
+          for (int r = 0; r < RG; ++r) x1[r] = -INFINITY;
         }
         {
-          // row maxima over the warp's 32 tokens (hardware warp reduction)
+          // row maxima over the warp's 32 tokens of the pass (hardware warp reduction)
           float mx[RG];
 #pragma unroll
-          for (int r = 0; r < RG; ++r) mx[r] = warp_max(PK ? fmaxf(x[r], xB[r]) : x[r]);
+          for (int r = 0; r < RG; ++r) mx[r] = warp_max(PK ? fmaxf(x0[r], xB[r]) : RS ? fmaxf(x0[r], x1[r]) : x0[r]);
           if (lane == 0) {
 #pragma unroll
             for (int q4 = 0; q4 < RG / 4; ++q4)
-              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red_s + 4 * (((b * NG + rblk) * 4 + wq) * RG + 4 * q4)),
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red_s + 4 * (((xs * NG + rblk) * 4 + wq) * RG + 4 * q4)),
                            "f"(mx[4 * q4]), "f"(mx[4 * q4 + 1]), "f"(mx[4 * q4 + 2]), "f"(mx[4 * q4 + 3]) : "memory");
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xbar[2 * b + rblk]);
-        if (!warp_wait(&xbar[2 * b + rblk], (j >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
+        if (lane == 0) mbar_arrive(&xbar[2 * xs + rblk]);
+        if (!warp_wait(&xbar[2 * xs + rblk], xph, abort_flag, KERR_TIMEOUT_FULL)) { ok = false; break; }
         float alpha[RG];
         {
-          const uint32_t rb = red_s + (b * NG + rblk) * 4 * RG * 4;
+          const uint32_t rb = red_s + (xs * NG + rblk) * 4 * RG * 4;
 #pragma unroll
           for (int q4 = 0; q4 < RG / 4; ++q4) {
             const float4 a0 = lds_f4(rb + 16 * q4), a1 = lds_f4(rb + 16 * (RG / 4 + q4));
@@ -381,88 +409,112 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             }
           }
         }
-        // probabilities (f16), the row sums, and P' = 3 e4m3 terms of 256 p
-        uint32_t tw[3][RG / 4];
-#pragma unroll
-        for (int k = 0; k < RG / 2; ++k) {
-          float pa0, pa1;
-          if constexpr (EXT) {
-            pa0 = x[2 * k] == -INFINITY ? 0.f : ex2(x[2 * k] - m[2 * k]);
-            pa1 = x[2 * k + 1] == -INFINITY ? 0.f : ex2(x[2 * k + 1] - m[2 * k + 1]);
-          } else {
-            pa0 = ex2(x[2 * k] - m[2 * k]);
-            pa1 = ex2(x[2 * k + 1] - m[2 * k + 1]);
-          }
-          const uint32_t p16 = f32x2_to_f16x2(pa0, pa1);
-          l[2 * k] = fmaf(l[2 * k], alpha[2 * k], f16_lo_to_f32(p16));
-          l[2 * k + 1] = fmaf(l[2 * k + 1], alpha[2 * k + 1], f16_hi_to_f32(p16));
-          // the PV operand: p, times the token's V scale with per-token scales
-          const uint32_t pv16 = per_token ? f32x2_to_f16x2(pa0 * vs_t, pa1 * vs_t) : p16;
-          uint32_t h = hmul2(pv16, 0x5C005C00u);                     // x 256
-          const uint32_t e0 = f16x2_to_e4m3x2(h);
-          h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e0)), 0x4C004C00u);   // residual x 16
-          const uint32_t e1 = f16x2_to_e4m3x2(h);
-          h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e1)), 0x4C004C00u);
-          const uint32_t e2 = f16x2_to_e4m3x2(h);
-          if (k & 1) {
-            tw[0][k >> 1] |= e0 << 16;
-            tw[1][k >> 1] |= e1 << 16;
-            tw[2][k >> 1] |= e2 << 16;
-          } else {
-            tw[0][k >> 1] = e0;
-            tw[1][k >> 1] = e1;
-            tw[2][k >> 1] = e2;
-          }
-        }
-        {
-          // columns slot * 8 + row of the group's 32: terms 0, 1 | term 2, zero slot
-          const uint32_t pb = ptok + ob * S::pBytes;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(tw[0][0]), "r"(tw[0][1]),
-                       "r"(tw[1][0]), "r"(tw[1][1]) : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(tw[2][0]), "r"(tw[2][1]),
-                       "r"(0u), "r"(0u) : "memory");
-        }
-        if constexpr (PK) {
-          // the B half: the same for token start + TILE + t, its columns after A's
-          uint32_t twB[3][RG / 4];
+        // ---- probabilities (f16) of tile j + u, the row sums, and P' = 3 e4m3
+        // terms of 256 p into P' buffer pbuf, published at once (16 rows: the
+        // first tile's PV starts while the second's P' is built)
+        auto emit = [&](int u, const float (&xo)[RG], float vso, int pbuf) {
+          uint32_t tw[3][RG / 4];
 #pragma unroll
           for (int k = 0; k < RG / 2; ++k) {
-            const uint32_t p16 = f32x2_to_f16x2(ex2(xB[2 * k] - m[2 * k]), ex2(xB[2 * k + 1] - m[2 * k + 1]));
-            l[2 * k] += f16_lo_to_f32(p16);
-            l[2 * k + 1] += f16_hi_to_f32(p16);
-            uint32_t h = hmul2(p16, 0x5C005C00u);
+            float pa0, pa1;
+            if constexpr (EXT) {
+              pa0 = xo[2 * k] == -INFINITY ? 0.f : ex2(xo[2 * k] - m[2 * k]);
+              pa1 = xo[2 * k + 1] == -INFINITY ? 0.f : ex2(xo[2 * k + 1] - m[2 * k + 1]);
+            } else {
+              pa0 = ex2(xo[2 * k] - m[2 * k]);
+              pa1 = ex2(xo[2 * k + 1] - m[2 * k + 1]);
+            }
+            const uint32_t p16 = f32x2_to_f16x2(pa0, pa1);
+            if (u == 0) {
+              l[2 * k] = fmaf(l[2 * k], alpha[2 * k], f16_lo_to_f32(p16));
+              l[2 * k + 1] = fmaf(l[2 * k + 1], alpha[2 * k + 1], f16_hi_to_f32(p16));
+            } else {
+              l[2 * k] += f16_lo_to_f32(p16);
+              l[2 * k + 1] += f16_hi_to_f32(p16);
+            }
+            // the PV operand: p, times the token's V scale with per-token scales
+            const uint32_t pv16 = per_token ? f32x2_to_f16x2(pa0 * vso, pa1 * vso) : p16;
+            uint32_t h = hmul2(pv16, 0x5C005C00u);                     // x 256
             const uint32_t e0 = f16x2_to_e4m3x2(h);
-            h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e0)), 0x4C004C00u);
+            h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e0)), 0x4C004C00u);   // residual x 16
             const uint32_t e1 = f16x2_to_e4m3x2(h);
             h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e1)), 0x4C004C00u);
             const uint32_t e2 = f16x2_to_e4m3x2(h);
             if (k & 1) {
-              twB[0][k >> 1] |= e0 << 16;
-              twB[1][k >> 1] |= e1 << 16;
-              twB[2][k >> 1] |= e2 << 16;
+              tw[0][k >> 1] |= e0 << 16;
+              tw[1][k >> 1] |= e1 << 16;
+              tw[2][k >> 1] |= e2 << 16;
             } else {
-              twB[0][k >> 1] = e0;
-              twB[1][k >> 1] = e1;
-              twB[2][k >> 1] = e2;
+              tw[0][k >> 1] = e0;
+              tw[1][k >> 1] = e1;
+              tw[2][k >> 1] = e2;
             }
           }
-          const uint32_t pb = ptok + ob * S::pBytes + 256;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(twB[0][0]), "r"(twB[0][1]),
-                       "r"(twB[1][0]), "r"(twB[1][1]) : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(twB[2][0]), "r"(twB[2][1]),
-                       "r"(0u), "r"(0u) : "memory");
-        }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pfull[ob]);
-        // ---- fold this group's previous O tile while the tensor core computes this one
-        if (pend_j >= 0 && !fold()) { ok = false; break; }
-        pend_j = j;
+          {
+            // columns slot * 8 + row of the group's 32: terms 0, 1 | term 2, zero slot
+            const uint32_t pb = ptok + pbuf * S::pBytes;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(tw[0][0]), "r"(tw[0][1]),
+                         "r"(tw[1][0]), "r"(tw[1][1]) : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(tw[2][0]), "r"(tw[2][1]),
+                         "r"(0u), "r"(0u) : "memory");
+          }
+          if (RS && threadIdx.x == 0) {
+            // the PV warp's orders for this P' buffer: O buffer, accumulate, commit O
+            const uint32_t d = uint32_t(ob) | (uint32_t(u) << 1) | (uint32_t(u == np - 1) << 2);
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(pd_s + 4 * pbuf), "r"(d) : "memory");
+          }
+          if constexpr (PK) {
+            // the B half: the same for token start + TILE + t, its columns after A's
+            uint32_t twB[3][RG / 4];
 #pragma unroll
-        for (int r = 0; r < RG; ++r) pend_alpha[r] = alpha[r];
+            for (int k = 0; k < RG / 2; ++k) {
+              const uint32_t p16 = f32x2_to_f16x2(ex2(xB[2 * k] - m[2 * k]), ex2(xB[2 * k + 1] - m[2 * k + 1]));
+              l[2 * k] += f16_lo_to_f32(p16);
+              l[2 * k + 1] += f16_hi_to_f32(p16);
+              uint32_t h = hmul2(p16, 0x5C005C00u);
+              const uint32_t e0 = f16x2_to_e4m3x2(h);
+              h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e0)), 0x4C004C00u);
+              const uint32_t e1 = f16x2_to_e4m3x2(h);
+              h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e1)), 0x4C004C00u);
+              const uint32_t e2 = f16x2_to_e4m3x2(h);
+              if (k & 1) {
+                twB[0][k >> 1] |= e0 << 16;
+                twB[1][k >> 1] |= e1 << 16;
+                twB[2][k >> 1] |= e2 << 16;
+              } else {
+                twB[0][k >> 1] = e0;
+                twB[1][k >> 1] = e1;
+                twB[2][k >> 1] = e2;
+              }
+            }
+            const uint32_t pb = ptok + pbuf * S::pBytes + 256;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(twB[0][0]), "r"(twB[0][1]),
+                         "r"(twB[1][0]), "r"(twB[1][1]) : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(twB[2][0]), "r"(twB[2][1]),
+                         "r"(0u), "r"(0u) : "memory");
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pfull[pbuf]);
+        };
+        emit(0, x0, vs0, RS ? j & 3 : ob);
+        if (RS && np > 1) emit(1, x1, vs1, (j + 1) & 3);
+        // ---- fold this group's previous O (relative to the previous maxima,
+        // so times alpha) while the tensor core computes this pass's
+        if (pend_ob >= 0 && !fold(alpha)) { ok = false; break; }
+        pend_ob = ob;
+        pend_oph = oph;
+        i += np;
+        j += np;
+        ++pc;
       }
-      if (ok && pend_j >= 0 && !fold()) ok = false;
-      pend_j = -1;
+      if (ok && pend_ob >= 0) {
+        float one[RG];
+#pragma unroll
+        for (int r = 0; r < RG; ++r) one[r] = 1.f;
+        if (!fold(one)) ok = false;
+      }
+      pend_ob = -1;
       if (!ok) break;
 
       // ---- item done: row sums over the group's 128 token lanes, then the
@@ -954,10 +1006,42 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     __syncwarp();
   } else {
     // ======================================================== PV warp
-    // O^T = V^T P'^T for each tile once its softmax group wrote P' (one cursor
-    // per buffer parity, so the two groups never wait for each other); frees
-    // the tile's ring slot.
-    if (lane == 0) {
+    // O^T = V^T P'^T for each tile once its softmax group wrote P' (8 rows: one
+    // cursor per buffer parity, so the two groups never wait for each other;
+    // 16 rows: tiles in order, into the O buffer of their pass); frees the
+    // tile's ring slot.
+    if (RS && lane == 0) {
+      int jj = 0;
+      unsigned long long t_prog = globaltimer();
+      while (true) {
+        const int total = *qk_total;
+        if (total >= 0 && jj >= total) break;
+        const int pb = jj & 3;
+        if (mbar_test_wait(&pfull[pb], (jj >> 2) & 1)) {
+          tc_fence_after();
+          const uint32_t d = lds32(pd_s + 4 * pb);
+          const uint32_t ob = d & 1u, acc = (d >> 1) & 1u;
+          const uint32_t va = ring + (jj % NS) * TILE_BYTES + V_OFF;
+          const uint32_t pa = psm + pb * S::pBytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_e4m3(tmem + 2 * NQS + ob * NQS, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
+                     umma_desc(pa + k * 32 * NQS, 8 * NQS, 128, kSwizzleNone), IDESC_PV, acc | uint32_t(k));
+          umma_commit(&empty[jj % NS]);
+          if (d & 4u) umma_commit(&ofull[ob]);
+          ++jj;
+          t_prog = globaltimer();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer() - t_prog > kWaitLimitNs) {
+            atomicExch(&g_kernel_error, KERR_TIMEOUT_FULL);
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+      umma_commit(done);
+    } else if (!RS && lane == 0) {
       int pv_n[2] = {0, 1};
       unsigned long long t_prog = globaltimer();
       while (true) {
