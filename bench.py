@@ -45,9 +45,10 @@ def _args():
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads' measurements")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=["fp8", "uq", "uq_rand", "idx"], default=None,
+    ap.add_argument("--profile-case", choices=["fp8", "fp8x", "uq", "uq_rand", "idx"], default=None,
                     help="run only this case's kernels (warmup + steps launches) for a profiler; "
-                         "fp8: 8 seqs x 16384 (268 MB), uq: 4 seqs x 75000 (173 MB), "
+                         "fp8: 8 seqs x 16384 (268 MB), fp8x: the same with 4 query tokens x group 4 "
+                         "and per-token scales, uq: 4 seqs x 75000 (173 MB), "
                          "idx: 128 requests (170 MB); prints one status line, not the bench line")
     return ap.parse_args()
 
@@ -427,6 +428,10 @@ def _profile_case(a):
     if a.profile_case == "fp8":
         c = synth.make_fp8_case(1001, [16384] * 8, 8, 8, 128, 16, poison=False)
         step, part = fp8_steps(c, 32, dev)
+    elif a.profile_case == "fp8x":
+        # the 16-row multi-token kernel: 4 query tokens x group 4, per-token scales
+        c = synth.fp8_ext_long(batch=8, query_group=4, query_len=4, per_token=True)
+        step = part = fp8_ext_step(c, 32, dev)
     elif a.profile_case in ("uq", "uq_rand"):
         cent = synth.sorted_random_centroids(5) if a.profile_case == "uq_rand" else None
         c = synth.uq_full(centroids=cent)

@@ -157,6 +157,11 @@ __device__ __forceinline__ int4 lds_i4(uint32_t addr) {
 __device__ __forceinline__ void sts_i4(uint32_t addr, int4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
+// a / b for a, b >= 0: a 32-bit division when both fit in 32 bits (the
+// 64-bit one is a much longer instruction sequence)
+__device__ __forceinline__ long long div_nonneg(long long a, long long b) {
+  return ((unsigned long long)(a | b) >> 32) == 0 ? (long long)((unsigned)a / (unsigned)b) : a / b;
+}
 // Maximum of x over the 32 lanes of the warp, returned to every lane.
 __device__ __forceinline__ float warp_max(float x) {
   float r;

@@ -249,9 +249,13 @@ pa_fp8_partition_kernel(const Fp8Params p) {
     // this token's P' row, the group's 32 columns
     // (PK: the B half's 32 columns follow at + 256)
     const uint32_t ptok = psm + (t >> 3) * (8 * NQS) + (t & 7) * 16 + 256 * rblk;
+    // a row's running maximum starts at kNoMax, finite, so that exponent
+    // differences stay defined for a row that has seen no token yet (masked
+    // scores are -inf: their terms are exactly 0, and two kNoMax give alpha 1)
+    constexpr float kNoMax = -1e30f;
     float m[RG], l[RG], o[RG], c[RG];
 #pragma unroll
-    for (int r = 0; r < RG; ++r) { o[r] = 0.f; m[r] = -INFINITY; l[r] = 0.f; c[r] = 0.f; }
+    for (int r = 0; r < RG; ++r) { o[r] = 0.f; m[r] = kNoMax; l[r] = 0.f; c[r] = 0.f; }
     int j = 0, qcnt = 0, pc = 0;         // pc: passes (16 rows)
     bool ok = true;
     int pend_ob = -1;                    // this group's O buffer not folded in yet
@@ -299,7 +303,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       int vis[RG];
 #pragma unroll
       for (int r = 0; r < RG; ++r) {
-        m[r] = -INFINITY;
+        m[r] = kNoMax;
         l[r] = 0.f;
         vis[r] = EXT ? L - QL + 1 + (rbase + RG * rblk + r) / p.qg : L;
       }
@@ -337,24 +341,31 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&sfree[b]);
           const bool valid = start + t < L;
+          // every row sees every token of the tile (warp-uniform): no masks
+          const bool whole = start + TILE <= L - (EXT ? QL - 1 : 0);
+          float cs[RG];                      // logit multiplier of each row for this token
+#pragma unroll
+          for (int r = 0; r < RG; ++r) cs[r] = c[r];
           if constexpr (EXT) {
-            float ks_t = 1.f;
             if (per_token) {
               // the tile's scales landed with its copies (the slot's full barrier)
               if (!warp_wait(&full[ju % NS], (ju / NS) & 1, abort_flag, KERR_TIMEOUT_FULL)) return false;
-              ks_t = ldsf(sc_s + 4 * ((ju % NS) * 2 * TILE + t));
+              const float ks_t = ldsf(sc_s + 4 * ((ju % NS) * 2 * TILE + t));
               vso = valid ? ldsf(sc_s + 4 * ((ju % NS) * 2 * TILE + TILE + t)) : 0.f;
-            }
 #pragma unroll
-            for (int r = 0; r < RG; ++r) {
-              const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
-              xo[r] = start + t < vis[r] ? sv * c[r] * ks_t : -INFINITY;
+              for (int r = 0; r < RG; ++r) cs[r] *= ks_t;
             }
+          }
+          if (whole) {
+#pragma unroll
+            for (int r = 0; r < RG; ++r)
+              xo[r] = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]) * cs[r];
           } else {
 #pragma unroll
             for (int r = 0; r < RG; ++r) {
               const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
-              xo[r] = valid ? sv * c[r] : -INFINITY;
+              // (EXT: the row's causal bound, which implies start + t < L)
+              xo[r] = (EXT ? start + t < vis[r] : valid) ? sv * cs[r] : -INFINITY;
             }
           }
           if constexpr (PK) {
@@ -403,37 +414,26 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             for (int u = 0; u < 4; ++u) {
               const int r = 4 * q4 + u;
               const float mn = fmaxf(m[r], tm[u]);
-              // (EXT: a row may have seen no token yet, -inf - -inf)
-              alpha[r] = (EXT && mn == -INFINITY) ? 1.f : ex2(m[r] - mn);
+              alpha[r] = ex2(m[r] - mn);
               m[r] = mn;
             }
           }
         }
-        // ---- probabilities (f16) of tile j + u, the row sums, and P' = 3 e4m3
-        // terms of 256 p into P' buffer pbuf, published at once (16 rows: the
-        // first tile's PV starts while the second's P' is built)
-        auto emit = [&](int u, const float (&xo)[RG], float vso, int pbuf) {
-          uint32_t tw[3][RG / 4];
+        // ---- probabilities (f16) of a tile's 8 rows for token t, the row sums
+        // (first: after the rescale by alpha), and the P' words tw = 3 e4m3
+        // terms of 256 p (times the token's V scale, f16, with per-token scales)
+        auto split = [&](const float (&xo)[RG], uint32_t vs16, bool first, uint32_t (&tw)[3][RG / 4]) {
 #pragma unroll
           for (int k = 0; k < RG / 2; ++k) {
-            float pa0, pa1;
-            if constexpr (EXT) {
-              pa0 = xo[2 * k] == -INFINITY ? 0.f : ex2(xo[2 * k] - m[2 * k]);
-              pa1 = xo[2 * k + 1] == -INFINITY ? 0.f : ex2(xo[2 * k + 1] - m[2 * k + 1]);
-            } else {
-              pa0 = ex2(xo[2 * k] - m[2 * k]);
-              pa1 = ex2(xo[2 * k + 1] - m[2 * k + 1]);
-            }
-            const uint32_t p16 = f32x2_to_f16x2(pa0, pa1);
-            if (u == 0) {
+            const uint32_t p16 = f32x2_to_f16x2(ex2(xo[2 * k] - m[2 * k]), ex2(xo[2 * k + 1] - m[2 * k + 1]));
+            if (first) {
               l[2 * k] = fmaf(l[2 * k], alpha[2 * k], f16_lo_to_f32(p16));
               l[2 * k + 1] = fmaf(l[2 * k + 1], alpha[2 * k + 1], f16_hi_to_f32(p16));
             } else {
               l[2 * k] += f16_lo_to_f32(p16);
               l[2 * k + 1] += f16_hi_to_f32(p16);
             }
-            // the PV operand: p, times the token's V scale with per-token scales
-            const uint32_t pv16 = per_token ? f32x2_to_f16x2(pa0 * vso, pa1 * vso) : p16;
+            const uint32_t pv16 = per_token ? hmul2(p16, vs16) : p16;
             uint32_t h = hmul2(pv16, 0x5C005C00u);                     // x 256
             const uint32_t e0 = f16x2_to_e4m3x2(h);
             h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e0)), 0x4C004C00u);   // residual x 16
@@ -441,64 +441,62 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e1)), 0x4C004C00u);
             const uint32_t e2 = f16x2_to_e4m3x2(h);
             if (k & 1) {
-              tw[0][k >> 1] |= e0 << 16;
-              tw[1][k >> 1] |= e1 << 16;
-              tw[2][k >> 1] |= e2 << 16;
+              tw[0][k >> 1] = prmt(tw[0][k >> 1], e0, 0x5410u);
+              tw[1][k >> 1] = prmt(tw[1][k >> 1], e1, 0x5410u);
+              tw[2][k >> 1] = prmt(tw[2][k >> 1], e2, 0x5410u);
             } else {
               tw[0][k >> 1] = e0;
               tw[1][k >> 1] = e1;
               tw[2][k >> 1] = e2;
             }
           }
-          {
-            // columns slot * 8 + row of the group's 32: terms 0, 1 | term 2, zero slot
-            const uint32_t pb = ptok + pbuf * S::pBytes;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(tw[0][0]), "r"(tw[0][1]),
-                         "r"(tw[1][0]), "r"(tw[1][1]) : "memory");
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(tw[2][0]), "r"(tw[2][1]),
-                         "r"(0u), "r"(0u) : "memory");
-          }
-          if (RS && threadIdx.x == 0) {
-            // the PV warp's orders for this P' buffer: O buffer, accumulate, commit O
+        };
+        // columns slot * 8 + row of the group's 32: terms 0, 1 | term 2, zero slot
+        auto store_p = [&](const uint32_t (&tw)[3][RG / 4], uint32_t pb) {
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(tw[0][0]), "r"(tw[0][1]),
+                       "r"(tw[1][0]), "r"(tw[1][1]) : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(tw[2][0]), "r"(tw[2][1]),
+                       "r"(0u), "r"(0u) : "memory");
+        };
+        // the PV warp's orders for P' buffer pbuf (16 rows): O buffer, accumulate, commit O
+        auto order = [&](int pbuf, int u) {
+          if (threadIdx.x == 0) {
             const uint32_t d = uint32_t(ob) | (uint32_t(u) << 1) | (uint32_t(u == np - 1) << 2);
             asm volatile("st.shared.u32 [%0], %1;" ::"r"(pd_s + 4 * pbuf), "r"(d) : "memory");
           }
-          if constexpr (PK) {
-            // the B half: the same for token start + TILE + t, its columns after A's
-            uint32_t twB[3][RG / 4];
-#pragma unroll
-            for (int k = 0; k < RG / 2; ++k) {
-              const uint32_t p16 = f32x2_to_f16x2(ex2(xB[2 * k] - m[2 * k]), ex2(xB[2 * k + 1] - m[2 * k + 1]));
-              l[2 * k] += f16_lo_to_f32(p16);
-              l[2 * k + 1] += f16_hi_to_f32(p16);
-              uint32_t h = hmul2(p16, 0x5C005C00u);
-              const uint32_t e0 = f16x2_to_e4m3x2(h);
-              h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e0)), 0x4C004C00u);
-              const uint32_t e1 = f16x2_to_e4m3x2(h);
-              h = hmul2(hsub2(h, e4m3x2_lo_to_f16x2(e1)), 0x4C004C00u);
-              const uint32_t e2 = f16x2_to_e4m3x2(h);
-              if (k & 1) {
-                twB[0][k >> 1] |= e0 << 16;
-                twB[1][k >> 1] |= e1 << 16;
-                twB[2][k >> 1] |= e2 << 16;
-              } else {
-                twB[0][k >> 1] = e0;
-                twB[1][k >> 1] = e1;
-                twB[2][k >> 1] = e2;
-              }
-            }
-            const uint32_t pb = ptok + pbuf * S::pBytes + 256;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb), "r"(twB[0][0]), "r"(twB[0][1]),
-                         "r"(twB[1][0]), "r"(twB[1][1]) : "memory");
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + 128), "r"(twB[2][0]), "r"(twB[2][1]),
-                         "r"(0u), "r"(0u) : "memory");
-          }
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&pfull[pbuf]);
         };
-        emit(0, x0, vs0, RS ? j & 3 : ob);
-        if (RS && np > 1) emit(1, x1, vs1, (j + 1) & 3);
+        {
+          uint32_t tw0[3][RG / 4];
+          split(x0, per_token ? f32x2_to_f16x2(vs0, vs0) : 0u, true, tw0);
+          if (RS && np > 1) {
+            // both tiles' words at once (independent chains), one proxy fence
+            uint32_t tw1[3][RG / 4];
+            split(x1, per_token ? f32x2_to_f16x2(vs1, vs1) : 0u, false, tw1);
+            store_p(tw0, ptok + (j & 3) * S::pBytes);
+            store_p(tw1, ptok + ((j + 1) & 3) * S::pBytes);
+            order(j & 3, 0);
+            order((j + 1) & 3, 1);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&pfull[j & 3]);
+              mbar_arrive(&pfull[(j + 1) & 3]);
+            }
+          } else {
+            const int pbuf = RS ? j & 3 : ob;
+            store_p(tw0, ptok + pbuf * S::pBytes);
+            if (RS) order(pbuf, 0);
+            if constexpr (PK) {
+              // the B half: the same for token start + TILE + t, its columns after A's
+              uint32_t twB[3][RG / 4];
+              split(xB, 0u, false, twB);
+              store_p(twB, ptok + pbuf * S::pBytes + 256);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pfull[pbuf]);
+          }
+        }
         // ---- fold this group's previous O (relative to the previous maxima,
         // so times alpha) while the tensor core computes this pass's
         if (pend_ob >= 0 && !fold(alpha)) { ok = false; break; }
@@ -577,12 +575,12 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         for (int r = 0; r < RG; ++r) {
           float mt = mg[0][r], lt = lsum[0][r], ot = o[r];
           if constexpr (!RS) {
-            // (each group's maximum is -inf only if it saw no token of the item)
+            // (a group that saw no token of the item kept kNoMax: its factor is 0
+            // next to the other's maximum, 1 with l = 0 when neither saw one)
             const float other = ldsf(stg_s + 4 * ((qb * RG + r) * D + t));
             const float m_me = mg[0][r], m_ot = mg[1][r];
             mt = fmaxf(m_me, m_ot);
-            const float a0 = (EXT && m_me == -INFINITY) ? 0.f : ex2(m_me - mt);
-            const float a1 = (EXT && m_ot == -INFINITY) ? 0.f : ex2(m_ot - mt);
+            const float a0 = ex2(m_me - mt), a1 = ex2(m_ot - mt);
             lt = lsum[0][r] * a0 + lsum[1][r] * a1;
             ot = o[r] * a0 + other * a1;
           }
@@ -597,7 +595,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           }
         }
         if (t < RG && RG * rblk + t < rows_here) {
-          p.part_m[row0 + RG * rblk + t] = mt_mine * kLn2;
+          // (EXT: a row that saw no token has l = 0 and no maximum)
+          p.part_m[row0 + RG * rblk + t] = lt_mine == 0.f ? -INFINITY : mt_mine * kLn2;
           p.part_l[row0 + RG * rblk + t] = lt_mine;
         }
         if (!RS) {
@@ -684,11 +683,11 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       // T <= Tmax tile groups then meets at most P of them
       const int den = max(1, P - 2);
       const long long rreq = (Tmax + den - 1) / den;
-      NGe = max(1LL, min((long long)NG, W / rreq));
+      NGe = max(1LL, min((long long)NG, div_nonneg(W, rreq)));
     }
     const bool active = W > 0 && g < NGe;
-    const long long rs = active ? W * g / NGe : 0, re = active ? W * (g + 1) / NGe : 0;
-    auto range_of = [&](long long x) -> long long { return ((x + 1) * NGe + W - 1) / W - 1; };
+    const long long rs = active ? div_nonneg(W * g, NGe) : 0, re = active ? div_nonneg(W * (g + 1), NGe) : 0;
+    auto range_of = [&](long long x) -> long long { return div_nonneg((x + 1) * NGe + W - 1, W) - 1; };
 
     // first sequence of the range: P >= 2, the one holding tile group rs;
     // P = 1, the first one starting at or after rs
@@ -1017,7 +1016,9 @@ pa_fp8_partition_kernel(const Fp8Params p) {
         const int total = *qk_total;
         if (total >= 0 && jj >= total) break;
         const int pb = jj & 3;
-        if (mbar_test_wait(&pfull[pb], (jj >> 2) & 1)) {
+        // (try_wait: the thread sleeps in the barrier instead of spinning on
+        // the issue slots of its sub-partition's softmax warps)
+        if (mbar_try_wait(&pfull[pb], (jj >> 2) & 1)) {
           tc_fence_after();
           const uint32_t d = lds32(pd_s + 4 * pb);
           const uint32_t ob = d & 1u, acc = (d >> 1) & 1u;
