@@ -221,9 +221,11 @@ int pa_decode_fp8_ext(const void* q, const uint8_t* kv_cache, const int32_t* blo
  *   bytes 136..263  V codes (same nibble order)
  *   bytes 264..271  V scales (e4m3fn), one per 32 dims
  * Q is rotated inside the partition kernel and the output is rotated back in
- * the combine kernel. Partition p owns the 256-token tile groups p, p+P,
- * p+2P, ... ([UQ] step F); L = 0 gives 0. The kernel splits each partition's
- * 32-token slices over J warps (J = 1, 2, 4 or 8, fixed by num_kv_heads and
+ * the combine kernel. Partition p owns the 32-token slices p, p+P, p+2P, ...
+ * of each sequence ([UQ] step F strides 256-token tile groups; the finer
+ * granule keeps partitions within one slice of each other, and the combined
+ * output does not depend on the split); L = 0 gives 0. The kernel splits each
+ * partition's slices over J warps (J = 1, 2, 4 or 8, fixed by num_kv_heads and
  * query_group), each of which keeps its own softmax state, so the workspace
  * holds P*J partial slots per (sequence, KV head): float32
  * O [num_seqs][num_kv_heads][P*J][query_group][256] (rotated domain,

@@ -8,8 +8,9 @@
 //    -- builder docstring and STEP F offsets;
 //  * in-kernel Walsh-Hadamard rotation of Q, q_r = q H / 16 (STEP B'), and
 //    attention in the rotated domain with softmax scale 1/sqrt(256);
-//  * tile groups of 256 tokens strided over partitions (STEP F), softmax
-//    partials (O, m, l) per (seq, kv_head, partition) (STEP G);
+//  * a split of each sequence over partitions (STEP F strides 256-token tile
+//    groups; here the stride granule is the 32-token slice, see below),
+//    softmax partials (O, m, l) per (seq, kv_head, partition) (STEP G);
 //  * the combine merges partitions and rotates the output back (o = o_r H/16).
 // Readings: the group scales are e4m3 and V decodes through a 16-entry fp32
 // centroid table (V = centroid[code] * scale); the page's own V convert
@@ -23,7 +24,10 @@
 // slices of a group of HG KV heads into a ring of shared-memory stages,
 // alternate stages each (one tensor-map box of 32 token rows x 272 bytes per
 // head, completion counted on the stage's mbarrier), and eight consumer warps
-// compute. A work item is (sequence, head group, partition); consumer warp w
+// compute. A work item is (sequence, head group, partition p), p owning the
+// slices p, p+P, ... of the sequence (a sequence of 75000 tokens has 293
+// tile groups, which no partition count divides evenly: strided slices keep
+// the partitions within one slice of each other); consumer warp w
 // owns one (head of the group, 8-row half of the query group) and every J-th
 // slice of the item (J = 8 / (HG x halves)), keeps its own softmax state and
 // writes it as its own partial slot, so the combine merges P x J slots per
@@ -54,7 +58,6 @@ namespace qpa {
 
 namespace uq {
 constexpr int D = 256;
-constexpr int TG = 256;
 constexpr int SLICE = 32;                        // tokens per stage: two 16-token MMA tiles
 constexpr int NC = 8;                            // consumer warps
 constexpr int NPW = 2;                           // producer warps (alternate stages)
@@ -102,14 +105,10 @@ __device__ __forceinline__ float e2m1_value(int k) {
   return (k & 8) ? -mag[k & 7] : mag[k & 7];
 }
 
-// Number of 32-token slices of partition p (tile groups p, p+P, ... below L).
+// Number of 32-token slices of partition p (slices p, p+P, ... below L).
 __device__ __forceinline__ int uq_slices(int L, int p, int P) {
-  const int ntg = (L + uq::TG - 1) / uq::TG;
-  if (p >= ntg) return 0;
-  const int n = (ntg - 1 - p) / P + 1;
-  const int last = p + (n - 1) * P;
-  const int tail = min(uq::TG, L - last * uq::TG);   // tokens of the partition's last tile group
-  return (n - 1) * (uq::TG / uq::SLICE) + (tail + uq::SLICE - 1) / uq::SLICE;
+  const int ns = (L + uq::SLICE - 1) / uq::SLICE;
+  return p < ns ? (ns - 1 - p) / P + 1 : 0;
 }
 
 // Largest byte of the eight in w (lo, hi).
@@ -152,40 +151,13 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
     fence_mbar_init();
   }
   if (threadIdx.x == NC * 32) prefetch_tmap(&kv_map);
-
-  // ---- centroid table: the e2m1 table takes the cvt path, anything else the
-  // shared-memory pair table of the centroids divided by 2^cexp (|c| < 1, so
-  // no f16 product with a scale overflows); the output is multiplied back.
-  bool e2m1_table = true;
-  int cexp = 0;
-  {
-    float cv[16];
-    float cmax = 0.f;
-    bool finite = true;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      cv[k] = __ldg(p.centroids + k);
-      e2m1_table = e2m1_table && (cv[k] == e2m1_value(k)) && (__float_as_uint(cv[k]) >> 31) == (uint32_t)(k >> 3);
-      finite = finite && isfinite(cv[k]);
-      cmax = fmaxf(cmax, fabsf(cv[k]));
-    }
-    if (!finite && threadIdx.x == 0) atomicExch(&g_kernel_error, KERR_RANGE);
-    if (!e2m1_table) {
-      if (cmax > 0.f && finite) frexpf(cmax, &cexp);
-      uint32_t* t = reinterpret_cast<uint32_t*>(lut_p);
-      for (int i = threadIdx.x; i < 256 * LUT_COPIES; i += THREADS) {
-        const int e = i / LUT_COPIES;
-        t[i] = f32x2_to_f16x2(ldexpf(cv[e & 15], -cexp), ldexpf(cv[e >> 4], -cexp));
-      }
-    }
-  }
-  __syncthreads();
-
   const int P = p.num_partitions;
   const int NHG = p.num_kv_heads / p.hg;
   const int num_items = p.num_seqs * NHG * P;
   const int bs = p.block_size;
   const int lbs = p.log2_bs;
+  __syncthreads();   // the barriers are initialised
+
   const uint32_t ring = smem_u32(smem);
   auto item_len = [&](int item) -> int {
     const int seq = item / (NHG * P);
@@ -210,17 +182,28 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
       const int rem = item % (NHG * P);
       const int part = rem / NHG, hgi = rem % NHG;
       const int L = item_len(item);
+      const int32_t* bt = p.block_table + (long long)seq * p.max_blocks;
+      // the table entries of slice k's first (and, block size 16, second) box:
+      // they depend on the slice alone, so they are read while the sequence
+      // length is still on its way, and masked by it afterwards
+      auto entries = [&](int k, int& ra, int& rb) {
+        const int t0 = (part + P * k) * SLICE;
+        const int ea = t0 >> lbs, eb = (t0 + 16) >> lbs;
+        ra = ea < p.max_blocks ? __ldg(bt + ea) : 0;
+        rb = two_boxes && eb < p.max_blocks ? __ldg(bt + eb) : 0;
+      };
+      int ra, rb, rna, rnb;
+      entries(lane, ra, rb);
+      entries(32 + lane, rna, rnb);
       const int nsl = uq_slices(L, part, P);
       if (nsl == 0) continue;
-      const int32_t* bt = p.block_table + (long long)seq * p.max_blocks;
-      // token-row coordinates of slice k's first box (and second box, block size 16)
-      auto coords = [&](int k, int& za, int& zb) {
+      // token-row coordinates of slice k's first (and second) box from its entries
+      auto coords = [&](int k, int ra, int rb, int& za, int& zb) {
         za = 0;
         zb = 0;
         if (k >= nsl) return;
-        const int t0 = (part + P * (k >> 3)) * TG + SLICE * (k & 7);
-        const int ea = t0 >> lbs;
-        int pa = (ea << lbs) < L ? __ldg(bt + ea) : 0;
+        const int t0 = (part + P * k) * SLICE;
+        int pa = ((t0 >> lbs) << lbs) < L ? ra : 0;
         if (pa < 0 || pa >= p.num_blocks) {
           atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
           pa = 0;
@@ -228,8 +211,7 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
         if (!two_boxes) {
           za = pa * bs + (t0 & (bs - 1));
         } else {
-          const int eb = (t0 + 16) >> lbs;
-          int pb = (eb << lbs) < L ? __ldg(bt + eb) : 0;
+          int pb = (((t0 + 16) >> lbs) << lbs) < L ? rb : 0;
           if (pb < 0 || pb >= p.num_blocks) {
             atomicExch(&g_kernel_error, KERR_BAD_BLOCK);
             pb = 0;
@@ -239,8 +221,8 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
         }
       };
       int za, zb, na, nb;
-      coords(lane, za, zb);
-      coords(32 + lane, na, nb);
+      coords(lane, ra, rb, za, zb);
+      coords(32 + lane, rna, rnb, na, nb);
       int chunk = 0;
       const uint32_t head0 = hgi * p.hg;
       // this warp's slices: stage g + k with (g + k) % NPW == pw
@@ -249,7 +231,8 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
           chunk = k >> 5;
           za = na;
           zb = nb;
-          coords(32 * (chunk + 1) + lane, na, nb);
+          entries(32 * (chunk + 1) + lane, rna, rnb);
+          coords(32 * (chunk + 1) + lane, rna, rnb, na, nb);
         }
         const int ya = __shfl_sync(0xffffffffu, za, k & 31);
         const int yb = __shfl_sync(0xffffffffu, zb, k & 31);
@@ -282,6 +265,35 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
   }
 
   // ================================================================== consumers
+  // ---- centroid table (consumer warps: the producers started streaming
+  // without it): the e2m1 table takes the cvt path, anything else the
+  // shared-memory pair table of the centroids divided by 2^cexp (|c| < 1, so
+  // no f16 product with a scale overflows); the output is multiplied back.
+  bool e2m1_table = true;
+  int cexp = 0;
+  {
+    float cv[16];
+    float cmax = 0.f;
+    bool finite = true;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      cv[k] = __ldg(p.centroids + k);
+      e2m1_table = e2m1_table && (cv[k] == e2m1_value(k)) && (__float_as_uint(cv[k]) >> 31) == (uint32_t)(k >> 3);
+      finite = finite && isfinite(cv[k]);
+      cmax = fmaxf(cmax, fabsf(cv[k]));
+    }
+    if (!finite && threadIdx.x == 0) atomicExch(&g_kernel_error, KERR_RANGE);
+    if (!e2m1_table) {
+      if (cmax > 0.f && finite) frexpf(cmax, &cexp);
+      uint32_t* t = reinterpret_cast<uint32_t*>(lut_p);
+      for (int i = threadIdx.x; i < 256 * LUT_COPIES; i += NC * 32) {
+        const int e = i / LUT_COPIES;
+        t[i] = f32x2_to_f16x2(ldexpf(cv[e & 15], -cexp), ldexpf(cv[e >> 4], -cexp));
+      }
+    }
+  }
+  named_barrier(1, NC * 32);   // the table is built (the consumer warps alone)
+
   const int cw = warp % C, jr = warp / C;
   const int hh = cw / p.nh, hf = cw % p.nh;
   const int g = lane >> 2;
@@ -415,7 +427,7 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
         break;
       }
       const uint32_t slot = ring + s * stage_bytes + hh * HEAD_SLICE;
-      const int t0 = (part + P * (k >> 3)) * TG + SLICE * (k & 7);
+      const int t0 = (part + P * k) * SLICE;
       const bool partial = t0 + SLICE > L;
 
       // ---- S^T (16 tokens x 8 rows) = K q_r^T per tile, one 32-dim scale
