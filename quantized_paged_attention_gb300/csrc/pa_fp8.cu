@@ -41,9 +41,13 @@
 //    fold each O buffer into per-dim register accumulators with the softmax
 //    rescale.
 // Exactness: the query (bf16) and the probabilities (f16) enter the fp8 MMA
-// as sums of e4m3 terms with power-of-two weights -- 4 terms for q (exact for
-// bf16 inputs), 3 terms for p (exact for its f16 value) -- so the tensor core
-// sees K and V unconverted and the products carry no fp8 rounding of q or p.
+// as sums of e4m3 terms with power-of-two weights -- 3 terms for p (exact for
+// its f16 value); 4 terms for q, and 2 with 16 rows: a row scaled to max |q|
+// in [128, 256) is then exact in every element of magnitude >= 2^-6 (down to
+// 2^-14 of the row maximum), the others within 2^-14, i.e. 2^-21 of the row
+// maximum (the 4 terms move that bound 2^-8 lower) -- so the tensor core sees
+// K and V unconverted and the products carry no fp8 rounding of q or p above
+// those bounds.
 // Every wait has a time limit; a timeout raises the error word and all roles
 // leave through the common teardown.
 #include "qpa.h"
@@ -76,7 +80,9 @@ struct Smem {
   static constexpr int R = 8 * NT;                 // query rows (padded)
   static constexpr int NQ = 32 * NT;               // 4 term slots x R rows
   static constexpr int NQS = PK ? 2 * NQ : NQ;     // MMA N: NQ per half
-  static constexpr int qBytes = NQS * D;           // Q' [NQS rows][128 dims] e4m3
+  static constexpr int QT = NT == 2 ? 2 : 4;       // e4m3 terms of the query (16 rows: 2)
+  static constexpr int NQK = NT == 2 ? 8 * QT * NT : NQS;   // QK N: QT terms x R rows (per half)
+  static constexpr int qBytes = NQK * D;           // Q' [NQK rows][128 dims] e4m3
   static constexpr int pBytes = TILE * NQS;        // P'^T [128 tokens][NQS] e4m3
   static constexpr int ringOff = 0;
   static constexpr int qOff = NS * TILE_BYTES;
@@ -94,7 +100,7 @@ struct Smem {
   static constexpr int miscOff = barOff + NBAR * 8;        // tmem base, abort flag, QK total
   static constexpr int total = miscOff + 16 + 1024;        // + alignment slack
   static_assert(total <= 227 * 1024, "shared memory");
-  static constexpr int TMEM_COLS = (NT == 1 && !PK) ? 256 : 512;   // S[2] then O[4] (6 NQS columns)
+  static constexpr int TMEM_COLS = (NT == 1 && !PK) ? 256 : 512;   // S[2] (NQK columns) then O[4] (NQS)
 };
 }  // namespace fp8
 
@@ -137,10 +143,10 @@ pa_fp8_partition_kernel(const Fp8Params p) {
   constexpr bool PK = HD == 64 && NT == 1 && !EXT;   // two 128-token halves per ring slot
   constexpr bool RS = NT == 2;                        // 16 rows: row split, two tiles per softmax pass
   using S = Smem<NT, EXT, PK>;
-  constexpr int R = S::R, NQ = S::NQ, NQS = S::NQS, NWG = S::NWG;
+  constexpr int R = S::R, NQ = S::NQ, NQS = S::NQS, NQK = S::NQK, QT = S::QT, NWG = S::NWG;
   constexpr int PD = PK ? 2 * HD : HD;                // floats per partial O row
   constexpr int WARP_PROD0 = S::WARP_PROD0, WARP_MMA = S::WARP_MMA;
-  constexpr uint32_t IDESC_QK = idesc_e4m3(128, NQS, false, false);
+  constexpr uint32_t IDESC_QK = idesc_e4m3(128, NQK, false, false);
   constexpr uint32_t IDESC_PV = idesc_e4m3(128, NQS, true, true);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -267,7 +273,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
       tc_fence_after();
       float w[32];
       // (PK: lanes 64..127, the B half's dims, read the B columns)
-      tmem_ld32(tl + 2 * NQS + pend_ob * NQS + 32 * rblk + (PK && wq >= 2 ? NQ : 0), w);
+      tmem_ld32(tl + 2 * NQK + pend_ob * NQS + 32 * rblk + (PK && wq >= 2 ? NQ : 0), w);
       tmem_wait_ld();
       tc_fence_before();
 #pragma unroll
@@ -332,10 +338,11 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           const int start = PK ? (tg0 + iu) * TG : (tg0 + (iu >> 1)) * TG + (iu & 1) * TILE;
           if (!warp_wait(&sfull[b], (ju >> 1) & 1, abort_flag, KERR_TIMEOUT_FULL)) return false;
           tc_fence_after();
-          float v[32];
+          float v[QT * RG];                  // the row block's S columns: term slot x row
           float vB[PK ? 32 : 1];
-          tmem_ld32(tl + b * NQS + 32 * rblk, v);
-          if constexpr (PK) tmem_ld32(tl + b * NQS + NQ, vB);
+          if constexpr (QT == 2) tmem_ld16(tl + b * NQK + 16 * rblk, v);
+          else tmem_ld32(tl + b * NQK + 32 * rblk, v);
+          if constexpr (PK) tmem_ld32(tl + b * NQK + NQ, vB);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
@@ -356,14 +363,18 @@ pa_fp8_partition_kernel(const Fp8Params p) {
               for (int r = 0; r < RG; ++r) cs[r] *= ks_t;
             }
           }
+          // the query terms' dot products, T1 + T2/16 (+ T3/256 + T4/4096)
+          auto sv_of = [&](int r) -> float {
+            if constexpr (QT == 2) return fmaf(v[RG + r], 0.0625f, v[r]);
+            else return fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
+          };
           if (whole) {
 #pragma unroll
-            for (int r = 0; r < RG; ++r)
-              xo[r] = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]) * cs[r];
+            for (int r = 0; r < RG; ++r) xo[r] = sv_of(r) * cs[r];
           } else {
 #pragma unroll
             for (int r = 0; r < RG; ++r) {
-              const float sv = fmaf(fmaf(fmaf(v[3 * RG + r], 0.0625f, v[2 * RG + r]), 0.0625f, v[RG + r]), 0.0625f, v[r]);
+              const float sv = sv_of(r);
               // (EXT: the row's causal bound, which implies start + t < L)
               xo[r] = (EXT ? start + t < vis[r] : valid) ? sv * cs[r] : -INFINITY;
             }
@@ -869,7 +880,8 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           ok = false;
           break;
         }
-        // ---- query operand: 4 e4m3 terms of q 2^a (a per row: max |q| 2^a in [128, 256))
+        // ---- query operand: QT e4m3 terms of q 2^a (a per row: max |q| 2^a in [128, 256)),
+        // each the rounding of the previous residual times 16 (QT = 4; 2 with 16 rows)
         const int qb = qcnt & 1;
         if (qcnt >= 2 && !warp_wait(&qempty[qb], ((qcnt >> 1) - 1) & 1, abort_flag, KERR_TIMEOUT_EMPTY)) {
           ok = false;
@@ -901,18 +913,18 @@ pa_fp8_partition_kernel(const Fp8Params p) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) x[k] *= up;
 #pragma unroll
-          for (int term = 0; term < 4; ++term) {
+          for (int term = 0; term < QT; ++term) {
             uint32_t e[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               e[k] = f32x2_to_e4m3x2(x[2 * k], x[2 * k + 1]);
-              if (term < 3) {
+              if (term < QT - 1) {
                 const uint32_t back = e4m3x2_lo_to_f16x2(e[k]);
                 x[2 * k] = (x[2 * k] - f16_lo_to_f32(back)) * 16.f;
                 x[2 * k + 1] = (x[2 * k + 1] - f16_hi_to_f32(back)) * 16.f;
               }
             }
-            const int rr = (row >> 3) * 32 + term * 8 + (row & 7);   // S / P' column layout
+            const int rr = (row >> 3) * (8 * QT) + term * 8 + (row & 7);   // S column layout (row block, term, row)
             const uint32_t addr = qsm + qb * S::qBytes + rr * D + (((h16 >> 1) ^ (rr & 7)) << 4) + 8 * (h16 & 1);
             if (h16 < HD / 8)
               asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(e[0] | (e[1] << 16)),
@@ -982,7 +994,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           const uint32_t ka = ring + s * TILE_BYTES;
 #pragma unroll
           for (int k = 0; k < (PK ? 4 : HD / 32); ++k)
-            mma_e4m3(tmem + b * NQS, umma_desc(ka + 32 * k, 16, 1024, kSwizzle128B),
+            mma_e4m3(tmem + b * NQK, umma_desc(ka + 32 * k, 16, 1024, kSwizzle128B),
                      umma_desc(qa + 32 * k, 16, 1024, kSwizzle128B), IDESC_QK, k);
           umma_commit(&sfull[b]);
           if (i == nt - 1) umma_commit(&qempty[qb]);
@@ -1026,7 +1038,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
           const uint32_t pa = psm + pb * S::pBytes;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_e4m3(tmem + 2 * NQS + ob * NQS, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
+            mma_e4m3(tmem + 2 * NQK + ob * NQS, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
                      umma_desc(pa + k * 32 * NQS, 8 * NQS, 128, kSwizzleNone), IDESC_PV, acc | uint32_t(k));
           umma_commit(&empty[jj % NS]);
           if (d & 4u) umma_commit(&ofull[ob]);
@@ -1059,7 +1071,7 @@ pa_fp8_partition_kernel(const Fp8Params p) {
             const uint32_t pa = psm + ob * S::pBytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_e4m3(tmem + 2 * NQS + ob * NQS, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
+              mma_e4m3(tmem + 2 * NQK + ob * NQS, umma_desc(va + 4096 * k, 16, 1024, kSwizzle128B),
                        umma_desc(pa + k * 32 * NQS, 8 * NQS, 128, kSwizzleNone), IDESC_PV, k);
             umma_commit(&ofull[ob]);
             umma_commit(&empty[jj % NS]);
