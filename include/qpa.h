@@ -79,6 +79,12 @@ int qpa_kernel_error(void* stream);
  * groups over the GPU's SMs, so a short sequence usually takes one slot and
  * a long one a few. Any P >= 1 gives the same result (up to rounding).
  * L = 0 gives 0.
+ * Precision: the K and V bytes enter the tensor core as they are; each query
+ * row, scaled by a power of two, enters as 4 e4m3 terms of its bf16 value (2
+ * terms when a KV head has more than 8 query rows), exact for every element
+ * down to 2^-22 (2 terms: 2^-14) of the row's largest |q| and within 2^-29
+ * (2^-21) of it below; the probabilities enter as the 3 exact e4m3 terms of
+ * their f16 value; products accumulate in f32.
  *
  * Layouts (row-major, element counts in brackets):
  *   q           bf16  [num_seqs][num_kv_heads*query_group][128] with the
