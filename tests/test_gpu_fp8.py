@@ -243,3 +243,20 @@ def test_head_dim_64_long_all_units():
     c = synth.make_fp8_case(960, [16384] * 16, 8, 8, head_dim=64, poison=False)
     out, _, _ = Fp8Dev(c).run(32)
     check_units(out.cpu().double().numpy(), fp8_reference(c), c, what="hd64 long")
+
+
+@pytest.mark.parametrize("qg", [8, 16])
+def test_query_rows_with_a_wide_dynamic_range(qg):
+    """Query rows with one outlier (+-64) and the other elements log-uniform
+    in 2^-24 .. 1 (massive-activation rows): the query enters as e4m3 terms (4
+    with up to 8 rows per KV head, 2 with 16), exact down to 2^-22 resp. 2^-14
+    of the row maximum; many elements fall below the 2-term bound, and the
+    result still matches the float64 oracle within the tolerance."""
+    c = synth.make_fp8_case(720 + qg, [300, 2049, 5000], 2, qg, 128, 16)
+    r = np.random.default_rng(720 + qg)
+    shape = c.q_bits.shape
+    q = np.where(r.random(shape) < 0.5, -1.0, 1.0) * 2.0 ** r.uniform(-24.0, 0.0, shape)
+    q[..., 0] = np.where(r.random(shape[:-1]) < 0.5, -64.0, 64.0)
+    c.q_bits = synth.round_to_bf16_bits(q.astype(np.float32))
+    out, _, _ = Fp8Dev(c).run(3)
+    _check(c, out.cpu().double().numpy(), what=f"wide-range q, group {qg}")
