@@ -220,19 +220,18 @@ uq_partition_kernel(const __grid_constant__ CUtensorMap kv_map, const UqParams p
           zb = pb * bs;
         }
       };
-      int za, zb, na, nb;
+      // the current chunk's coordinates; the next chunk's table entries are
+      // read one chunk ahead and turned into coordinates only when it starts
+      int za, zb;
       coords(lane, ra, rb, za, zb);
-      coords(32 + lane, rna, rnb, na, nb);
       int chunk = 0;
       const uint32_t head0 = hgi * p.hg;
       // this warp's slices: stage g + k with (g + k) % NPW == pw
       for (int k = (pw - g % NPW + NPW) % NPW; k < nsl; k += NPW) {
         if ((k >> 5) != chunk) {
           chunk = k >> 5;
-          za = na;
-          zb = nb;
+          coords(32 * chunk + lane, rna, rnb, za, zb);
           entries(32 * (chunk + 1) + lane, rna, rnb);
-          coords(32 * (chunk + 1) + lane, rna, rnb, na, nb);
         }
         const int ya = __shfl_sync(0xffffffffu, za, k & 31);
         const int yb = __shfl_sync(0xffffffffu, zb, k & 31);
