@@ -76,7 +76,9 @@ struct Smem {
   static constexpr int WARP_PROD0 = 4 * NWG;       // 4 copy warps
   static constexpr int WARP_MMA = WARP_PROD0 + 4;  // QK issuing warp, then the PV issuing warp
   static constexpr int THREADS = (WARP_MMA + 2) * 32;
-  static constexpr int NS = PK ? 4 : 5;            // ring slots (tiles, PK: tile groups)
+  // ring slots (tiles, PK: tile groups): as many as shared memory holds, since
+  // about two of them are always held by the MMAs and the softmax
+  static constexpr int NS = (NT == 1 && !EXT && !PK) ? 6 : 5;
   static constexpr int R = 8 * NT;                 // query rows (padded)
   static constexpr int NQ = 32 * NT;               // 4 term slots x R rows
   static constexpr int NQS = PK ? 2 * NQ : NQ;     // MMA N: NQ per half
