@@ -53,3 +53,23 @@ def test_reference_arm_runs_on_rank_zero_only():
                         "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_roofline_traffic_only_from_a_summary_of_the_current_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu summary only while its
+    recorded source hash matches the kernel source; otherwise it is null."""
+    sys.path.insert(0, ROOT)
+    import hashlib
+    import bench
+    t = bench._profiled_traffic()
+    cur = hashlib.sha256(open(bench.KERNEL_SRC, "rb").read()).hexdigest()
+    recorded = open(bench.PROFILE_SUMMARY).read()
+    if f"kernel_source_sha256: {cur}" in recorded:
+        # a full launch reads at least its algorithmic KV bytes
+        assert t is not None and t >= 16 * 16384 * 8 * 256
+    else:
+        assert t is None
+    changed = tmp_path / "pa_fp8.cu"
+    changed.write_bytes(open(bench.KERNEL_SRC, "rb").read() + b"\n")
+    monkeypatch.setattr(bench, "KERNEL_SRC", str(changed))
+    assert bench._profiled_traffic() is None
